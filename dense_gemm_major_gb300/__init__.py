@@ -1,0 +1,167 @@
+"""Python binding of the GB300 dense row-major GEMM library.
+
+The binding only marshals arguments: every step of the GEMM runs in the
+CUDA library ``libdense_gemm.so`` (built in-tree by ``_build.build()``),
+whose C ABI is declared in ``include/dense_gemm.h``.  The functions of the
+same names as the C entry points take integers (device addresses, sizes,
+a ``cudaStream_t`` value); ``matmul`` is a convenience wrapper for torch
+tensors on the current device and stream.  There is no fallback: if the
+library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdense_gemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_MISALIGNED = 2
+GEMM_ERR_UNSUPPORTED_DEVICE = 3
+GEMM_ERR_LAUNCH = 4
+GEMM_ERR_DEVICE_TIMEOUT = 5
+
+PATH_NOOP, PATH_ZERO_FILL, PATH_SIMT_TMA, PATH_SIMT_CPASYNC, PATH_TC_TMA = range(5)
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+
+# Every symbol include/dense_gemm.h declares.
+EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_device_check",
+            "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})" if what
+                         else f"{status_string(status)} (status {status})")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("block_m", ctypes.c_int), ("block_n", ctypes.c_int),
+                ("block_k", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built ({LIB_PATH} missing); "
+                           "run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    i, vp = ctypes.c_int, ctypes.c_void_p
+    gemm_args = [i, i, i, vp, i, vp, i, vp, i, vp]
+    for name in ("gemm_f32", "gemm_f16", "gemm_bf16"):
+        fn = getattr(lib, name)
+        fn.restype = i
+        fn.argtypes = gemm_args
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_status_string.argtypes = [i]
+    lib.gemm_device_check.restype = i
+    lib.gemm_device_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.gemm_plan.restype = i
+    lib.gemm_plan.argtypes = [i, i, i, i, vp, i, vp, i, vp, i, i, ctypes.POINTER(Plan)]
+    lib.gemm_smem_layout_offset.restype = i
+    lib.gemm_smem_layout_offset.argtypes = [i, i, i]
+    lib.gemm_selftest_timeout.restype = i
+    lib.gemm_selftest_timeout.argtypes = [ctypes.c_uint, vp]
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ C-ABI mirrors
+
+def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return load().gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return load().gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return load().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+gemm_status_string = status_string
+
+
+def gemm_device_check(stream=0):
+    """Returns (status, fault_bits)."""
+    bits = ctypes.c_uint(0)
+    st = load().gemm_device_check(stream, ctypes.byref(bits))
+    return st, bits.value
+
+
+def gemm_plan(dtype, M, N, K, A, lda, B, ldb, C, ldc, num_sms=152):
+    """Returns (status, Plan)."""
+    plan = Plan()
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = load().gemm_plan(code, M, N, K, A, lda, B, ldb, C, ldc, num_sms, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_smem_layout_offset(layout: int, row: int, col: int) -> int:
+    return load().gemm_smem_layout_offset(layout, row, col)
+
+
+def gemm_selftest_timeout(timeout_us: int, stream=0) -> int:
+    return load().gemm_selftest_timeout(timeout_us, stream)
+
+
+_ENTRY = {"f32": gemm_f32, "f16": gemm_f16, "bf16": gemm_bf16}
+
+
+def gemm(dtype: str, M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    return _ENTRY[dtype](M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+# ------------------------------------------------------------ torch wrapper
+
+def _torch_dtype_code(t):
+    import torch
+    return {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[t.dtype]
+
+
+def _ld(t, rows, cols):
+    if t.dim() != 2 or (cols > 1 and t.stride(1) != 1):
+        raise ValueError("operands must be 2-D row-major (unit column stride)")
+    return t.stride(0) if rows > 1 else max(cols, t.stride(0), 1)
+
+
+def matmul(A, B, out=None, stream=None):
+    """C = A @ B for row-major CUDA tensors of one dtype (float32, float16,
+    bfloat16), queued on ``stream`` (default: torch's current stream).
+    Row-padded views (row stride > width) are accepted for A, B and out."""
+    import torch
+    if A.device.type != "cuda" or B.device.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have the same dtype")
+    code = _torch_dtype_code(A)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    elif out.shape != (M, N) or out.dtype != A.dtype:
+        raise ValueError("out has the wrong shape or dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    st = gemm(code, M, N, K, A.data_ptr(), _ld(A, M, K), B.data_ptr(), _ld(B, K, N),
+              out.data_ptr(), _ld(out, M, N), stream)
+    if st != GEMM_OK:
+        raise GemmError(st, f"gemm_{code}")
+    return out

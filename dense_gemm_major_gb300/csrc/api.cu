@@ -1,0 +1,342 @@
+// C-ABI entry points: argument validation, path selection, TMA descriptor
+// encoding and launch.  See include/dense_gemm.h for the contract.
+//
+// The dispatcher plays the role of the pages' torch-extension binding macros
+// ("[CUDA 优化实战] sgemm - 超越 cuBLAS", section 1 binding_func_gen and section 2
+// binding_tiled_func_gen: read M, K, N, pick grid and block, launch on the
+// caller's stream), with plain pointers and sizes instead of tensors, and a
+// shape/alignment-driven choice of kernel path in the spirit of the library
+// launcher described in the GB300 GEMM roadmap (m.nxbn.cn, section 1.2).
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "dense_gemm.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace {
+
+// The device fault word: kernels OR a dgemm::FaultCode into it when a
+// bounded wait gives up.  One copy per device.
+__device__ unsigned g_fault_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sms = 0;
+  unsigned* fault = nullptr;  // device address of g_fault_word
+};
+
+std::mutex g_mu;
+DeviceInfo g_devices[kMaxDevices];
+
+unsigned long long wait_timeout_ns() {
+  static const unsigned long long v = [] {
+    unsigned long long ms = 2000;  // a bounded wait gives up after 2 s by default
+    if (const char* s = std::getenv("DENSE_GEMM_TIMEOUT_MS")) {
+      char* end = nullptr;
+      const unsigned long long x = std::strtoull(s, &end, 10);
+      if (end != s && x > 0) ms = x;
+    }
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+gemm_status_t current_device(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.probed) {
+    d.probed = true;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    // The kernels are built for sm_103a only.
+    d.supported = (prop.major == 10 && prop.minor == 3);
+    d.sms = prop.multiProcessorCount;
+    void* addr = nullptr;
+    if (d.supported && cudaGetSymbolAddress(&addr, g_fault_word) != cudaSuccess) {
+      cudaGetLastError();
+      d.supported = false;
+    }
+    d.fault = static_cast<unsigned*>(addr);
+  }
+  if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return GEMM_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D row-major tensor {inner, outer} with row pitch `pitch_bytes`.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bytes spanned by a rows x cols block with leading dimension ld.
+inline uint64_t span_bytes(long long rows, long long cols, long long ld, int es) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return (uint64_t)((rows - 1) * ld + cols) * (uint64_t)es;
+}
+
+inline bool overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
+  if (an == 0 || bn == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
+                        int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
+  if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+  std::memset(plan, 0, sizeof(*plan));
+  if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    plan->path = GEMM_PATH_NOOP;
+    return GEMM_OK;
+  }
+  const int es = dtype == 0 ? 4 : 2;
+  if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(C) % es) != 0) return GEMM_ERR_INVALID_ARG;
+  if (K == 0) {
+    plan->path = GEMM_PATH_ZERO_FILL;
+    plan->threads = 256;
+    return GEMM_OK;
+  }
+  if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (lda < K || ldb < N) return GEMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(A) % es) != 0 || (reinterpret_cast<uintptr_t>(B) % es) != 0)
+    return GEMM_ERR_INVALID_ARG;
+  const uint64_t cbytes = span_bytes(M, N, ldc, es);
+  if (overlap(A, span_bytes(M, K, lda, es), C, cbytes) ||
+      overlap(B, span_bytes(K, N, ldb, es), C, cbytes))
+    return GEMM_ERR_INVALID_ARG;
+
+  if (dtype == 0) {
+    const bool tma = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
+    plan->path = tma ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
+    plan->block_m = dgemm::kSgemmBM;
+    plan->block_n = dgemm::kSgemmBN;
+    plan->block_k = dgemm::kSgemmBK;
+    plan->stages = dgemm::kSgemmStages;
+    plan->threads = dgemm::kSgemmThreads;
+    plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::kSgemmBN);
+    plan->ctas = plan->tiles;
+    plan->smem_bytes = dgemm::kSgemmSmemBytes;
+    return GEMM_OK;
+  }
+  // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda % 8) || (ldb % 8) || (ldc % 8))
+    return GEMM_ERR_MISALIGNED;
+  plan->path = GEMM_PATH_TC_TMA;
+  plan->block_m = dgemm::kTcBM;
+  plan->block_n = dgemm::kTcBN;
+  plan->block_k = dgemm::kTcBK;
+  plan->stages = dgemm::kTcStages;
+  plan->threads = dgemm::kTcThreads;
+  plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
+  const int sms = num_sms > 0 ? num_sms : 1;
+  plan->ctas = plan->tiles < sms ? plan->tiles : sms;
+  plan->smem_bytes = dgemm::kTcSmemBytes;
+  return GEMM_OK;
+}
+
+gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const void* B, int ldb,
+                  void* C, int ldc, cudaStream_t stream) {
+  gemm_plan_t plan;
+  gemm_status_t st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, 0, &plan);
+  if (st != GEMM_OK) return st;
+  if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
+  DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  const int es = dtype == 0 ? 4 : 2;
+  cudaError_t e = cudaSuccess;
+
+  if (plan.path == GEMM_PATH_ZERO_FILL) {
+    e = dgemm::launch_zero_fill(C, M, N, ldc, es, stream);
+  } else if (dtype == 0) {
+    dgemm::SgemmParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.A = static_cast<const float*>(A);
+    p.lda = lda;
+    p.B = static_cast<const float*>(B);
+    p.ldb = ldb;
+    p.C = static_cast<float*>(C);
+    p.ldc = ldc;
+    p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
+    p.tiles_n = ceil_div(N, dgemm::kSgemmBN);
+    p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
+    p.fault = dev->fault;
+    p.timeout_ns = wait_timeout_ns();
+    const bool tma = plan.path == GEMM_PATH_SIMT_TMA;
+    alignas(64) CUtensorMap tmA, tmB;
+    if (tma) {
+      if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
+                     (uint64_t)lda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
+                     (uint64_t)ldb * 4, dgemm::kSgemmBN, dgemm::kSgemmBK,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GEMM_ERR_LAUNCH;
+    }
+    e = dgemm::launch_sgemm(p, tma, &tmA, &tmB, stream);
+  } else {
+    const CUtensorMapDataType dt =
+        dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    alignas(64) CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2, dgemm::kTcBK,
+                   dgemm::kTcBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb * 2, 64, dgemm::kTcBK,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, dt, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * 2, dgemm::kTcEpiCols,
+                   32, CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
+    dgemm::TcParams p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.tiles_m = ceil_div(M, dgemm::kTcBM);
+    p.tiles_n = ceil_div(N, dgemm::kTcBN);
+    p.fault = dev->fault;
+    p.timeout_ns = wait_timeout_ns();
+    const int grid = plan.tiles < dev->sms ? plan.tiles : dev->sms;
+    e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, grid, stream);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                       float* C, int ldc, cudaStream_t stream) {
+  return run(0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+gemm_status_t gemm_f16(int M, int N, int K, const gemm_half_t* A, int lda, const gemm_half_t* B,
+                       int ldb, gemm_half_t* C, int ldc, cudaStream_t stream) {
+  return run(1, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+gemm_status_t gemm_bf16(int M, int N, int K, const gemm_bfloat16_t* A, int lda,
+                        const gemm_bfloat16_t* B, int ldb, gemm_bfloat16_t* C, int ldc,
+                        cudaStream_t stream) {
+  return run(2, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+const char* gemm_status_string(gemm_status_t status) {
+  switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument (size, leading dimension, null or overlap)";
+    case GEMM_ERR_MISALIGNED: return "operand base or leading dimension not 16-byte aligned";
+    case GEMM_ERR_UNSUPPORTED_DEVICE: return "no current CUDA device of compute capability 10.3";
+    case GEMM_ERR_LAUNCH: return "kernel launch failed";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
+  }
+  return "unknown status";
+}
+
+gemm_status_t gemm_device_check(cudaStream_t stream, unsigned* fault_bits) {
+  if (fault_bits) *fault_bits = 0;
+  DeviceInfo* dev = nullptr;
+  gemm_status_t st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  unsigned v = 0;
+  if (cudaMemcpy(&v, dev->fault, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  if (fault_bits) *fault_bits = v;
+  if (v != 0) {
+    const unsigned zero = 0;
+    cudaMemcpy(dev->fault, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  }
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
+                        int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
+  return plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, num_sms, plan);
+}
+
+int gemm_smem_layout_offset(int layout, int row, int col) {
+  if (layout == 0) {
+    if (row < 0 || row >= dgemm::kSgemmBM || col < 0 || col >= dgemm::kSgemmBK) return -1;
+    return dgemm::sgemm_smem_offset(0, row, col);
+  }
+  if (layout == 1) {
+    if (row < 0 || row >= dgemm::kSgemmBK || col < 0 || col >= dgemm::kSgemmBN) return -1;
+    return dgemm::sgemm_smem_offset(1, row, col);
+  }
+  return -1;
+}
+
+gemm_status_t gemm_selftest_timeout(unsigned timeout_us, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  gemm_status_t st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (dgemm::launch_selftest_timeout(dev->fault, (unsigned long long)timeout_us * 1000ull,
+                                     stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,398 @@
+// FP16 / BF16 GEMM on sm_103a tensor cores: C = A . B, row-major, FP32
+// accumulation in tensor memory, FP16 / BF16 output rounded to nearest-even.
+//
+// The structure is the five-step flow of the GB300 GEMM roadmap (m.nxbn.cn,
+// section 4.2): TMA copies A and B tiles into shared memory; tcgen05.mma reads
+// them from shared memory and accumulates into tensor memory (TMEM); loading
+// of the next tiles continues meanwhile; after the K loop tcgen05.ld brings
+// the accumulator into registers; the epilogue writes C to global memory.
+// Section 4.1 of the same page: the MMA is issued asynchronously and the
+// issuing warp does not wait for it; section 3.1: a 3-4 stage shared-memory
+// ring overlaps loads with MMAs; section 1.1: the data supply, not the MMA
+// unit, is what limits a GEMM on this chip.
+//
+// GB300-specific choices (no page gives a tcgen05 kernel):
+//  * Persistent grid, at most one CTA per SM, static round-robin over
+//    128 x 256 output tiles in groups of 8 tile rows (L2 reuse).
+//  * Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator and MMA
+//    issuer (one thread issues every tcgen05.mma), warps 2-5 = epilogue (each
+//    owns the 32 TMEM lanes its warp index mod 4 may access).
+//  * Ring: 4 stages of A (128 x 64, K-major, 128-byte swizzle) and B (64 x 256,
+//    N-major, as four 64-column boxes, 128-byte swizzle); `full` mbarriers
+//    carry TMA transaction bytes, `empty` mbarriers are arrived by
+//    tcgen05.commit once the MMAs reading a stage are done.
+//  * Accumulator: two 128 x 256 FP32 buffers in TMEM (all 512 columns), so
+//    the epilogue of one tile overlaps the main loop of the next.
+//  * Epilogue: tcgen05.ld 32x32b -> FP32 registers -> RN conversion ->
+//    128-byte-swizzled shared staging (conflict-free) -> TMA store of 32 x 64
+//    boxes; TMA clips rows and columns beyond M and N.
+//  * Every mbarrier wait is bounded; a wait that gives up records a fault,
+//    stops this CTA's roles, drains its copies and MMAs and frees TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace dgemm {
+namespace {
+
+constexpr int BM = kTcBM;
+constexpr int BN = kTcBN;
+constexpr int BK = kTcBK;
+constexpr int S = kTcStages;
+constexpr int UMMA_K = 16;                         // K per tcgen05.mma (16-bit inputs)
+constexpr uint32_t kABytes = BM * BK * 2;          // 16 KB
+constexpr uint32_t kBBoxBytes = 64 * BK * 2;       // one 64-column box of B: 8 KB
+constexpr uint32_t kBBytes = BN * BK * 2;          // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kEpiBufBytes = 32 * kTcEpiCols * 2;   // 4 KB
+constexpr uint32_t kTmemCols = 2 * BN;             // two accumulators
+constexpr int kEpiWarps = 4;
+
+static_assert(BK * 2 == 128, "A rows of a stage are one 128-byte swizzle row");
+static_assert(kTcEpiCols * 2 == 128, "epilogue boxes are one 128-byte swizzle row wide");
+static_assert(kTmemCols == 512, "TMEM holds exactly two accumulators");
+
+struct alignas(8) Barriers {
+  uint64_t full[S];
+  uint64_t empty[S];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ------------------------------------------------------------ tcgen05 PTX
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16: FP32 accumulator, A and B of one
+// type (0 = FP16, 1 = BF16), A K-major, B N-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type) {
+  return (1u << 4)                 // D format: FP32
+         | (ab_type << 7)          // A format
+         | (ab_type << 10)         // B format
+         | (0u << 15)              // A major: K
+         | (1u << 16)              // B major: MN
+         | ((uint32_t)(BN >> 3) << 17)
+         | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on `bar` when all tcgen05 operations this thread issued so
+// far have completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
+  const int per_group = kTcGroupM * p.tiles_n;
+  const int group = t / per_group;
+  const int first_m = group * kTcGroupM;
+  const int gsize = min(p.tiles_m - first_m, kTcGroupM);
+  const int r = t - group * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcParams& p,
+                                          Barriers* bars, unsigned fault_code) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    ok = mbar_wait_bounded(bar, parity, p.timeout_ns, &bars->abort) ? 1 : 0;
+    if (!ok) {
+      // Only the role that timed out raises its code; roles that stop
+      // because another one gave up just follow.
+      if (!*(volatile int*)&bars->abort) raise_fault(p.fault, fault_code);
+      *(volatile int*)&bars->abort = 1;
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <typename T, uint32_t kAbType>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+  unsigned char* sA = reinterpret_cast<unsigned char*>(base);
+  unsigned char* sB = sA + S * kABytes;
+  unsigned char* sEpi = sB + S * kBBytes;
+  Barriers* bars = reinterpret_cast<Barriers*>(sEpi + kEpiWarps * 2 * kEpiBufBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int nk = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->acc_full[b]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  uint32_t issued = 0;   // producer: k-tiles issued (lane 0 of warp 0)
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      for (int kt = 0; kt < nk; ++kt, ++it) {
+        const uint32_t s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        ok = warp_wait(smem_u32(&bars->empty[s]), ph ^ 1u, p, bars, kFaultTcProducerWait);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&bars->full[s]);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(smem_u32(sA + s * kABytes), &tmA, fb, kt * BK, tm * BM);
+          const uint32_t bdst = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, tn * BN + j * 64, kt * BK);
+          issued = it + 1;
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = instr_desc(kAbType);
+    uint32_t it = 0;
+    int local = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+      const uint32_t b = local & 1;
+      const uint32_t aph = (local >> 1) & 1u;
+      ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + b * BN;
+      for (int kt = 0; kt < nk; ++kt, ++it) {
+        const uint32_t s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        ok = warp_wait(smem_u32(&bars->full[s]), ph, p, bars, kFaultTcMmaWait);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA + s * kABytes);
+          const uint32_t b0 = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // A: +32 bytes per 16 k inside the swizzled 128-byte rows;
+            //    8-row groups 1024 bytes apart.
+            // B: +16 rows (2048 bytes) per 16 k; 64-column blocks 8 KB apart
+            //    (leading offset), 8-row k groups 1024 bytes apart (stride).
+            const uint64_t ad = smem_desc(a0 + k * UMMA_K * 2, 16, 1024);
+            const uint64_t bd = smem_desc(b0 + k * UMMA_K * 128, kBBoxBytes, 1024);
+            mma_f16(d_tmem, ad, bd, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->empty[s]));   // frees the stage when the MMAs finish
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(smem_u32(&bars->acc_full[b]));   // accumulator ready
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;                    // TMEM lane quadrant of this warp
+    const int ew = warp - 2;                   // epilogue warp index 0..3
+    unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
+    int local = 0;
+    int nstore = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      int tm, tn;
+      tile_coords(t, p, tm, tn);
+      const uint32_t b = local & 1;
+      const uint32_t aph = (local >> 1) & 1u;
+      if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      for (int c = 0; c < BN / kTcEpiCols; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_row + c * kTcEpiCols, r0);
+        tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
+        tmem_ld_wait();
+        if (c == BN / kTcEpiCols - 1) {
+          // The accumulator buffer is free for the next tile's MMAs.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
+        }
+        unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
+        // The store issued from this buffer two boxes ago must have read it.
+        if (lane == 0) tma_store_wait_read<1>();
+        __syncwarp();
+        uint32_t* row = reinterpret_cast<uint32_t*>(buf + lane * 128);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 v;
+          const uint32_t* src = ch < 4 ? &r0[ch * 8] : &r1[(ch - 4) * 8];
+          v.x = pack2<T>(__uint_as_float(src[0]), __uint_as_float(src[1]));
+          v.y = pack2<T>(__uint_as_float(src[2]), __uint_as_float(src[3]));
+          v.z = pack2<T>(__uint_as_float(src[4]), __uint_as_float(src[5]));
+          v.w = pack2<T>(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
+                                    ((ch ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), tn * BN + c * kTcEpiCols, tm * BM + q * 32);
+          tma_store_commit();
+        }
+        ++nstore;
+      }
+    }
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && bars->abort) {
+    // Let this CTA's in-flight TMA loads land before the CTA exits.
+    const uint32_t first = issued > (uint32_t)S ? issued - S : 0;
+    for (uint32_t it = first; it < issued; ++it) {
+      if (!mbar_wait_bounded(smem_u32(&bars->full[it % S]), (it / S) & 1u, p.timeout_ns,
+                             nullptr)) {
+        raise_fault(p.fault, kFaultDrainWait);
+        break;
+      }
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    if (lane == 0) {
+      // Wait for every MMA this CTA issued before freeing TMEM.
+      mma_commit(smem_u32(&bars->drain));
+      if (!mbar_wait_bounded(smem_u32(&bars->drain), 0, p.timeout_ns, nullptr))
+        raise_fault(p.fault, kFaultDrainWait);
+    }
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <typename T, uint32_t kAb>
+cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                         const CUtensorMap* tmC, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, kAb>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<T, kAb><<<grid, kTcThreads, kTcSmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static_assert(sizeof(Barriers) <= 256, "barrier block must fit its reserved space");
+
+cudaError_t launch_gemm_tc(int dtype, const TcParams& p, const CUtensorMap* tmA,
+                           const CUtensorMap* tmB, const CUtensorMap* tmC, int grid,
+                           cudaStream_t stream) {
+  if (dtype == 1) return launch_typed<__half, 0>(p, tmA, tmB, tmC, grid, stream);
+  return launch_typed<__nv_bfloat16, 1>(p, tmA, tmB, tmC, grid, stream);
+}
+
+}  // namespace dgemm

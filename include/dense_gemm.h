@@ -1,0 +1,157 @@
+/*
+ * dense_gemm.h -- C ABI of the GB300 (sm_103a) dense row-major GEMM library.
+ *
+ *     C[M x N] = A[M x K] . B[K x N]
+ *
+ * The operation is the row-major product that every page on the subject
+ * starts from: "GEMM：从朴素实现到 shared memory tiling 与寄存器分块" (quant67.com)
+ * states it as its computation target (row-major C_{MxN} = A_{MxK} x B_{KxN},
+ * 2MNK floating-point operations), "[CUDA 优化实战] sgemm - 超越 cuBLAS"
+ * (wingedge777.com) section 1 computes one C element per thread by
+ * accumulating a[row*k+i] * b[i*n+col] along k, and the GB300 GEMM roadmap
+ * (m.nxbn.cn) section 4.2 lays out the tensor-core form: TMA stages A and B
+ * tiles in shared memory, tcgen05.mma accumulates into tensor memory, and
+ * tcgen05.ld brings the result back for the epilogue.  The leading-dimension
+ * arguments generalise the pages' dense layouts to row-padded ones.
+ *
+ * Conventions shared by every GEMM entry point:
+ *  - Element (i,k) of A is A[i*lda + k]; (k,j) of B is B[k*ldb + j]; (i,j) of
+ *    C is C[i*ldc + j].  Leading dimensions are in elements.
+ *  - Requirements: M, N, K >= 0; lda >= K and ldb >= N when K > 0 and the
+ *    operand is read; ldc >= N; A, B non-null when K > 0 and M, N > 0; C
+ *    non-null when M, N > 0.  C must not overlap A or B.
+ *  - M == 0 or N == 0: nothing is done and GEMM_OK is returned.  K == 0: C is
+ *    set to zero (the empty sum).
+ *  - C is overwritten (no alpha / beta); columns j >= N of padded C rows are
+ *    never written.
+ *  - Every pointer is caller-owned DEVICE memory of the current device.  The
+ *    library allocates no device memory per call and never synchronises: the
+ *    work is queued on `stream` and the call returns.
+ *  - Accumulation is FP32 in every type.  FP16 / BF16 results are rounded to
+ *    nearest-even once, from the FP32 accumulator.
+ *  - Errors: argument problems are reported synchronously, before anything
+ *    is queued.  A launch failure returns GEMM_ERR_LAUNCH.  A device-side
+ *    wait that gave up (GEMM_ERR_DEVICE_TIMEOUT) is only visible through
+ *    gemm_device_check().
+ */
+#ifndef DENSE_GEMM_H_
+#define DENSE_GEMM_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__cplusplus)
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+typedef __half gemm_half_t;
+typedef __nv_bfloat16 gemm_bfloat16_t;
+extern "C" {
+#else
+/* Storage-only views of the same 16-bit formats for C callers. */
+typedef struct { unsigned short bits; } gemm_half_t;     /* IEEE binary16 */
+typedef struct { unsigned short bits; } gemm_bfloat16_t; /* bfloat16      */
+#endif
+
+typedef enum gemm_status_t {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,        /* sizes, leading dimensions, nulls, overlap */
+  GEMM_ERR_MISALIGNED = 2,         /* FP16/BF16: base or ld not 16-byte aligned */
+  GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 / no device   */
+  GEMM_ERR_LAUNCH = 4,             /* the CUDA launch itself failed              */
+  GEMM_ERR_DEVICE_TIMEOUT = 5      /* a kernel's bounded wait gave up            */
+} gemm_status_t;
+
+/*
+ * FP32 GEMM on the FFMA pipes (no TF32): the SIMT kernel family of
+ * wingedge777 sections 2-6 (block tiling, 8x8 register outer product,
+ * swizzled shared memory, coalesced write-back, multi-stage pipeline),
+ * re-designed for sm_103a with a TMA-fed 3-stage ring.
+ * Any alignment is accepted: when a base pointer or lda/ldb is not 16-byte
+ * aligned the tiles are staged with 4-byte cp.async instead of TMA.
+ */
+gemm_status_t gemm_f32(int M, int N, int K,
+                       const float *A, int lda,
+                       const float *B, int ldb,
+                       float *C, int ldc,
+                       cudaStream_t stream);
+
+/*
+ * FP16 inputs and output, FP32 accumulation, on the 5th-generation tensor
+ * cores (tcgen05.mma into tensor memory, m.nxbn.cn sections 4.1-4.2).
+ * A, B and C must be 16-byte aligned and lda, ldb, ldc multiples of 8
+ * elements (TMA stride rule), else GEMM_ERR_MISALIGNED.
+ */
+gemm_status_t gemm_f16(int M, int N, int K,
+                       const gemm_half_t *A, int lda,
+                       const gemm_half_t *B, int ldb,
+                       gemm_half_t *C, int ldc,
+                       cudaStream_t stream);
+
+/* As gemm_f16 with bfloat16 inputs and output. */
+gemm_status_t gemm_bf16(int M, int N, int K,
+                        const gemm_bfloat16_t *A, int lda,
+                        const gemm_bfloat16_t *B, int ldb,
+                        gemm_bfloat16_t *C, int ldc,
+                        cudaStream_t stream);
+
+/* Static, never-null description of a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's fault
+ * word, which a kernel sets when one of its bounded waits gives up.
+ * Returns GEMM_ERR_DEVICE_TIMEOUT if it was set, GEMM_ERR_LAUNCH if the
+ * stream reports an error, else GEMM_OK.  *fault_bits (may be NULL)
+ * receives the raw fault bits.
+ */
+gemm_status_t gemm_device_check(cudaStream_t stream, unsigned *fault_bits);
+
+/*
+ * Host-side plan: which kernel path a call with these arguments would take.
+ * Pure host logic (no CUDA call); the dispatcher uses the same function.
+ * dtype: 0 = FP32, 1 = FP16, 2 = BF16.  Pointers are only inspected for
+ * alignment and overlap.  num_sms sizes persistent grids.
+ */
+enum {
+  GEMM_PATH_NOOP = 0,          /* M == 0 or N == 0                   */
+  GEMM_PATH_ZERO_FILL = 1,     /* K == 0: C := 0                     */
+  GEMM_PATH_SIMT_TMA = 2,      /* FP32 SIMT, TMA-staged tiles        */
+  GEMM_PATH_SIMT_CPASYNC = 3,  /* FP32 SIMT, 4-byte cp.async tiles   */
+  GEMM_PATH_TC_TMA = 4         /* FP16/BF16 tcgen05, TMA in and out  */
+};
+typedef struct gemm_plan_t {
+  int path;
+  int block_m, block_n, block_k, stages;
+  int threads;
+  int ctas;          /* grid size                         */
+  int tiles;         /* output tiles                      */
+  int smem_bytes;    /* dynamic shared memory per CTA     */
+} gemm_plan_t;
+gemm_status_t gemm_plan(int dtype, int M, int N, int K,
+                        const void *A, int lda, const void *B, int ldb,
+                        const void *C, int ldc, int num_sms, gemm_plan_t *plan);
+
+/*
+ * Shared-memory layout of the kernels' operand tiles, as an element offset
+ * inside one stage (for host-side bank-conflict and bijectivity checks of
+ * the swizzle; wingedge777 section 4 derives its SWIZZLE_A the same way).
+ * layout: 0 = FP32 A tile (128 rows x 32 k, 128-byte XOR swizzle),
+ *         1 = FP32 B tile (32 k x 128 columns, unswizzled).
+ * Returns -1 for an unknown layout or out-of-range coordinates.
+ */
+int gemm_smem_layout_offset(int layout, int row, int col);
+
+/*
+ * Failure-detection self test: launches one thread that waits on an
+ * mbarrier nothing will complete, with a bound of `timeout_us`
+ * microseconds.  The wait gives up, sets the fault word, and the kernel
+ * returns; gemm_device_check() then reports GEMM_ERR_DEVICE_TIMEOUT and
+ * the context stays usable.
+ */
+gemm_status_t gemm_selftest_timeout(unsigned timeout_us, cudaStream_t stream);
+
+#if defined(__cplusplus)
+}
+#endif
+
+#endif /* DENSE_GEMM_H_ */

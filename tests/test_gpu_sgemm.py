@@ -1,0 +1,133 @@
+"""GPU parity of the FP32 SIMT SGEMM against the CPU oracle, called through
+the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import TOL, check_device, compare, gpu_lib, padded, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dg():
+    return gpu_lib()
+
+
+def _run_workload(dg, w, rows=None, exact=False):
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    return compare(w.dtype, A, B, C, rows=rows, exact=exact)
+
+
+def test_f32_256_uniform(dg):
+    _run_workload(dg, workloads.WORKLOADS["f32_256"])
+
+
+def test_f32_256_integer_bit_exact(dg):
+    _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)
+
+
+def test_f32_integer_bit_exact_large_k(dg):
+    # entries in {-2..2}, K = 4096: |partial sums| <= 4 K = 16384 < 2^24
+    w = workloads.Workload("int4096", "f32", 384, 320, 4096, "int", 101, -2, 2)
+    _run_workload(dg, w, exact=True)
+
+
+def test_f32_2048_sampled_rows(dg):
+    w = workloads.WORKLOADS["f32_2048"]
+    _run_workload(dg, w, rows=workloads.sample_rows(w.M, 96, seed=1))
+
+
+def test_f32_4096_sampled_rows(dg):
+    w = workloads.WORKLOADS["f32_4096"]
+    _run_workload(dg, w, rows=workloads.sample_rows(w.M, 64, seed=2))
+
+
+def test_f32_edge_full(dg):
+    # 1000 x 1030 x 777, lda = 777: not 16-byte pitched -> cp.async staging
+    _run_workload(dg, workloads.WORKLOADS["f32_edge"])
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 3, 1), (2, 3, 4), (1, 300, 7), (300, 1, 9),
+                                   (129, 130, 33), (127, 255, 31), (64, 64, 5), (1000, 2000, 500),
+                                   (256, 256, 96), (128, 128, 777), (513, 257, 1025)])
+def test_f32_shapes(dg, shape):
+    M, N, K = shape
+    w = workloads.Workload(f"s{M}x{N}x{K}", "f32", M, N, K, "uniform", M + 7 * N + 13 * K)
+    _run_workload(dg, w)
+
+
+@pytest.mark.parametrize("pad", [(0, 0, 0), (4, 8, 12), (3, 1, 5), (1, 0, 0), (0, 0, 3)])
+def test_f32_padded_leading_dimensions(dg, pad):
+    pa, pb, pc = pad
+    M, N, K = 200, 260, 150
+    w = workloads.Workload("pad", "f32", M, N, K, "uniform", 17)
+    A, B = workloads.make(w)
+    Ad, Bd = padded(A, pa), padded(B, pb)
+    Cbuf = torch.full((M, N + pc), -7.0, dtype=torch.float32, device="cuda")
+    C = Cbuf[:, :N]
+    C.fill_(float("nan"))
+    run_gemm(dg, Ad, Bd, C)
+    compare("f32", A, B, C)
+    if pc:
+        assert torch.all(Cbuf[:, N:] == -7.0), "padding columns of C were written"
+
+
+def test_f32_misaligned_base_pointer(dg):
+    # A and B start 4 bytes into their buffers: not 16-byte aligned.
+    M, N, K = 130, 132, 96
+    w = workloads.Workload("mis", "f32", M, N, K, "uniform", 23)
+    A, B = workloads.make(w)
+    abuf = torch.zeros(M * K + 1, device="cuda")
+    bbuf = torch.zeros(K * N + 1, device="cuda")
+    Ad = abuf[1:].view(M, K)
+    Bd = bbuf[1:].view(K, N)
+    Ad.copy_(A)
+    Bd.copy_(B)
+    st, plan = dg.gemm_plan("f32", M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), N,
+                            1 << 40, N)
+    assert plan.path == dg.PATH_SIMT_CPASYNC
+    C = run_gemm(dg, Ad, Bd)
+    compare("f32", A, B, C)
+
+
+def test_f32_zero_k_writes_zeros(dg):
+    C = torch.full((33, 17), float("nan"), device="cuda")
+    A = torch.empty((33, 0), device="cuda")
+    B = torch.empty((0, 17), device="cuda")
+    st = dg.gemm_f32(33, 17, 0, A.data_ptr(), 1, B.data_ptr(), 17, C.data_ptr(), 17,
+                     torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK
+    check_device(dg)
+    assert torch.all(C == 0)
+
+
+def test_f32_empty_output_leaves_memory_untouched(dg):
+    C = torch.full((4, 4), 3.0, device="cuda")
+    st = dg.gemm_f32(0, 4, 4, C.data_ptr(), 4, C.data_ptr(), 4, C.data_ptr(), 4,
+                     torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK
+    check_device(dg)
+    assert torch.all(C == 3.0)
+
+
+def test_f32_repeat_is_deterministic(dg):
+    w = workloads.WORKLOADS["f32_edge"]
+    A, B = workloads.make(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = run_gemm(dg, Ad, Bd)
+    C2 = run_gemm(dg, Ad, Bd)
+    assert torch.equal(C1, C2)
+
+
+def test_bounded_wait_self_test_reports_timeout(dg):
+    stream = torch.cuda.current_stream().cuda_stream
+    assert dg.gemm_selftest_timeout(20000, stream) == dg.GEMM_OK
+    st, bits = dg.gemm_device_check(stream)
+    assert st == dg.GEMM_ERR_DEVICE_TIMEOUT and bits & (1 << 4)
+    # the fault word was cleared and the context still works
+    st, bits = dg.gemm_device_check(stream)
+    assert st == dg.GEMM_OK and bits == 0
+    _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)

@@ -1,0 +1,124 @@
+"""GPU parity of the FP16 / BF16 tcgen05 GEMM against the CPU oracle,
+called through the C ABI."""
+import pytest
+import torch
+
+import workloads
+from parity import check_device, compare, gpu_lib, padded, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dg():
+    return gpu_lib()
+
+
+def _run(dg, w, rows=None, exact=False):
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    return compare(w.dtype, A, B, C, rows=rows, exact=exact)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(128, 256, 64), (1, 8, 8), (2, 8, 16), (256, 512, 192),
+                                   (200, 296, 136), (129, 264, 72), (300, 520, 8),
+                                   (640, 768, 1000), (1000, 2000, 504)])
+def test_tc_shapes_full(dg, dtype, shape):
+    M, N, K = shape
+    dist = "normal" if dtype == "f16" else "uniform"
+    w = workloads.Workload(f"{dtype}_{M}x{N}x{K}", dtype, M, N, K, dist, M + 3 * N + 7 * K)
+    _run(dg, w)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_many_tiles_per_cta_full(dg, dtype):
+    # 16 x 16 = 256 output tiles > 152 SMs: CTAs loop over tiles and the
+    # double-buffered accumulator is reused.
+    w = workloads.Workload(f"{dtype}_multi", dtype, 2048, 4096, 128, "normal", 31)
+    _run(dg, w)
+
+
+def test_f16_integer_bit_exact(dg):
+    # entries in {-2..2}, K = 512: |C| <= 2048, exact in FP16 and in the FP32 accumulator
+    w = workloads.Workload("f16_int", "f16", 384, 512, 512, "int", 41, -2, 2)
+    _run(dg, w, exact=True)
+
+
+def test_bf16_integer_bit_exact(dg):
+    # entries in {-1, 0, 1}, K = 256: |C| <= 256, exact in BF16
+    w = workloads.Workload("bf16_int", "bf16", 384, 512, 256, "int", 42, -1, 1)
+    _run(dg, w, exact=True)
+
+
+def test_bf16_edge_integer_rounded_exact(dg):
+    # Edge shape with integer entries: the FP32 accumulator is exact (|C| <=
+    # 1536 < 2^24), so the output is the exact product rounded once to BF16.
+    w = workloads.Workload("bf16_edge_int", "bf16", 4097, 3000, 1536, "int", 43, -1, 1)
+    _run(dg, w, rows=workloads.sample_rows(w.M, 48, seed=43), exact=True)
+
+
+def test_f16_4096_sampled_rows(dg):
+    w = workloads.WORKLOADS["f16_4096"]
+    _run(dg, w, rows=workloads.sample_rows(w.M, 48, seed=3))
+
+
+def test_bf16_8192_sampled_rows(dg):
+    w = workloads.WORKLOADS["bf16_8192"]
+    _run(dg, w, rows=workloads.sample_rows(w.M, 24, seed=3))
+
+
+def test_bf16_edge_sampled_rows(dg):
+    w = workloads.WORKLOADS["bf16_edge"]
+    _run(dg, w, rows=workloads.sample_rows(w.M, 64, seed=4))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_padded_leading_dimensions(dg, dtype):
+    M, N, K = 300, 264, 200
+    w = workloads.Workload("pad", dtype, M, N, K, "uniform", 51)
+    A, B = workloads.make(w)
+    Ad, Bd = padded(A, 8), padded(B, 16)
+    Cbuf = torch.full((M, N + 8), -3.0, dtype=A.dtype, device="cuda")
+    C = Cbuf[:, :N]
+    C.fill_(float("nan"))
+    run_gemm(dg, Ad, Bd, C)
+    compare(dtype, A, B, C)
+    assert torch.all(Cbuf[:, N:] == -3.0), "padding columns of C were written"
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_misaligned_is_refused(dg, dtype):
+    td = workloads.TORCH_DTYPES[dtype]
+    A = torch.zeros(64, 60, dtype=td, device="cuda")     # lda = 60: 120-byte pitch
+    B = torch.zeros(60, 64, dtype=td, device="cuda")
+    C = torch.full((64, 64), 5.0, dtype=td, device="cuda")
+    run_gemm(dg, A, B, C, expect_status=dg.GEMM_ERR_MISALIGNED)
+    buf = torch.zeros(64 * 64 + 1, dtype=td, device="cuda")
+    A2 = buf[1:].view(64, 64)                             # 2-byte aligned base
+    B2 = torch.zeros(64, 64, dtype=td, device="cuda")
+    run_gemm(dg, A2, B2, C, expect_status=dg.GEMM_ERR_MISALIGNED)
+    check_device(dg)
+    assert torch.all(C == 5.0)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_zero_k(dg, dtype):
+    td = workloads.TORCH_DTYPES[dtype]
+    C = torch.full((40, 24), float("nan"), dtype=td, device="cuda")
+    A = torch.empty((40, 0), dtype=td, device="cuda")
+    B = torch.empty((0, 24), dtype=td, device="cuda")
+    st = dg.gemm(dtype, 40, 24, 0, A.data_ptr(), 8, B.data_ptr(), 24, C.data_ptr(), 24,
+                 torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK
+    check_device(dg)
+    assert torch.all(C == 0)
+
+
+def test_tc_repeat_is_deterministic(dg):
+    w = workloads.WORKLOADS["bf16_edge"]
+    A, B = workloads.make(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = run_gemm(dg, Ad, Bd)
+    C2 = run_gemm(dg, Ad, Bd)
+    assert torch.equal(C1, C2)
