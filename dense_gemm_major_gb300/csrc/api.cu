@@ -128,6 +128,20 @@ inline bool overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Measurement override: DENSE_GEMM_SGEMM_TILE=narrow|wide forces the FP32
+// tile configuration (0 = no override).
+int forced_sgemm_tn() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_SGEMM_TILE");
+    if (s == nullptr) return 0;
+    if (std::strcmp(s, "narrow") == 0) return 8;
+    if (std::strcmp(s, "wide") == 0) return 16;
+    if (std::strcmp(s, "narrow1") == 0) return 9;
+    return 0;
+  }();
+  return v;
+}
+
 gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
                         int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
@@ -155,17 +169,33 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
       overlap(B, span_bytes(K, N, ldb, es), C, cbytes))
     return GEMM_ERR_INVALID_ARG;
 
+  const int sms = num_sms > 0 ? num_sms : 1;
   if (dtype == 0) {
     const bool tma = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
     plan->path = tma ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
+    // With the last partial wave split into k-halves, the wide tile (8 x 16
+    // per thread, one CTA per SM) is at least as fast as the narrow one (8 x 8,
+    // two CTAs per SM) once the narrow grid has more tiles than SMs (measured
+    // on GB300: 4096^3 53.9 vs 53.8, 8192^3 56.5 vs 56.0, 2048^3 46.0 vs 43.9
+    // TFLOP/s); smaller grids keep the narrow tile for parallelism.
+    const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
+    int tn = narrow_tiles > sms ? 16 : 8;
+    if (const int forced = forced_sgemm_tn()) tn = forced == 16 ? 16 : 8;
     plan->block_m = dgemm::kSgemmBM;
-    plan->block_n = dgemm::kSgemmBN;
+    plan->block_n = dgemm::sgemm_bn(tn);
     plan->block_k = dgemm::kSgemmBK;
-    plan->stages = dgemm::kSgemmStages;
+    plan->stages = dgemm::sgemm_stages(tn);
     plan->threads = dgemm::kSgemmThreads;
-    plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::kSgemmBN);
-    plan->ctas = plan->tiles;
-    plan->smem_bytes = dgemm::kSgemmSmemBytes;
+    plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
+    plan->smem_bytes = dgemm::sgemm_smem_bytes(tn);
+    // Wave quantisation: the tiles of a last partial wave (or of a grid that
+    // is a single partial wave) are split into two k-halves when twice their
+    // number still fits in one wave of CTA slots.
+    const int slots = (tn == 8 && forced_sgemm_tn() != 9 ? 2 : 1) * sms;
+    const int rem = plan->tiles % slots;
+    const int nk = ceil_div(K, dgemm::kSgemmBK);
+    plan->split_tiles = (rem > 0 && 2 * rem <= slots && nk >= 2) ? rem : 0;
+    plan->ctas = plan->tiles + plan->split_tiles;
     return GEMM_OK;
   }
   // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
@@ -178,7 +208,6 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   plan->stages = dgemm::kTcStages;
   plan->threads = dgemm::kTcThreads;
   plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
-  const int sms = num_sms > 0 ? num_sms : 1;
   plan->ctas = plan->tiles < sms ? plan->tiles : sms;
   plan->smem_bytes = dgemm::kTcSmemBytes;
   return GEMM_OK;
@@ -187,11 +216,14 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
 gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const void* B, int ldb,
                   void* C, int ldc, cudaStream_t stream) {
   gemm_plan_t plan;
-  gemm_status_t st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, 0, &plan);
+  gemm_status_t st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, 1, &plan);
   if (st != GEMM_OK) return st;
   if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
   DeviceInfo* dev = nullptr;
   st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  // Re-plan with the device's SM count (validation above needs no device).
+  st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sms, &plan);
   if (st != GEMM_OK) return st;
   const int es = dtype == 0 ? 4 : 2;
   cudaError_t e = cudaSuccess;
@@ -209,8 +241,11 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.ldb = ldb;
     p.C = static_cast<float*>(C);
     p.ldc = ldc;
+    const int tn = plan.block_n == dgemm::sgemm_bn(16) ? 16 : (forced_sgemm_tn() == 9 ? 9 : 8);
     p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
-    p.tiles_n = ceil_div(N, dgemm::kSgemmBN);
+    p.tiles_n = ceil_div(N, plan.block_n);
+    p.full_tiles = plan.tiles - plan.split_tiles;
+    p.split_kt = ceil_div(K, dgemm::kSgemmBK) / 2;
     p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
@@ -221,11 +256,11 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
                      (uint64_t)lda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
           !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
-                     (uint64_t)ldb * 4, dgemm::kSgemmBN, dgemm::kSgemmBK,
+                     (uint64_t)ldb * 4, (uint32_t)plan.block_n, dgemm::kSgemmBK,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_LAUNCH;
     }
-    e = dgemm::launch_sgemm(p, tma, &tmA, &tmB, stream);
+    e = dgemm::launch_sgemm(p, tn, tma, &tmA, &tmB, stream);
   } else {
     const CUtensorMapDataType dt =
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -318,11 +353,12 @@ gemm_status_t gemm_plan(int dtype, int M, int N, int K, const void* A, int lda, 
 int gemm_smem_layout_offset(int layout, int row, int col) {
   if (layout == 0) {
     if (row < 0 || row >= dgemm::kSgemmBM || col < 0 || col >= dgemm::kSgemmBK) return -1;
-    return dgemm::sgemm_smem_offset(0, row, col);
+    return dgemm::sgemm_smem_offset(0, 0, row, col);
   }
-  if (layout == 1) {
-    if (row < 0 || row >= dgemm::kSgemmBK || col < 0 || col >= dgemm::kSgemmBN) return -1;
-    return dgemm::sgemm_smem_offset(1, row, col);
+  if (layout == 1 || layout == 2) {
+    const int bn = dgemm::sgemm_bn(layout == 1 ? 8 : 16);
+    if (row < 0 || row >= dgemm::kSgemmBK || col < 0 || col >= bn) return -1;
+    return dgemm::sgemm_smem_offset(1, bn, row, col);
   }
   return -1;
 }

@@ -10,16 +10,20 @@ namespace dgemm {
 
 // ---------------------------------------------------------------- FP32 SIMT
 
-// Block tile 128 x 128 x 32, 256 threads (8 warps of 32 x 64), 8 x 8 outputs
-// per thread, a 3-stage shared-memory ring, two CTAs per SM.
+// Two tile configurations, both 256 threads (8 warps as 4 x 2, each warp a
+// 4 x 8 lane grid), BM = 128, BK = 32, TM = 8 rows per thread:
+//   narrow: TN = 8  -> 8 x 8 per thread,  BN = 128, 3 stages, 2 CTAs per SM;
+//   wide:   TN = 16 -> 8 x 16 per thread, BN = 256, 4 stages, 1 CTA per SM.
 constexpr int kSgemmBM = 128;
-constexpr int kSgemmBN = 128;
 constexpr int kSgemmBK = 32;
-constexpr int kSgemmStages = 3;
 constexpr int kSgemmThreads = 256;
 constexpr int kSgemmGroupM = 16;   // tile rows per rasterisation group (L2 reuse)
-constexpr int kSgemmSmemBytes =
-    kSgemmStages * (kSgemmBM * kSgemmBK + kSgemmBK * kSgemmBN) * 4 + 1024 /*align*/ + 64;
+constexpr int sgemm_bn(int tn) { return 16 * tn; }
+constexpr int sgemm_stages(int tn) { return tn == 8 ? 3 : 4; }
+constexpr int sgemm_smem_bytes(int tn) {
+  return sgemm_stages(tn) * (kSgemmBM * kSgemmBK + kSgemmBK * sgemm_bn(tn)) * 4 + 1024 /*align*/ +
+         64 /*barriers*/;
+}
 
 struct SgemmParams {
   int M, N, K;
@@ -30,19 +34,42 @@ struct SgemmParams {
   float* C;
   long long ldc;
   int tiles_m, tiles_n;
+  // Tiles [0, full_tiles) are computed whole and stored.  Each tile t >=
+  // full_tiles is computed as two pieces (k-tiles [0, split_kt) and
+  // [split_kt, nk)) by consecutive CTAs that add their FP32 partial sums
+  // into C, which must hold zeros for those tiles beforehand; with exactly
+  // two addends the result does not depend on their order.
+  int full_tiles;
+  int split_kt;
   int c_vec4;        // C rows may be written with 16-byte stores
   unsigned* fault;   // device fault word
   unsigned long long timeout_ns;
 };
 
-// use_tma: A and B are staged by TMA (16-byte aligned bases and strides);
-// otherwise by 4-byte cp.async with zero fill.  Returns the launch error.
-cudaError_t launch_sgemm(const SgemmParams& p, bool use_tma, const CUtensorMap* tmA,
+// Tile (tm, tn) of linear tile index t under grouped rasterisation: tiles
+// walk down a group of `group` tile rows before moving one tile column right.
+__host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, int group, int& tm,
+                                             int& tn) {
+  const int per_group = group * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * group;
+  const int gsize = (tiles_m - first_m) < group ? (tiles_m - first_m) : group;
+  const int r = t - g * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+// tn: 8 (narrow) or 16 (wide).  use_tma: A and B are staged by TMA
+// (16-byte aligned bases and strides); otherwise by 4-byte cp.async with
+// zero fill.  When p.full_tiles < tiles, first zeroes C on the split tiles
+// (one extra launch).  Returns the launch error.
+cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream);
 
 // Element offset of (row, col) inside one stage of the FP32 A tile
-// (which = 0) or B tile (which = 1); host copy of the device layout.
-int sgemm_smem_offset(int which, int r, int c);
+// (which = 0) or the B tile of a BN-wide configuration (which = 1); host
+// copy of the device layout.
+int sgemm_smem_offset(int which, int bn, int r, int c);
 
 // ---------------------------------------------------------------- FP16/BF16 tcgen05
 

@@ -6,12 +6,19 @@
 //    thread and a 128 x 128 block tile ("[CUDA 优化实战] sgemm - 超越 cuBLAS",
 //    section 2 and its resource-sizing analysis; "GEMM：从朴素实现到 shared memory
 //    tiling 与寄存器分块", section 3; m.lqnn.cn SGEMM article, the v3 register
-//    micro-tile).
-//  * 16-byte fragment loads from shared memory (wingedge777 section 3 reads A
+//    micro-tile).  A wide configuration (8 x 16 per thread, 128 x 256 block
+//    tile, one CTA per SM) serves grids of one to two narrow waves.
+//  * Vector fragment loads from shared memory (wingedge777 section 3 reads A
 //    fragments as float4 after transposing A into shared memory).  Here A is
 //    not transposed: TMA cannot transpose 4-byte elements, so A stays
-//    K-contiguous and each LDS.128 returns four k-steps of one row.  The
-//    instruction count per FFMA is the same (2 A + 2 B LDS.128 per 64 FFMA).
+//    K-contiguous and one LDS.64 returns two k-steps of one row; B fragments
+//    are LDS.128.  Measured on sm_103a with a shared-load probe: a wavefront
+//    delivers one distinct 16-byte chunk to each group of 4 consecutive
+//    lanes (broadcast within the group is free) and a 16-byte load costs at
+//    least 2 wavefronts.  Each 4-lane group is therefore a 2 x 2 block of the
+//    warp's 4 x 8 lane grid, so every fragment load costs the minimum, 8
+//    bytes per lane per wavefront (0.125 wavefronts per FFMA at 8 x 8 outputs
+//    per thread).
 //  * An XOR-swizzled shared-memory layout that makes every fragment read
 //    conflict-free (wingedge777 section 4's SWIZZLE_A idea; GB300 roadmap
 //    m.nxbn.cn section 3.3).  The A tile uses the pattern TMA's 128-byte
@@ -20,6 +27,9 @@
 //    tr + 4i) so that its four distinct rows fall in four distinct chunks.
 //  * Coalesced 16-byte C stores: each warp writes whole 128-byte row segments
 //    (wingedge777 section 5's write-back re-mapping).
+//  * The outer product is issued as packed fma.rn.f32x2 (two FP32 FMAs per
+//    lane per instruction, each rounded like fmaf): scalar FFMA would need
+//    every issue slot of an SM sub-partition to reach the FFMA peak.
 //  * A multi-stage pipeline (wingedge777 section 6 double buffer; m.lqnn.cn v4
 //    cp.async double buffer; m.nxbn.cn section 3.1-3.2 three or four stages and
 //    TMA).  Here: a 3-stage ring filled by TMA (one thread issues both tile
@@ -36,12 +46,8 @@ namespace dgemm {
 namespace {
 
 constexpr int BM = kSgemmBM;
-constexpr int BN = kSgemmBN;
 constexpr int BK = kSgemmBK;
-constexpr int S = kSgemmStages;
 constexpr int kAStageFloats = BM * BK;
-constexpr int kBStageFloats = BK * BN;
-constexpr uint32_t kStageBytes = (kAStageFloats + kBStageFloats) * 4;
 
 static_assert(BK == 32, "A tile rows must be 128 bytes for the 128-byte swizzle");
 static_assert(kSgemmThreads == 256, "thread mapping below assumes 8 warps");
@@ -52,18 +58,46 @@ __host__ __device__ constexpr int a_tile_offset(int m, int k) {
   return m * BK + ((((k >> 2) ^ (m & 7))) << 2) + (k & 3);
 }
 
-// Offset (in floats) of B element (k, n) inside one B stage: plain rows of
-// 128 floats; a warp always reads 8 consecutive 16-byte chunks of one row.
-__host__ __device__ constexpr int b_tile_offset(int k, int n) { return k * BN + n; }
+// Offset (in floats) of B element (k, n) inside one B stage of width BN:
+// plain rows; a quarter warp always reads 8 consecutive 16-byte chunks of
+// one row.
+__host__ __device__ constexpr int b_tile_offset(int bn, int k, int n) { return k * bn + n; }
 
-__device__ __forceinline__ float4 lds128(const float* p) {
-  return *reinterpret_cast<const float4*>(p);
+// 16 bytes of shared memory as two packed float pairs (one LDS.128).
+__device__ __forceinline__ ulonglong2 lds128_pairs(const float* p) {
+  return *reinterpret_cast<const ulonglong2*>(p);
 }
 
-template <bool kTma>
-__global__ void __launch_bounds__(kSgemmThreads, 2)
+__device__ __forceinline__ unsigned long long pack_pair(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+// d.lo += a.lo * b.lo and d.hi += a.hi * b.hi, each one correctly rounded
+// FMA (the same result as fmaf), issued as one packed instruction: half the
+// issue slots of two scalar FFMA.
+__device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long a,
+                                      unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+template <bool kTma, int TN, int kMinBlocks>
+__global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const SgemmParams p) {
+  constexpr int BN = sgemm_bn(TN);
+  constexpr int S = sgemm_stages(TN);
+  constexpr int kBStageFloats = BK * BN;
+  constexpr uint32_t kStageBytes = (kAStageFloats + kBStageFloats) * 4;
+  constexpr int NH = TN / 4;   // 16-byte column groups per thread
+
   extern __shared__ unsigned char smem_raw[];
   __shared__ int s_abort;
   const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
@@ -75,22 +109,31 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
   const int lane = tid & 31;
   const int warp = tid >> 5;
 
-  // Grouped rasterisation: consecutive CTAs walk down a group of
-  // kSgemmGroupM tile rows before moving one tile column to the right.
-  int tm, tn;
+  // Work unit of this CTA: a whole tile, or one of the two k-pieces of a
+  // split tile (consecutive CTAs), in grouped raster order.
+  int tile, k_begin, k_end;
+  bool add_into_c;
   {
-    const int t = blockIdx.x;
-    const int per_group = kSgemmGroupM * p.tiles_n;
-    const int group = t / per_group;
-    const int first_m = group * kSgemmGroupM;
-    const int gsize = min(p.tiles_m - first_m, kSgemmGroupM);
-    const int r = t - group * per_group;
-    tm = first_m + r % gsize;
-    tn = r / gsize;
+    const int nk_all = (p.K + BK - 1) / BK;
+    const int b = blockIdx.x;
+    if (b < p.full_tiles) {
+      tile = b;
+      k_begin = 0;
+      k_end = nk_all;
+      add_into_c = false;
+    } else {
+      const int j = b - p.full_tiles;
+      tile = p.full_tiles + (j >> 1);
+      k_begin = (j & 1) ? p.split_kt : 0;
+      k_end = (j & 1) ? nk_all : p.split_kt;
+      add_into_c = true;
+    }
   }
+  int tm, tn;
+  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
   const int m0 = tm * BM;
   const int n0 = tn * BN;
-  const int nk = (p.K + BK - 1) / BK;
+  const int nk = k_end - k_begin;   // k-tiles of this unit
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), kTma ? 1u : kSgemmThreads);
@@ -103,9 +146,9 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
   }
   __syncthreads();
 
-  // Stage k-tile kt into ring slot s.
+  // Stage k-tile kt (counted from k_begin) into ring slot s.
   auto issue = [&](int kt, int s) {
-    const int k0 = kt * BK;
+    const int k0 = (k_begin + kt) * BK;
     const uint32_t bar = smem_u32(&full[s]);
     if constexpr (kTma) {
       if (tid == 0) {
@@ -126,17 +169,18 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
         const float* src = v ? p.A + (long long)gm * p.lda + gk : p.A;
         cp_async_4(a_dst + 4u * a_tile_offset(m, ka), src, v);
       }
-      // B: 128 threads copy one 128-float row segment (n contiguous).
+      // B: BN consecutive threads copy one BN-float row segment.
+      constexpr int kRowsPerPass = kSgemmThreads / BN;
       const uint32_t b_dst = smem_u32(sB + s * kBStageFloats);
-      const int nb = tid & (BN - 1);
+      const int nb = tid % BN;
       const int gn = n0 + nb;
 #pragma unroll
-      for (int j = 0; j < BK / 2; ++j) {
-        const int k = (tid >> 7) + 2 * j;
+      for (int j = 0; j < BK / kRowsPerPass; ++j) {
+        const int k = tid / BN + kRowsPerPass * j;
         const int gk2 = k0 + k;
         const bool v = (gk2 < p.K) && (gn < p.N);
         const float* src = v ? p.B + (long long)gk2 * p.ldb + gn : p.B;
-        cp_async_4(b_dst + 4u * b_tile_offset(k, nb), src, v);
+        cp_async_4(b_dst + 4u * b_tile_offset(BN, k, nb), src, v);
       }
       cp_async_mbar_arrive_noinc(bar);
     }
@@ -145,21 +189,26 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
   const int pre = nk < S ? nk : S;
   for (int kt = 0; kt < pre; ++kt) issue(kt, kt);
 
-  // Thread -> output mapping.  Warp (warp_m, warp_n) owns a 32 x 64 block;
-  // lane (tr, tc) owns rows tr + 4i (i < 8) and columns tc*4 + {0..3} and
-  // 32 + tc*4 + {0..3} of it.
+  // Thread -> output mapping.  Warp (warp_m, warp_n) owns a 32 x (BN/2)
+  // block; lane (tr, tc) owns rows tr + 4i (i < 8) and columns
+  // tc*4 + 32h + {0..3} (h < TN/4) of it.
+  // Each group of 4 consecutive lanes is a 2 x 2 block of (tr, tc): a
+  // shared-memory wavefront delivers one distinct 16-byte chunk to each
+  // 4-lane group, so a 16-byte fragment load costs the minimum 2 wavefronts
+  // only if the group touches at most 2 chunks (2 A rows, 2 B column groups).
   const int warp_m = warp >> 1;
   const int warp_n = warp & 1;
-  const int tr = lane >> 3;
-  const int tc = lane & 7;
+  const int tr = ((lane >> 4) << 1) | ((lane >> 1) & 1);       // 0..3
+  const int tc = (((lane >> 2) & 3) << 1) | (lane & 1);        // 0..7
   const int a_row0 = warp_m * 32 + tr;            // row for i = 0
-  const int b_col0 = warp_n * 64 + tc * 4;
+  const int b_col0 = warp_n * (BN / 2) + tc * 4;
 
-  float acc[8][8];
+  // acc[i][j] holds columns (2j, 2j+1) of row i as a packed float pair.
+  unsigned long long acc[8][TN / 2];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
 
   int kt = 0;
   for (; kt < nk; ++kt) {
@@ -169,35 +218,37 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
     if (!ok) {
       s_abort = 1;
     } else {
-      const float* As = sA + s * kAStageFloats;
+      const float* As = sA + s * kAStageFloats + a_row0 * BK;
       const float* Bs = sB + s * kBStageFloats + b_col0;
-      // Row (a_row0 + 4i) mod 8 = tr + 4 (i mod 2): its chunk for k-quad kq is
-      // kq ^ tr ^ 4(i mod 2).  Four base pointers cover (kq mod 4) ^ tr.
+      // Row (a_row0 + 4i) mod 8 = tr + 4 (i mod 2), so k-quad kq of the
+      // thread's even rows sits in chunk kq ^ tr, of its odd rows in chunk
+      // kq ^ tr ^ 4.  Four base pointers cover (kq mod 4) ^ tr.
       const float* a_base[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) a_base[q] = As + a_row0 * BK + (((q ^ tr) & 3) << 2);
+      for (int q = 0; q < 4; ++q) a_base[q] = As + (((q ^ tr) & 3) << 2);
 #pragma unroll
       for (int kq = 0; kq < BK / 4; ++kq) {
+        // A fragment: four k-steps of each of the thread's 8 rows.
         float4 a[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          a[i] = lds128(a_base[kq & 3] + 4 * i * BK + (((kq & 4) ^ ((i & 1) << 2)) << 2));
+          a[i] = *reinterpret_cast<const float4*>(a_base[kq & 3] + 4 * i * BK +
+                                                  (((kq & 4) ^ ((i & 1) << 2)) << 2));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const float* brow = Bs + (kq * 4 + kk) * BN;
-          const float4 b0 = lds128(brow);
-          const float4 b1 = lds128(brow + 32);
+          ulonglong2 b[NH];
+#pragma unroll
+          for (int h = 0; h < NH; ++h) b[h] = lds128_pairs(brow + 32 * h);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float av = (&a[i].x)[kk];
-            acc[i][0] = fmaf(av, b0.x, acc[i][0]);
-            acc[i][1] = fmaf(av, b0.y, acc[i][1]);
-            acc[i][2] = fmaf(av, b0.z, acc[i][2]);
-            acc[i][3] = fmaf(av, b0.w, acc[i][3]);
-            acc[i][4] = fmaf(av, b1.x, acc[i][4]);
-            acc[i][5] = fmaf(av, b1.y, acc[i][5]);
-            acc[i][6] = fmaf(av, b1.z, acc[i][6]);
-            acc[i][7] = fmaf(av, b1.w, acc[i][7]);
+            const unsigned long long aa = pack_pair(av, av);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              ffma2(acc[i][2 * h + 0], aa, b[h].x);
+              ffma2(acc[i][2 * h + 1], aa, b[h].y);
+            }
           }
         }
       }
@@ -237,11 +288,21 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
     if (gm >= p.M) continue;
     float* crow = p.C + (long long)gm * p.ldc;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       const int gn = n0 + b_col0 + 32 * h;
-      const float v0 = acc[i][4 * h + 0], v1 = acc[i][4 * h + 1];
-      const float v2 = acc[i][4 * h + 2], v3 = acc[i][4 * h + 3];
-      if (p.c_vec4 && gn + 3 < p.N) {
+      const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+      const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+      const float v0 = lo.x, v1 = lo.y, v2 = hi.x, v3 = hi.y;
+      if (add_into_c) {
+        if (p.c_vec4 && gn + 3 < p.N) {
+          atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
+        } else {
+          if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
+          if (gn + 1 < p.N) atomicAdd(crow + gn + 1, v1);
+          if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
+          if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
+        }
+      } else if (p.c_vec4 && gn + 3 < p.N) {
         *reinterpret_cast<float4*>(crow + gn) = make_float4(v0, v1, v2, v3);
       } else {
         if (gn + 0 < p.N) crow[gn + 0] = v0;
@@ -253,32 +314,61 @@ __global__ void __launch_bounds__(kSgemmThreads, 2)
   }
 }
 
-}  // namespace
+// Zeroes C on the split tiles [full_tiles, tiles_m * tiles_n), one CTA per
+// tile, before their two k-pieces add into it.
+__global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn) {
+  int tm, tn;
+  grouped_tile(p.full_tiles + (int)blockIdx.x, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
+  const int rows = min(BM, p.M - tm * BM);
+  const int cols = min(bn, p.N - tn * bn);
+  for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
+    const int r = idx / cols;
+    const int c = idx - r * cols;
+    p.C[(long long)(tm * BM + r) * p.ldc + tn * bn + c] = 0.f;
+  }
+}
 
-cudaError_t launch_sgemm(const SgemmParams& p, bool use_tma, const CUtensorMap* tmA,
-                         const CUtensorMap* tmB, cudaStream_t stream) {
+template <bool kTma, int TN, int kMinBlocks>
+cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                       cudaStream_t stream) {
   // The attribute is per function; setting it on every call is cheap and
   // keeps this correct for every device of the process.
-  cudaError_t e;
-  const dim3 grid((unsigned)(p.tiles_m * p.tiles_n));
-  if (use_tma) {
-    e = cudaFuncSetAttribute(sgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSgemmSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(sgemm_kernel<kTma, TN, kMinBlocks>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sgemm_smem_bytes(TN));
+  if (e != cudaSuccess) return e;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int split = tiles - p.full_tiles;
+  if (split > 0) {
+    sgemm_zero_split_tiles<<<split, 256, 0, stream>>>(p, sgemm_bn(TN));
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    sgemm_kernel<true><<<grid, kSgemmThreads, kSgemmSmemBytes, stream>>>(*tmA, *tmB, p);
-  } else {
-    e = cudaFuncSetAttribute(sgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSgemmSmemBytes);
-    if (e != cudaSuccess) return e;
-    CUtensorMap none{};
-    sgemm_kernel<false><<<grid, kSgemmThreads, kSgemmSmemBytes, stream>>>(none, none, p);
   }
+  const dim3 grid((unsigned)(tiles + split));
+  sgemm_kernel<kTma, TN, kMinBlocks>
+      <<<grid, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
   return cudaGetLastError();
 }
 
+}  // namespace
+
+cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
+                         const CUtensorMap* tmB, cudaStream_t stream) {
+  CUtensorMap none{};
+  if (!use_tma) tmA = tmB = &none;
+  if (tn == 16)
+    return use_tma ? launch_cfg<true, 16, 1>(p, tmA, tmB, stream)
+                   : launch_cfg<false, 16, 1>(p, tmA, tmB, stream);
+  if (tn == 9)   // 8 x 8 per thread, one CTA per SM, up to 255 registers
+    return use_tma ? launch_cfg<true, 8, 1>(p, tmA, tmB, stream)
+                   : launch_cfg<false, 8, 1>(p, tmA, tmB, stream);
+  return use_tma ? launch_cfg<true, 8, 2>(p, tmA, tmB, stream)
+                 : launch_cfg<false, 8, 2>(p, tmA, tmB, stream);
+}
+
 // Host-visible copy of the A / B stage layouts, for layout checks on the CPU.
-int sgemm_smem_offset(int which, int r, int c) {
-  return which == 0 ? a_tile_offset(r, c) : b_tile_offset(r, c);
+int sgemm_smem_offset(int which, int bn, int r, int c) {
+  return which == 0 ? a_tile_offset(r, c) : b_tile_offset(bn, r, c);
 }
 
 }  // namespace dgemm

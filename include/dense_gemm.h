@@ -63,9 +63,10 @@ typedef enum gemm_status_t {
 
 /*
  * FP32 GEMM on the FFMA pipes (no TF32): the SIMT kernel family of
- * wingedge777 sections 2-6 (block tiling, 8x8 register outer product,
- * swizzled shared memory, coalesced write-back, multi-stage pipeline),
- * re-designed for sm_103a with a TMA-fed 3-stage ring.
+ * wingedge777 sections 2-6 (block tiling, register outer product, swizzled
+ * shared memory, coalesced write-back, multi-stage pipeline), re-designed
+ * for sm_103a with a TMA-fed multi-stage ring and an 8x8 or 8x16 per-thread
+ * tile chosen by problem size.
  * Any alignment is accepted: when a base pointer or lda/ldb is not 16-byte
  * aligned the tiles are staged with 4-byte cp.async instead of TMA.
  */
@@ -126,6 +127,10 @@ typedef struct gemm_plan_t {
   int ctas;          /* grid size                         */
   int tiles;         /* output tiles                      */
   int smem_bytes;    /* dynamic shared memory per CTA     */
+  int split_tiles;   /* FP32: tiles computed as two k-halves that are
+                        added into C (zeroed first); these are the tiles of
+                        the last partial wave, or all tiles of a grid that
+                        fills at most half of the CTA slots               */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,
@@ -136,7 +141,9 @@ gemm_status_t gemm_plan(int dtype, int M, int N, int K,
  * inside one stage (for host-side bank-conflict and bijectivity checks of
  * the swizzle; wingedge777 section 4 derives its SWIZZLE_A the same way).
  * layout: 0 = FP32 A tile (128 rows x 32 k, 128-byte XOR swizzle),
- *         1 = FP32 B tile (32 k x 128 columns, unswizzled).
+ *         1 = FP32 B tile of the narrow configuration (32 k x 128 columns),
+ *         2 = FP32 B tile of the wide configuration (32 k x 256 columns);
+ *         B tiles are unswizzled.
  * Returns -1 for an unknown layout or out-of-range coordinates.
  */
 int gemm_smem_layout_offset(int layout, int row, int col);

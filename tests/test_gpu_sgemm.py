@@ -114,6 +114,7 @@ def test_f32_empty_output_leaves_memory_untouched(dg):
 
 
 def test_f32_repeat_is_deterministic(dg):
+    # The edge shape splits every tile into two k-pieces added into C.
     w = workloads.WORKLOADS["f32_edge"]
     A, B = workloads.make(w)
     Ad, Bd = A.cuda(), B.cuda()
@@ -131,3 +132,29 @@ def test_bounded_wait_self_test_reports_timeout(dg):
     st, bits = dg.gemm_device_check(stream)
     assert st == dg.GEMM_OK and bits == 0
     _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 64), (2688, 3072, 96), (1000, 1030, 65),
+                                   (300, 260, 999)])
+def test_f32_split_tail_tiles(dg, shape):
+    # Grids whose last partial wave (or whole grid) is split into k-halves
+    # that add into C; C starts as NaN, so a tile the zeroing kernel or a
+    # piece misses shows up.
+    M, N, K = shape
+    w = workloads.Workload(f"split{M}x{N}x{K}", "f32", M, N, K, "uniform", 61)
+    A, B = workloads.make(w)
+    st, plan = dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N,
+                            torch.cuda.get_device_properties(0).multi_processor_count)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    rows = None if M * N * K < 3e9 else workloads.sample_rows(M, 64, seed=61)
+    compare("f32", A, B, C, rows=rows)
+    return plan.split_tiles
+
+
+def test_f32_split_tail_integer_exact(dg):
+    # 1024 tiles -> 112 split tiles at 4096 x 4096; integer entries make the
+    # two-piece sums exact, so the split result is bit-exact.
+    w = workloads.Workload("split_int", "f32", 4096, 4096, 256, "int", 62, -2, 2)
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare("f32", A, B, C, rows=workloads.sample_rows(w.M, 96, seed=62), exact=True)

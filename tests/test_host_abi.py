@@ -85,13 +85,35 @@ def test_plan_paths():
     ok, p = dg.gemm_plan("f32", 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
                          FAKE + (2 << 30), 4096)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_TMA
-    assert (p.block_m, p.block_n, p.block_k) == (128, 128, 32)
-    assert p.tiles == 32 * 32 and p.ctas == 1024
+    # many tiles: the wide 128 x 256 configuration, one CTA per SM; the last
+    # partial wave (512 - 3 x 152 = 56 tiles) runs as 112 k-halves
+    assert (p.block_m, p.block_n, p.block_k, p.stages) == (128, 256, 32, 4)
+    assert p.tiles == 32 * 16 and p.split_tiles == 56 and p.ctas == 512 + 56
+    # 8192^3: 2048 tiles = 13 x 152 + 72, 2 x 72 <= 152 -> split
+    ok, p = dg.gemm_plan("f32", 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
+                         FAKE + (2 << 30), 8192, num_sms=152)
+    assert p.split_tiles == 72
+    # a remainder larger than half a wave is not split (252 = 152 + 100)
+    ok, p = dg.gemm_plan("f32", 128 * 21, 256 * 12, 256, FAKE, 256, FAKE + (1 << 30), 3072,
+                         FAKE + (2 << 30), 3072, num_sms=152)
+    assert p.tiles == 252 and p.split_tiles == 0 and p.ctas == 252
+    # a single k-tile cannot be split
+    ok, p = dg.gemm_plan("f32", 1000, 1030, 32, FAKE, 32, FAKE + (1 << 30), 1030,
+                         FAKE + (2 << 30), 1030, num_sms=152)
+    assert p.split_tiles == 0
+    ok, p = dg.gemm_plan("f32", 2048, 2048, 2048, FAKE, 2048, FAKE + (1 << 30), 2048,
+                         FAKE + (2 << 30), 2048, num_sms=152)
+    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles, p.split_tiles) == (256, 4, 128, 0)
+    # at most one narrow tile per SM: the narrow 128 x 128 configuration
+    ok, p = dg.gemm_plan("f32", 1024, 1024, 512, FAKE, 512, FAKE + (1 << 30), 1024,
+                         FAKE + (2 << 30), 1024, num_sms=152)
+    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles) == (128, 3, 64)
     # lda = 777 floats is not a 16-byte pitch: cp.async staging
     ok, p = dg.gemm_plan("f32", 1000, 1030, 777, FAKE, 777, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_CPASYNC
-    assert p.tiles == 8 * 9
+    # 72 tiles fill less than half of the 304 slots: all split into k-halves
+    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 72 and p.ctas == 144
     # misaligned base pointer (4-byte aligned only)
     ok, p = dg.gemm_plan("f32", 64, 64, 64, FAKE + 4, 64, FAKE + (1 << 30), 64,
                          FAKE + (2 << 30), 64)
@@ -136,39 +158,80 @@ def test_a_tile_layout_is_the_tma_128b_swizzle_and_a_bijection():
             seen.add(off)
     assert len(seen) == 128 * 32
     assert dg.gemm_smem_layout_offset(0, 128, 0) == -1
-    assert dg.gemm_smem_layout_offset(2, 0, 0) == -1
+    assert dg.gemm_smem_layout_offset(3, 0, 0) == -1
 
 
 def _wavefronts(byte_addrs, width):
-    """Shared-memory wavefronts one warp-wide access needs: requests to the
-    same address are merged (broadcast); each distinct `width`-byte word
-    occupies width/4 consecutive banks; the access takes as many wavefronts as
-    the most-loaded bank has distinct words, and at least total/128 bytes."""
-    distinct = sorted(set(byte_addrs))
+    """Shared-memory wavefronts of one warp-wide load, by the rule measured on
+    sm_103a with a shared-load probe under ncu: requests to one address are
+    merged (broadcast); a wavefront delivers at most 16 bytes of distinct data
+    to each group of 4 consecutive lanes; a 16-byte load takes at least 2
+    wavefronts; and distinct words that fall in one bank serialise."""
+    lanes = list(byte_addrs)
+    per_group = max(len(set(lanes[4 * g:4 * g + 4])) * width for g in range(8))
+    need = max(2 if width == 16 else 1, -(-per_group // 16))
     load = [0] * 32
-    for a in distinct:
+    for a in sorted(set(lanes)):
         for b in range(width // 4):
             load[(a // 4 + b) % 32] += 1
-    return max(max(load), -(-len(distinct) * width // 128))
+    return max(need, max(load))
 
 
-def test_fragment_reads_are_conflict_free():
-    # The SGEMM thread mapping: warp (wm, wn) of a 4 x 2 grid, lane (tr, tc)
-    # = (lane // 8, lane % 8) owns rows 32 wm + tr + 4 i and columns
-    # 64 wn + 4 tc + {0..3} (+32).  A reads: one 16-byte k-quad of one row.
+def _lane_rc(l):
+    """The SGEMM kernel's lane -> (tr, tc) map: each 4-lane group is a 2 x 2
+    block of the 4 x 8 lane grid."""
+    return ((l >> 4) << 1) | ((l >> 1) & 1), (((l >> 2) & 3) << 1) | (l & 1)
+
+
+def test_lane_map_is_a_bijection():
+    assert sorted(_lane_rc(l) for l in range(32)) == [(r, c) for r in range(4) for c in range(8)]
+
+
+def test_wavefront_rule_reproduces_the_probe():
+    # Values measured on GB300 for 32 lanes reading 16-byte chunk f(l)
+    # (or 8-byte word f(l) for the 8-byte loads).
+    cases16 = {lambda l: 0: 2, lambda l: l >> 3: 2, lambda l: l >> 4: 2, lambda l: l & 1: 2,
+               lambda l: (l >> 2) & 1: 2, lambda l: l >> 2: 2, lambda l: (l >> 1) & 3: 2,
+               lambda l: l & 7: 4, lambda l: (l & 1) + 2 * (l >> 4): 2,
+               lambda l: (l >> 1) & 7: 2, lambda l: l >> 1: 2,
+               lambda l: ((l >> 3) & 1) + 2 * (l & 1): 2}
+    for f, wf in cases16.items():
+        assert _wavefronts([16 * f(l) for l in range(32)], 16) == wf
+    cases8 = {lambda l: 0: 1, lambda l: l >> 3: 1, lambda l: l & 7: 2,
+              lambda l: (l >> 1) & 3: 1, lambda l: (l >> 1) & 7: 1, lambda l: l >> 1: 1}
+    for f, wf in cases8.items():
+        assert _wavefronts([8 * f(l) for l in range(32)], 8) == wf
+    assert _wavefronts([128 * (l >> 3) for l in range(32)], 16) == 4   # bank conflict
+
+
+def test_fragment_reads_take_the_minimum_wavefronts():
+    # Warp (wm, wn) of a 4 x 2 grid; lane (tr, tc) owns rows 32 wm + tr + 4 i
+    # and columns (BN/2) wn + 4 tc + 32 h.  A reads: 16 bytes (four k-steps)
+    # of one row; B reads: 16 bytes of one k row.  Both must deliver 8 bytes
+    # per lane per wavefront: 2 wavefronts each.
     for wm in range(4):
         for i in range(8):
             for kq in range(8):
-                addrs = [4 * dg.gemm_smem_layout_offset(0, 32 * wm + (l // 8) + 4 * i, 4 * kq)
+                addrs = [4 * dg.gemm_smem_layout_offset(0, 32 * wm + _lane_rc(l)[0] + 4 * i, 4 * kq)
                          for l in range(32)]
-                assert _wavefronts(addrs, 16) == 1, (wm, i, kq)
-    # B reads: 16 bytes at column 64 wn + 4 tc (+32) of one k row.
-    for wn in range(2):
-        for k in range(32):
-            for h in range(2):
-                addrs = [4 * dg.gemm_smem_layout_offset(1, k, 64 * wn + 4 * (l % 8) + 32 * h)
-                         for l in range(32)]
-                assert _wavefronts(addrs, 16) == 1
+                assert _wavefronts(addrs, 16) == 2, (wm, i, kq)
+    for layout, bn in ((1, 128), (2, 256)):
+        for wn in range(2):
+            for k in range(32):
+                for h in range(bn // 64):
+                    addrs = [4 * dg.gemm_smem_layout_offset(
+                        layout, k, (bn // 2) * wn + 4 * _lane_rc(l)[1] + 32 * h) for l in range(32)]
+                    assert _wavefronts(addrs, 16) == 2
+    assert dg.gemm_smem_layout_offset(2, 0, 255) == 255
+    assert dg.gemm_smem_layout_offset(1, 0, 128) == -1
+
+
+def test_row_major_lane_map_would_cost_more():
+    # With lanes laid out row-major (tc = l % 8) a 4-lane group reads 4 B
+    # chunks and the B reads cost 4 wavefronts: the check above can tell the
+    # two lane maps apart.
+    addrs = [4 * dg.gemm_smem_layout_offset(1, 0, 4 * (l % 8)) for l in range(32)]
+    assert _wavefronts(addrs, 16) == 4
 
 
 def test_cp_async_tile_writes_are_conflict_free():
@@ -178,14 +241,15 @@ def test_cp_async_tile_writes_are_conflict_free():
         for j in range(16):
             addrs = [4 * dg.gemm_smem_layout_offset(0, w + 8 * j, l) for l in range(32)]
             assert _wavefronts(addrs, 4) == 1
-    for k in range(32):
-        for c0 in range(0, 128, 32):
-            addrs = [4 * dg.gemm_smem_layout_offset(1, k, c0 + l) for l in range(32)]
-            assert _wavefronts(addrs, 4) == 1
+    for layout, bn in ((1, 128), (2, 256)):
+        for k in range(32):
+            for c0 in range(0, bn, 32):
+                addrs = [4 * dg.gemm_smem_layout_offset(layout, k, c0 + l) for l in range(32)]
+                assert _wavefronts(addrs, 4) == 1
 
 
 def test_naive_row_major_a_tile_would_conflict():
-    # The same A read pattern on an unswizzled tile is a 4-way conflict: the
-    # check above is able to see one.
-    addrs = [4 * ((l // 8) * 32 + 0) for l in range(32)]
+    # The A read pattern on an unswizzled tile (rows 128 bytes apart) is a
+    # bank conflict: the check above is able to see one.
+    addrs = [4 * (_lane_rc(l)[0] * 32 + 0) for l in range(32)]
     assert _wavefronts(addrs, 16) == 4
