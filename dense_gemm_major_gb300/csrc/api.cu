@@ -128,6 +128,16 @@ inline bool overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Measurement override: DENSE_GEMM_TC_SPLIT=0 turns off the column split of
+// the last partial round of FP16/BF16 tiles.
+bool tc_split_disabled() {
+  static const bool v = [] {
+    const char* s = std::getenv("DENSE_GEMM_TC_SPLIT");
+    return s != nullptr && std::strcmp(s, "0") == 0;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_SGEMM_TILE=narrow|wide forces the FP32
 // tile configuration (0 = no override).
 int forced_sgemm_tn() {
@@ -195,6 +205,7 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
     const int rem = plan->tiles % slots;
     const int nk = ceil_div(K, dgemm::kSgemmBK);
     plan->split_tiles = (rem > 0 && 2 * rem <= slots && nk >= 2) ? rem : 0;
+    plan->split_pieces = plan->split_tiles ? 2 : 1;
     plan->ctas = plan->tiles + plan->split_tiles;
     return GEMM_OK;
   }
@@ -208,7 +219,12 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   plan->stages = dgemm::kTcStages;
   plan->threads = dgemm::kTcThreads;
   plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
-  plan->ctas = plan->tiles < sms ? plan->tiles : sms;
+  dgemm::TcSplit sp = dgemm::tc_split(plan->tiles, sms);
+  if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
+  plan->split_tiles = sp.split_tiles;
+  plan->split_pieces = sp.parts;
+  const int units = plan->tiles + sp.split_tiles * (sp.parts - 1);
+  plan->ctas = units < sms ? units : sms;
   plan->smem_bytes = dgemm::kTcSmemBytes;
   return GEMM_OK;
 }
@@ -278,10 +294,12 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.K = K;
     p.tiles_m = ceil_div(M, dgemm::kTcBM);
     p.tiles_n = ceil_div(N, dgemm::kTcBN);
+    p.full_tiles = plan.tiles - plan.split_tiles;
+    p.split_tiles = plan.split_tiles;
+    p.parts = plan.split_pieces;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
-    const int grid = plan.tiles < dev->sms ? plan.tiles : dev->sms;
-    e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, grid, stream);
+    e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, plan.ctas, stream);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -13,7 +13,10 @@
 //
 // GB300-specific choices (no page gives a tcgen05 kernel):
 //  * Persistent grid, at most one CTA per SM, static round-robin over
-//    128 x 256 output tiles in groups of 8 tile rows (L2 reuse).
+//    128 x 256 output tiles in groups of 8 tile rows (L2 reuse).  The tiles
+//    of a last partial round run as 2 or 4 column parts (N = 128 or 64 per
+//    tcgen05.mma, full K each), so that round ends sooner without any
+//    cross-CTA reduction: results are the same bits as unsplit tiles.
 //  * Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator and MMA
 //    issuer (one thread issues every tcgen05.mma), warps 2-5 = epilogue (each
 //    owns the 32 TMEM lanes its warp index mod 4 may access).
@@ -79,14 +82,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor for kind::f16: FP32 accumulator, A and B of one
-// type (0 = FP16, 1 = BF16), A K-major, B N-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type) {
+// type (0 = FP16, 1 = BF16), A K-major, B N-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, uint32_t n) {
   return (1u << 4)                 // D format: FP32
          | (ab_type << 7)          // A format
          | (ab_type << 10)         // B format
          | (0u << 15)              // A major: K
          | (1u << 16)              // B major: MN
-         | ((uint32_t)(BN >> 3) << 17)
+         | ((n >> 3) << 17)
          | ((uint32_t)(BM >> 4) << 24);
 }
 
@@ -158,14 +161,28 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void tile_coords(int t, const TcParams& p, int& tm, int& tn) {
-  const int per_group = kTcGroupM * p.tiles_n;
-  const int group = t / per_group;
-  const int first_m = group * kTcGroupM;
-  const int gsize = min(p.tiles_m - first_m, kTcGroupM);
-  const int r = t - group * per_group;
-  tm = first_m + r % gsize;
-  tn = r / gsize;
+// Work unit u of the persistent grid: output tile (tm, tn) in grouped raster
+// order and the columns [n_off, n_off + n_w) of it that the unit computes
+// (the whole 256 columns, or one of 2 or 4 parts of a split tile).
+struct Unit {
+  int tm, tn, n_off, n_w;
+};
+__device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
+  Unit w;
+  int tile;
+  if (u < p.full_tiles) {
+    tile = u;
+    w.n_off = 0;
+    w.n_w = BN;
+  } else {
+    const int j = u - p.full_tiles;
+    const int part = j % p.parts;
+    tile = p.full_tiles + j / p.parts;
+    w.n_w = BN / p.parts;
+    w.n_off = part * w.n_w;
+  }
+  grouped_tile(tile, p.tiles_m, p.tiles_n, kTcGroupM, w.tm, w.tn);
+  return w;
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
@@ -198,7 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int num_units = p.full_tiles + p.split_tiles * p.parts;
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -231,9 +248,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------ TMA producer
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(t, p, tm, tn);
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Unit w = unit_of(u, p);
+      const int tm = w.tm, tn = w.tn;
+      const int boxes = w.n_w / 64;   // B boxes (64 columns each) this unit needs
       for (int kt = 0; kt < nk; ++kt, ++it) {
         const uint32_t s = it % S;
         const uint32_t ph = (it / S) & 1u;
@@ -241,12 +259,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = smem_u32(&bars->full[s]);
-          mbar_arrive_expect_tx(fb, kStageBytes);
+          mbar_arrive_expect_tx(fb, kABytes + boxes * kBBoxBytes);
           tma_load_2d(smem_u32(sA + s * kABytes), &tmA, fb, kt * BK, tm * BM);
           const uint32_t bdst = smem_u32(sB + s * kBBytes);
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, tn * BN + j * 64, kt * BK);
+          for (int j = 0; j < boxes; ++j)
+            tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, tn * BN + w.n_off + j * 64, kt * BK);
           issued = it + 1;
         }
         __syncwarp();
@@ -254,11 +271,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = instr_desc(kAbType);
+
     uint32_t it = 0;
     int local = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
+      const Unit w = unit_of(u, p);
+      const uint32_t idesc = instr_desc(kAbType, (uint32_t)w.n_w);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
       ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
@@ -299,48 +318,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
     int local = 0;
     int nstore = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      int tm, tn;
-      tile_coords(t, p, tm, tn);
+    // Rounds 64 FP32 columns (r0: 32, r1: the next 32) of this lane's row to
+    // T, stages them 128-byte swizzled and TMA-stores the warp's 32 x 64 box
+    // at tile column `col`.
+    auto store_box = [&](const uint32_t (&r0)[32], const uint32_t (&r1)[32], int tm, int tn,
+                         int col) {
+      unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
+      // The store issued from this buffer two boxes ago must have read it.
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+      uint32_t* row = reinterpret_cast<uint32_t*>(buf + lane * 128);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 v;
+        const uint32_t* src = ch < 4 ? &r0[ch * 8] : &r1[(ch - 4) * 8];
+        v.x = pack2<T>(__uint_as_float(src[0]), __uint_as_float(src[1]));
+        v.y = pack2<T>(__uint_as_float(src[2]), __uint_as_float(src[3]));
+        v.z = pack2<T>(__uint_as_float(src[4]), __uint_as_float(src[5]));
+        v.w = pack2<T>(__uint_as_float(src[6]), __uint_as_float(src[7]));
+        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
+                                  ((ch ^ (lane & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tmC, smem_u32(buf), tn * BN + col, tm * BM + q * 32);
+        tma_store_commit();
+      }
+      ++nstore;
+    };
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++local) {
+      const Unit w = unit_of(u, p);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-      for (int c = 0; c < BN / kTcEpiCols; ++c) {
+      const int chunks = w.n_w / kTcEpiCols;
+      for (int c = 0; c < chunks; ++c) {
         uint32_t r0[32], r1[32];
         tmem_ld32(t_row + c * kTcEpiCols, r0);
         tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
         tmem_ld_wait();
-        if (c == BN / kTcEpiCols - 1) {
-          // The accumulator buffer is free for the next tile's MMAs.
+        if (c == chunks - 1) {
+          // The accumulator buffer is free for the next unit's MMAs.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
         }
-        unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
-        // The store issued from this buffer two boxes ago must have read it.
-        if (lane == 0) tma_store_wait_read<1>();
-        __syncwarp();
-        uint32_t* row = reinterpret_cast<uint32_t*>(buf + lane * 128);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint4 v;
-          const uint32_t* src = ch < 4 ? &r0[ch * 8] : &r1[(ch - 4) * 8];
-          v.x = pack2<T>(__uint_as_float(src[0]), __uint_as_float(src[1]));
-          v.y = pack2<T>(__uint_as_float(src[2]), __uint_as_float(src[3]));
-          v.z = pack2<T>(__uint_as_float(src[4]), __uint_as_float(src[5]));
-          v.w = pack2<T>(__uint_as_float(src[6]), __uint_as_float(src[7]));
-          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
-                                    ((ch ^ (lane & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmC, smem_u32(buf), tn * BN + c * kTcEpiCols, tm * BM + q * 32);
-          tma_store_commit();
-        }
-        ++nstore;
+        store_box(r0, r1, w.tm, w.tn, w.n_off + c * kTcEpiCols);
       }
     }
     if (lane == 0) tma_store_wait_all<0>();

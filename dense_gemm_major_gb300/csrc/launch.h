@@ -91,9 +91,33 @@ constexpr int kTcSmemBytes =
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n;
+  // Work units: tiles [0, full_tiles) whole (128 x 256); each later tile
+  // as `parts` consecutive units of 128 x (256 / parts) columns, each over
+  // the full K range.
+  int full_tiles;
+  int split_tiles;
+  int parts;
   unsigned* fault;
   unsigned long long timeout_ns;
 };
+
+// Split of an FP16/BF16 problem on `sms` persistent CTAs: the tiles of the
+// last partial round (all tiles when there are fewer than `sms`) run as 2 or
+// 4 narrower column parts when that many parts per tile fit in the round.
+struct TcSplit {
+  int split_tiles;
+  int parts;
+};
+inline TcSplit tc_split(int tiles, int sms) {
+  TcSplit sp{0, 1};
+  const int rem = tiles % sms;
+  if (rem == 0) return sp;
+  const int fit = sms / rem;
+  if (fit < 2) return sp;
+  sp.split_tiles = rem;
+  sp.parts = fit >= 4 ? 4 : 2;
+  return sp;
+}
 
 // dtype: 1 = FP16, 2 = BF16.  tmA: A as {K, M} with 64 x 128 boxes;
 // tmB: B as {N, K} with 64 x 64 boxes; tmC: C as {N, M} with 64 x 32 boxes;

@@ -25,8 +25,8 @@
  *  - C is overwritten (no alpha / beta); columns j >= N of padded C rows are
  *    never written.
  *  - Every pointer is caller-owned DEVICE memory of the current device.  The
- *    library allocates no device memory per call and never synchronises: the
- *    work is queued on `stream` and the call returns.
+ *    library allocates no device memory and never synchronises: the work is
+ *    queued on `stream` and the call returns.
  *  - Accumulation is FP32 in every type.  FP16 / BF16 results are rounded to
  *    nearest-even once, from the FP32 accumulator.
  *  - Errors: argument problems are reported synchronously, before anything
@@ -127,10 +127,13 @@ typedef struct gemm_plan_t {
   int ctas;          /* grid size                         */
   int tiles;         /* output tiles                      */
   int smem_bytes;    /* dynamic shared memory per CTA     */
-  int split_tiles;   /* FP32: tiles computed as two k-halves that are
-                        added into C (zeroed first); these are the tiles of
-                        the last partial wave, or all tiles of a grid that
-                        fills at most half of the CTA slots               */
+  int split_tiles;   /* tiles of the last partial wave (or of a grid that
+                        fills at most half of the CTA slots) that run as
+                        split_pieces smaller work units                   */
+  int split_pieces;  /* 1 when nothing is split.  FP32: 2 k-halves whose
+                        FP32 partials are added into C after zeroing it.
+                        FP16/BF16: 2 or 4 column parts of the 128 x 256
+                        tile, each over the full K range                  */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,

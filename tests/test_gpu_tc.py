@@ -122,3 +122,38 @@ def test_tc_repeat_is_deterministic(dg):
     C1 = run_gemm(dg, Ad, Bd)
     C2 = run_gemm(dg, Ad, Bd)
     assert torch.equal(C1, C2)
+
+
+def _plan(dg, dtype, M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = dg.gemm_plan(dtype, M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)
+    return plan
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(4096, 4096, 256), (256, 512, 1024), (256, 25856, 512),
+                                   (128, 256, 200), (384, 768, 8200), (1000, 2000, 64)])
+def test_tc_split_tiles(dg, dtype, shape):
+    # Tiles of the last partial round run as 2 or 4 column parts (N = 128 or
+    # 64 per MMA, full K each); C starts as NaN, so a column a part misses
+    # shows up.
+    M, N, K = shape
+    plan = _plan(dg, dtype, M, N, K)
+    assert plan.split_tiles > 0 and plan.split_pieces in (2, 4), (plan.split_tiles, plan.split_pieces)
+    w = workloads.Workload(f"{dtype}_split", dtype, M, N, K, "normal", 71)
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    rows = None if M * N * K < 4e9 else workloads.sample_rows(M, 48, seed=71)
+    compare(dtype, A, B, C, rows=rows)
+    C2 = run_gemm(dg, A.cuda(), B.cuda())
+    assert torch.equal(C, C2)
+
+
+def test_bf16_split_integer_exact(dg):
+    # {-1, 0, 1} with K = 256: the FP32 accumulator is exact and |C| <= 256
+    # is exact in BF16; 56 of the 512 tiles run as column parts.
+    w = workloads.Workload("bf16_split_int", "bf16", 4096, 4096, 256, "int", 72, -1, 1)
+    assert _plan(dg, "bf16", w.M, w.N, w.K).split_tiles == 56
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare("bf16", A, B, C, rows=workloads.sample_rows(w.M, 96, seed=72), exact=True)

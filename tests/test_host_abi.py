@@ -126,12 +126,26 @@ def test_plan_paths():
         ok, p = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
                              FAKE + (2 << 30), 4096, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA
+        # 512 tiles = 3 x 152 + 56: the last 56 tiles run as 2 column parts
         assert p.tiles == 32 * 16 and p.ctas == 152
+        assert (p.split_tiles, p.split_pieces) == (56, 2)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA and p.tiles == 33 * 12
         ok, p = dg.gemm_plan(dt, 2, 3, 4, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, num_sms=152)
-        assert ok == dg.GEMM_OK and p.ctas == 1
+        assert ok == dg.GEMM_OK and (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 1, 4, 4)
+        # 4 tiles: every tile runs as 4 column parts on 16 CTAs
+        ok, p = dg.gemm_plan(dt, 256, 512, 1024, FAKE, 1024, FAKE + (1 << 30), 512,
+                             FAKE + (2 << 30), 512, num_sms=152)
+        assert (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (4, 4, 4, 16)
+        # 8192^3: 2048 tiles = 13 x 152 + 72 -> 2 parts; the edge shape:
+        # 396 tiles = 2 x 152 + 92 -> no split
+        ok, p = dg.gemm_plan(dt, 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
+                             FAKE + (2 << 30), 8192, num_sms=152)
+        assert (p.split_tiles, p.split_pieces) == (72, 2)
+        ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
+                             FAKE + (2 << 30), 3000, num_sms=152)
+        assert (p.split_tiles, p.split_pieces) == (0, 1)
         # lda not a multiple of 8 elements, or a 2-byte aligned base: refused
         ok, _ = dg.gemm_plan(dt, 64, 64, 60, FAKE, 60, FAKE + 4096, 64, FAKE + 65536, 64)
         assert ok == dg.GEMM_ERR_MISALIGNED
