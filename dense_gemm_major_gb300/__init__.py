@@ -42,7 +42,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("block_m", ctypes.c_int), ("block_n", ctypes.c_int),
                 ("block_k", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int)]
+                ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int),
+                ("cluster_ctas", ctypes.c_int)]
 
 
 _lib = None

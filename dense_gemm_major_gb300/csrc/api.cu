@@ -138,6 +138,19 @@ bool tc_split_disabled() {
   return v;
 }
 
+// Measurement override: DENSE_GEMM_TC_KERNEL=single|pair forces the FP16/BF16
+// kernel (0 = no override, 1 = single CTAs, 2 = CTA pairs).
+int forced_tc_kernel() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_TC_KERNEL");
+    if (s == nullptr) return 0;
+    if (std::strcmp(s, "single") == 0) return 1;
+    if (std::strcmp(s, "pair") == 0) return 2;
+    return 0;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_SGEMM_TILE=narrow|wide forces the FP32
 // tile configuration (0 = no override).
 int forced_sgemm_tn() {
@@ -213,11 +226,33 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda % 8) || (ldb % 8) || (ldc % 8))
     return GEMM_ERR_MISALIGNED;
   plan->path = GEMM_PATH_TC_TMA;
+  plan->threads = dgemm::kTcThreads;
+  plan->cluster_ctas = 1;
+  // CTA pairs (256 x 256 tiles, half of B staged per SM) once there are at
+  // least as many pair tiles as SM pairs; single CTAs for smaller grids.
+  const int pairs = sms / 2;
+  const int pair_tiles = ceil_div(M, 2 * dgemm::kTc2BM) * ceil_div(N, dgemm::kTc2BN);
+  const int forced = forced_tc_kernel();
+  if (pairs >= 1 && (forced == 2 || (forced == 0 && pair_tiles >= pairs))) {
+    plan->cluster_ctas = 2;
+    plan->block_m = 2 * dgemm::kTc2BM;
+    plan->block_n = dgemm::kTc2BN;
+    plan->block_k = dgemm::kTc2BK;
+    plan->stages = dgemm::kTc2Stages;
+    plan->tiles = pair_tiles;
+    dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
+    if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
+    plan->split_tiles = sp.split_tiles;
+    plan->split_pieces = sp.parts;
+    const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
+    plan->ctas = 2 * (units < pairs ? units : pairs);
+    plan->smem_bytes = dgemm::kTc2SmemBytes;
+    return GEMM_OK;
+  }
   plan->block_m = dgemm::kTcBM;
   plan->block_n = dgemm::kTcBN;
   plan->block_k = dgemm::kTcBK;
   plan->stages = dgemm::kTcStages;
-  plan->threads = dgemm::kTcThreads;
   plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
   dgemm::TcSplit sp = dgemm::tc_split(plan->tiles, sms);
   if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
@@ -292,14 +327,17 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.M = M;
     p.N = N;
     p.K = K;
-    p.tiles_m = ceil_div(M, dgemm::kTcBM);
-    p.tiles_n = ceil_div(N, dgemm::kTcBN);
+    p.tiles_m = ceil_div(M, plan.block_m);
+    p.tiles_n = ceil_div(N, plan.block_n);
     p.full_tiles = plan.tiles - plan.split_tiles;
     p.split_tiles = plan.split_tiles;
     p.parts = plan.split_pieces;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
-    e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, plan.ctas, stream);
+    if (plan.cluster_ctas == 2)
+      e = dgemm::launch_gemm_tc_pair(dtype, p, &tmA, &tmB, &tmC, plan.ctas / 2, stream);
+    else
+      e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, plan.ctas, stream);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -1,0 +1,342 @@
+// FP16 / BF16 GEMM on sm_103a tensor cores with CTA pairs: C = A . B,
+// row-major, FP32 accumulation in tensor memory, FP16 / BF16 output rounded to
+// nearest-even.
+//
+// Same five-step flow as the single-CTA kernel (GB300 GEMM roadmap,
+// m.nxbn.cn, section 4.2: TMA -> shared memory -> tcgen05.mma into TMEM ->
+// tcgen05.ld -> epilogue), and the same reading of its section 1.1 that the
+// data supply limits a GEMM here: a trace of the single-CTA kernel showed
+// its MMA thread waiting for loaded stages 27-29 % of the time, with a
+// 4-stage ring of 48 KB stages being all the shared memory there is.
+//
+// A cluster of two CTAs on two SMs computes a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA stages its own 128 rows of A
+// and its own half (128 columns) of B, and the MMA reads the peer's half
+// through the cluster.  Per SM that is 32 KB per 64-deep k-tile instead of
+// 48 KB, so six stages fit and each SM fetches a third fewer operand bytes
+// per FLOP.
+//
+// Roles per CTA (192 threads): warp 0 TMA producer, warp 1 TMEM allocator
+// (both CTAs) and MMA issuer (even CTA only, one thread), warps 2-5 epilogue
+// (each CTA drains its own 128 TMEM lanes).  Barriers:
+//  * full[s]   (even CTA): both CTAs' TMA loads complete on it; the even
+//              CTA's producer posts the pair's byte count;
+//  * empty[s]  (each CTA): arrived by a multicast tcgen05.commit once the
+//              MMAs reading stage s are done;
+//  * acc_full  (each CTA): multicast commit after a unit's last k-tile;
+//  * acc_empty (even CTA): both CTAs' epilogue warps arrive (8 arrivals).
+// The tiles of a last partial round run as two 128-column parts.  Every
+// wait is bounded; a wait that gives up records a fault and the roles unwind.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace dgemm {
+namespace {
+
+constexpr int BM = kTc2BM;            // rows per CTA (256 per pair)
+constexpr int BN = kTc2BN;            // columns per pair tile
+constexpr int BK = kTc2BK;
+constexpr int S = kTc2Stages;
+constexpr int UMMA_K = 16;
+constexpr uint32_t kABytes = BM * BK * 2;          // 16 KB
+constexpr uint32_t kBBoxBytes = 64 * BK * 2;       // one 64-column box: 8 KB
+constexpr uint32_t kBBytes = (BN / 2) * BK * 2;    // this CTA's half of B: 16 KB
+constexpr uint32_t kEpiBufBytes = 32 * kTcEpiCols * 2;
+constexpr int kAccBufs = kTc2AccBufs;              // accumulator buffers in TMEM
+constexpr uint32_t kTmemCols = kAccBufs * BN;
+constexpr int kEpiWarps = 4;
+
+static_assert(BK * 2 == 128, "A rows of a stage are one 128-byte swizzle row");
+static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
+
+struct alignas(8) Barriers {
+  uint64_t full[S];
+  uint64_t empty[S];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Work unit u of the pair-persistent grid: 256 x 256 tile (tm, tn) and the
+// columns [n_off, n_off + n_w) of it (all 256, or one of two 128-column
+// parts of a tile of the last partial round).
+struct Unit {
+  int tm, tn, n_off, n_w;
+};
+__device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
+  Unit w;
+  int tile;
+  if (u < p.full_tiles) {
+    tile = u;
+    w.n_off = 0;
+    w.n_w = BN;
+  } else {
+    const int j = u - p.full_tiles;
+    tile = p.full_tiles + j / p.parts;
+    w.n_w = BN / p.parts;
+    w.n_off = (j % p.parts) * w.n_w;
+  }
+  grouped_tile(tile, p.tiles_m, p.tiles_n, kTcGroupM, w.tm, w.tn);
+  return w;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcParams& p,
+                                          Barriers* bars, unsigned fault_code) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0) {
+    ok = mbar_wait_bounded(bar, parity, p.timeout_ns, &bars->abort) ? 1 : 0;
+    if (!ok) {
+      if (!*(volatile int*)&bars->abort) raise_fault(p.fault, fault_code);
+      *(volatile int*)&bars->abort = 1;
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <typename T, uint32_t kAbType>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+  unsigned char* sA = reinterpret_cast<unsigned char*>(base);
+  unsigned char* sB = sA + S * kABytes;
+  unsigned char* sEpi = sB + S * kBBytes;
+  Barriers* bars = reinterpret_cast<Barriers*>(sEpi + kEpiWarps * 2 * kEpiBufBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();     // 0: issues the MMAs
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int num_units = p.full_tiles + p.split_tiles * p.parts;
+  const int nk = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->acc_full[b]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();     // the peer's barriers are initialised
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+  if (rank == 1 && threadIdx.x == 0) {
+    // The pair's MMAs address both CTAs' TMEM at the even CTA's base.
+    uint32_t leader_base;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(leader_base)
+                 : "r"(mapa_shared(smem_u32(&bars->tmem_base), 0)));
+    if (leader_base != tmem_base) raise_fault(p.fault, kFaultTcPairTmem);
+  }
+
+  uint32_t issued = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = pair; u < num_units && ok; u += npairs) {
+      const Unit w = unit_of(u, p);
+      const int half = w.n_w / 2;          // columns of B this CTA stages
+      const int boxes = half / 64;
+      for (int kt = 0; kt < nk; ++kt, ++it) {
+        const uint32_t s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        ok = warp_wait(smem_u32(&bars->empty[s]), ph ^ 1u, p, bars, kFaultTcProducerWait);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t fb = mapa_shared(smem_u32(&bars->full[s]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * (kABytes + boxes * kBBoxBytes));
+          tma_load_2d_pair(smem_u32(sA + s * kABytes), &tmA, fb, kt * BK,
+                           w.tm * (2 * BM) + (int)rank * BM);
+          const uint32_t bdst = smem_u32(sB + s * kBBytes);
+          for (int j = 0; j < boxes; ++j)
+            tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb,
+                             w.tn * BN + w.n_off + (int)rank * half + j * 64, kt * BK);
+          issued = it + 1;
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0) {
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = pair; u < num_units && ok; u += npairs, ++local) {
+        const Unit w = unit_of(u, p);
+        const uint32_t idesc = instr_desc(kAbType, 2 * BM, (uint32_t)w.n_w);
+        const uint32_t b = local % kAccBufs;
+        const uint32_t aph = (local / kAccBufs) & 1u;
+        ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const uint32_t s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          ok = warp_wait(smem_u32(&bars->full[s]), ph, p, bars, kFaultTcMmaWait);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sA + s * kABytes);
+            const uint32_t b0 = smem_u32(sB + s * kBBytes);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              const uint64_t ad = smem_desc(a0 + k * UMMA_K * 2, 16, 1024);
+              const uint64_t bd = smem_desc(b0 + k * UMMA_K * 128, kBBoxBytes, 1024);
+              mma_f16_pair(d_tmem, ad, bd, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+            }
+            // Both CTAs' stage s is free once these MMAs finish.
+            mma_commit_pair_multicast(smem_u32(&bars->empty[s]), 0x3);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit_pair_multicast(smem_u32(&bars->acc_full[b]), 0x3);
+        __syncwarp();
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
+    int local = 0;
+    int nstore = 0;
+    for (int u = pair; u < num_units; u += npairs, ++local) {
+      const Unit w = unit_of(u, p);
+      const uint32_t b = local % kAccBufs;
+      const uint32_t aph = (local / kAccBufs) & 1u;
+      if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      const int row0 = w.tm * (2 * BM) + (int)rank * BM + q * 32;
+      const int chunks = w.n_w / kTcEpiCols;
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_row + c * kTcEpiCols, r0);
+        tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
+        tmem_ld_wait();
+        if (c == chunks - 1) {
+          // This CTA's half of the accumulator is drained.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[b]), 0));
+        }
+        unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
+        if (lane == 0) tma_store_wait_read<1>();
+        __syncwarp();
+        uint32_t* row = reinterpret_cast<uint32_t*>(buf + lane * 128);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 v;
+          const uint32_t* src = ch < 4 ? &r0[ch * 8] : &r1[(ch - 4) * 8];
+          v.x = pack2<T>(__uint_as_float(src[0]), __uint_as_float(src[1]));
+          v.y = pack2<T>(__uint_as_float(src[2]), __uint_as_float(src[3]));
+          v.z = pack2<T>(__uint_as_float(src[4]), __uint_as_float(src[5]));
+          v.w = pack2<T>(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
+                                    ((ch ^ (lane & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), w.tn * BN + w.n_off + c * kTcEpiCols, row0);
+          tma_store_commit();
+        }
+        ++nstore;
+      }
+    }
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------ teardown
+  if (warp == 1 && rank == 0 && lane == 0) {
+    // Every MMA of the pair has completed before TMEM is freed.
+    mma_commit_pair_multicast(smem_u32(&bars->drain), 0x1);
+    if (!mbar_wait_bounded(smem_u32(&bars->drain), 0, p.timeout_ns, nullptr))
+      raise_fault(p.fault, kFaultDrainWait);
+  }
+  if (warp == 0 && lane == 0 && rank == 0 && bars->abort) {
+    // Let in-flight loads (both CTAs count on the even CTA's barriers) land.
+    const uint32_t first = issued > (uint32_t)S ? issued - S : 0;
+    for (uint32_t it = first; it < issued; ++it) {
+      if (!mbar_wait_bounded(smem_u32(&bars->full[it % S]), (it / S) & 1u, p.timeout_ns,
+                             nullptr)) {
+        raise_fault(p.fault, kFaultDrainWait);
+        break;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();     // neither CTA leaves while the pair may still touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+template <typename T, uint32_t kAb>
+cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                         const CUtensorMap* tmC, int pairs, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<T, kAb>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kTc2SmemBytes);
+  if (e != cudaSuccess) return e;
+  gemm_tc_pair_kernel<T, kAb><<<2 * pairs, kTcThreads, kTc2SmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static_assert(sizeof(Barriers) <= 256, "barrier block must fit its reserved space");
+
+cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap* tmA,
+                                const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,
+                                cudaStream_t stream) {
+  if (dtype == 1) return launch_typed<__half, 0>(p, tmA, tmB, tmC, pairs, stream);
+  return launch_typed<__nv_bfloat16, 1>(p, tmA, tmB, tmC, pairs, stream);
+}
+
+}  // namespace dgemm

@@ -126,6 +126,37 @@ cudaError_t launch_gemm_tc(int dtype, const TcParams& p, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, const CUtensorMap* tmC, int grid,
                            cudaStream_t stream);
 
+// ---------------------------------------------------------------- FP16/BF16 CTA pairs
+
+// A cluster of two CTAs computes a 256 x 256 tile with tcgen05.mma.cta_group::2;
+// each CTA stages 128 rows of A and 128 columns of B per 64-deep k-tile in a
+// 6-stage ring.  Same 192-thread role layout as the single-CTA kernel.
+constexpr int kTc2BM = 128;              // rows per CTA
+constexpr int kTc2BN = 256;              // columns per pair tile
+constexpr int kTc2BK = 64;
+constexpr int kTc2Stages = 6;
+constexpr int kTc2AccBufs = 2;           // accumulator buffers (256 TMEM columns each)
+constexpr int kTc2SmemBytes =
+    kTc2Stages * (kTc2BM * kTc2BK + kTc2BK * (kTc2BN / 2)) * 2   // A and B-half ring
+    + 4 * 2 * 32 * kTcEpiCols * 2                                  // epilogue staging
+    + 1024 /*align*/ + 256 /*barriers*/;
+
+// Pair version of tc_split: the tiles of the last partial round run as two
+// 128-column parts when that fits the round.
+inline TcSplit tc_pair_split(int tiles, int pairs) {
+  TcSplit sp{0, 1};
+  const int rem = tiles % pairs;
+  if (rem == 0 || 2 * rem > pairs) return sp;
+  sp.split_tiles = rem;
+  sp.parts = 2;
+  return sp;
+}
+
+// tiles_m / tiles_n in p count 256 x 256 tiles; grid = 2 * pairs CTAs.
+cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap* tmA,
+                                const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,
+                                cudaStream_t stream);
+
 // ---------------------------------------------------------------- zero fill
 
 // C[i][j] = 0 for i < M, j < N (row-major, leading dimension ldc, element

@@ -150,6 +150,7 @@ enum FaultCode : unsigned {
   kFaultTcEpilogueWait = 1u << 3,
   kFaultSelftestWait = 1u << 4,
   kFaultDrainWait = 1u << 5,
+  kFaultTcPairTmem = 1u << 6,   // the two CTAs of a pair got different TMEM bases
 };
 
 __device__ __forceinline__ void raise_fault(unsigned* fault, unsigned code) {

@@ -132,8 +132,10 @@ typedef struct gemm_plan_t {
                         split_pieces smaller work units                   */
   int split_pieces;  /* 1 when nothing is split.  FP32: 2 k-halves whose
                         FP32 partials are added into C after zeroing it.
-                        FP16/BF16: 2 or 4 column parts of the 128 x 256
+                        FP16/BF16: 2 or 4 column parts of the output
                         tile, each over the full K range                  */
+  int cluster_ctas;  /* FP16/BF16: 2 when CTA pairs (tcgen05 cta_group::2)
+                        compute 256 x 256 tiles, else 1                   */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,

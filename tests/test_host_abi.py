@@ -126,26 +126,34 @@ def test_plan_paths():
         ok, p = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
                              FAKE + (2 << 30), 4096, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA
-        # 512 tiles = 3 x 152 + 56: the last 56 tiles run as 2 column parts
-        assert p.tiles == 32 * 16 and p.ctas == 152
-        assert (p.split_tiles, p.split_pieces) == (56, 2)
+        # CTA pairs: 256 tiles of 256 x 256 = 3 x 76 + 28; the last 28 tiles
+        # run as 2 column parts
+        assert (p.cluster_ctas, p.block_m, p.block_n, p.stages) == (2, 256, 256, 6)
+        assert p.tiles == 16 * 16 and p.ctas == 152
+        assert (p.split_tiles, p.split_pieces) == (28, 2)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
-        assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA and p.tiles == 33 * 12
+        assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA and p.tiles == 17 * 12
+        assert p.cluster_ctas == 2
         ok, p = dg.gemm_plan(dt, 2, 3, 4, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, num_sms=152)
         assert ok == dg.GEMM_OK and (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 1, 4, 4)
+        assert p.cluster_ctas == 1 and (p.block_m, p.block_n) == (128, 256)
         # 4 tiles: every tile runs as 4 column parts on 16 CTAs
         ok, p = dg.gemm_plan(dt, 256, 512, 1024, FAKE, 1024, FAKE + (1 << 30), 512,
                              FAKE + (2 << 30), 512, num_sms=152)
         assert (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (4, 4, 4, 16)
-        # 8192^3: 2048 tiles = 13 x 152 + 72 -> 2 parts; the edge shape:
-        # 396 tiles = 2 x 152 + 92 -> no split
+        # 8192^3: 1024 pair tiles = 13 x 76 + 36 -> 2 parts; the edge shape:
+        # 204 pair tiles = 2 x 76 + 52 -> no split
         ok, p = dg.gemm_plan(dt, 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
                              FAKE + (2 << 30), 8192, num_sms=152)
-        assert (p.split_tiles, p.split_pieces) == (72, 2)
+        assert (p.cluster_ctas, p.split_tiles, p.split_pieces) == (2, 36, 2)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
         assert (p.split_tiles, p.split_pieces) == (0, 1)
+        # fewer pair tiles than SM pairs: single CTAs (2048 x 1024: 32 tiles)
+        ok, p = dg.gemm_plan(dt, 2048, 1024, 512, FAKE, 512, FAKE + (1 << 30), 1024,
+                             FAKE + (2 << 30), 1024, num_sms=152)
+        assert p.cluster_ctas == 1 and p.tiles == 16 * 4
         # lda not a multiple of 8 elements, or a 2-byte aligned base: refused
         ok, _ = dg.gemm_plan(dt, 64, 64, 60, FAKE, 60, FAKE + 4096, 64, FAKE + 65536, 64)
         assert ok == dg.GEMM_ERR_MISALIGNED
