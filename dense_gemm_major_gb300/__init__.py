@@ -43,7 +43,8 @@ class Plan(ctypes.Structure):
                 ("block_k", ctypes.c_int), ("stages", ctypes.c_int), ("threads", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int),
-                ("cluster_ctas", ctypes.c_int)]
+                ("cluster_ctas", ctypes.c_int), ("splitk_slices", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_longlong)]
 
 
 _lib = None

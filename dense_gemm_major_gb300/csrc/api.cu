@@ -10,7 +10,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -37,6 +39,54 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_devices[kMaxDevices];
+
+// Split-K workspaces: one per (device, stream), grown on demand, never
+// shrunk, freed at process exit by the driver.
+struct Workspace {
+  float* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;   // guarded by g_mu
+
+gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  if (w.bytes < bytes) {
+    // Earlier work queued on this stream may still use the old buffer.
+    if (w.ptr != nullptr) {
+      if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    if (cudaMalloc(&w.ptr, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      w.ptr = nullptr;
+      return GEMM_ERR_LAUNCH;
+    }
+    w.bytes = bytes;
+  }
+  *out = w.ptr;
+  return GEMM_OK;
+}
+
+constexpr long long kSplitkWorkspaceCap = 64ll << 20;   // bytes
+
+// Slices for a split-K problem, bounded so the workspace stays under the cap.
+int splitk_slices_capped(int tiles, int slots, int nk, int M, int N) {
+  int s = dgemm::splitk_slices(tiles, slots, nk);
+  const long long slice_bytes = (long long)M * (((long long)N + 3) / 4 * 4) * 4;
+  while (s > 1 && s * slice_bytes > kSplitkWorkspaceCap) --s;
+  return s >= 2 ? s : 1;
+}
 
 unsigned long long wait_timeout_ns() {
   static const unsigned long long v = [] {
@@ -202,6 +252,25 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
     // on GB300: 4096^3 53.9 vs 53.8, 8192^3 56.5 vs 56.0, 2048^3 46.0 vs 43.9
     // TFLOP/s); smaller grids keep the narrow tile for parallelism.
     const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
+    const int nk_all = ceil_div(K, dgemm::kSgemmBK);
+    // A grid of narrow tiles that fills at most half of the CTA slots runs
+    // as split-K (k-slices into a workspace, then a reduction).
+    const int slices = forced_sgemm_tn() ? 1
+                                         : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
+    if (slices > 1) {
+      plan->block_m = dgemm::kSgemmBM;
+      plan->block_n = dgemm::sgemm_bn(8);
+      plan->block_k = dgemm::kSgemmBK;
+      plan->stages = dgemm::sgemm_stages(8);
+      plan->threads = dgemm::kSgemmThreads;
+      plan->tiles = narrow_tiles;
+      plan->smem_bytes = dgemm::sgemm_smem_bytes(8);
+      plan->split_pieces = 1;
+      plan->splitk_slices = slices;
+      plan->workspace_bytes = (long long)slices * M * (((long long)N + 3) / 4 * 4) * 4;
+      plan->ctas = narrow_tiles * slices;
+      return GEMM_OK;
+    }
     int tn = narrow_tiles > sms ? 16 : 8;
     if (const int forced = forced_sgemm_tn()) tn = forced == 16 ? 16 : 8;
     plan->block_m = dgemm::kSgemmBM;
@@ -219,6 +288,7 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
     const int nk = ceil_div(K, dgemm::kSgemmBK);
     plan->split_tiles = (rem > 0 && 2 * rem <= slots && nk >= 2) ? rem : 0;
     plan->split_pieces = plan->split_tiles ? 2 : 1;
+    plan->splitk_slices = 1;
     plan->ctas = plan->tiles + plan->split_tiles;
     return GEMM_OK;
   }
@@ -244,6 +314,7 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
     if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
     plan->split_tiles = sp.split_tiles;
     plan->split_pieces = sp.parts;
+    plan->splitk_slices = 1;
     const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
     plan->ctas = 2 * (units < pairs ? units : pairs);
     plan->smem_bytes = dgemm::kTc2SmemBytes;
@@ -254,10 +325,24 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   plan->block_k = dgemm::kTcBK;
   plan->stages = dgemm::kTcStages;
   plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
+  plan->smem_bytes = dgemm::kTcSmemBytes;
+  // A grid filling at most half of the SMs with a long K runs as split-K.
+  const int slices = tc_split_disabled() ? 1
+                                         : splitk_slices_capped(plan->tiles, sms,
+                                                                ceil_div(K, dgemm::kTcBK), M, N);
+  if (slices > 1) {
+    plan->split_pieces = 1;
+    plan->splitk_slices = slices;
+    plan->workspace_bytes = (long long)slices * M * (((long long)N + 3) / 4 * 4) * 4;
+    const int units = plan->tiles * slices;
+    plan->ctas = units < sms ? units : sms;
+    return GEMM_OK;
+  }
   dgemm::TcSplit sp = dgemm::tc_split(plan->tiles, sms);
   if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
   plan->split_tiles = sp.split_tiles;
   plan->split_pieces = sp.parts;
+  plan->splitk_slices = 1;
   const int units = plan->tiles + sp.split_tiles * (sp.parts - 1);
   plan->ctas = units < sms ? units : sms;
   plan->smem_bytes = dgemm::kTcSmemBytes;
@@ -297,6 +382,13 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.tiles_n = ceil_div(N, plan.block_n);
     p.full_tiles = plan.tiles - plan.split_tiles;
     p.split_kt = ceil_div(K, dgemm::kSgemmBK) / 2;
+    p.slices = plan.splitk_slices;
+    p.ws = nullptr;
+    p.ldw = ((long long)N + 3) / 4 * 4;
+    if (p.slices > 1) {
+      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
+      if (st != GEMM_OK) return st;
+    }
     p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
@@ -312,6 +404,8 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
         return GEMM_ERR_LAUNCH;
     }
     e = dgemm::launch_sgemm(p, tn, tma, &tmA, &tmB, stream);
+    if (e == cudaSuccess && p.slices > 1)
+      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, stream);
   } else {
     const CUtensorMapDataType dt =
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -332,12 +426,21 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.full_tiles = plan.tiles - plan.split_tiles;
     p.split_tiles = plan.split_tiles;
     p.parts = plan.split_pieces;
+    p.slices = plan.splitk_slices;
+    p.ws = nullptr;
+    p.ldw = ((long long)N + 3) / 4 * 4;
+    if (p.slices > 1) {
+      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
+      if (st != GEMM_OK) return st;
+    }
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
     if (plan.cluster_ctas == 2)
       e = dgemm::launch_gemm_tc_pair(dtype, p, &tmA, &tmB, &tmC, plan.ctas / 2, stream);
     else
       e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, plan.ctas, stream);
+    if (e == cudaSuccess && p.slices > 1)
+      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, dtype, stream);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -1,5 +1,8 @@
 // Small kernels around the GEMM path: the K == 0 product (C := 0) and the
 // self-test of the bounded mbarrier wait.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -31,7 +34,55 @@ __global__ void selftest_timeout_kernel(unsigned* fault, unsigned long long time
   if (!mbar_wait_bounded(b, 0, timeout_ns, nullptr)) raise_fault(fault, kFaultSelftestWait);
 }
 
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Sums the split-K slices of each output element in slice order and rounds
+// once.  Consecutive threads take consecutive columns (coalesced reads of
+// every slice and coalesced writes of C).
+template <typename T>
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int slices, int M, int N,
+                                     long long ldw, T* __restrict__ C, long long ldc) {
+  const long long total = (long long)M * N;
+  const long long slice_stride = (long long)M * ldw;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long i = idx / N;
+    const long long j = idx - i * N;
+    const float* src = ws + i * ldw + j;
+    float acc = __ldg(src);
+    for (int s = 1; s < slices; ++s) acc += __ldg(src + s * slice_stride);
+    C[i * ldc + j] = from_f32<T>(acc);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
+                                 void* C, long long ldc, int elem, cudaStream_t stream) {
+  const long long total = (long long)M * N;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  if (elem == 0)
+    splitk_reduce_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(
+        ws, slices, M, N, ldw, static_cast<float*>(C), ldc);
+  else if (elem == 1)
+    splitk_reduce_kernel<__half><<<(unsigned)blocks, 256, 0, stream>>>(
+        ws, slices, M, N, ldw, static_cast<__half*>(C), ldc);
+  else
+    splitk_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
+        ws, slices, M, N, ldw, static_cast<__nv_bfloat16*>(C), ldc);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_zero_fill(void* C, int M, int N, long long ldc, int elem_bytes,
                              cudaStream_t stream) {

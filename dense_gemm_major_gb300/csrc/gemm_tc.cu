@@ -69,18 +69,27 @@ struct alignas(8) Barriers {
 };
 
 // Work unit u of the persistent grid: output tile (tm, tn) in grouped raster
-// order and the columns [n_off, n_off + n_w) of it that the unit computes
-// (the whole 256 columns, or one of 2 or 4 parts of a split tile).
+// order, the columns [n_off, n_off + n_w) of it that the unit computes (the
+// whole 256 columns, or one of 2 or 4 parts of a split tile), and its k-tile
+// range [kb, ke) (a k-slice in split-K mode, else all of K).
 struct Unit {
-  int tm, tn, n_off, n_w;
+  int tm, tn, n_off, n_w, kb, ke, slice;
 };
-__device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
+__device__ __forceinline__ Unit unit_of(int u, const TcParams& p, int nk) {
   Unit w;
   int tile;
-  if (u < p.full_tiles) {
+  w.kb = 0;
+  w.ke = nk;
+  w.slice = -1;
+  w.n_off = 0;
+  w.n_w = BN;
+  if (p.slices > 1) {
+    tile = u / p.slices;
+    w.slice = u - tile * p.slices;
+    w.kb = w.slice * nk / p.slices;
+    w.ke = (w.slice + 1) * nk / p.slices;
+  } else if (u < p.full_tiles) {
     tile = u;
-    w.n_off = 0;
-    w.n_w = BN;
   } else {
     const int j = u - p.full_tiles;
     const int part = j % p.parts;
@@ -122,7 +131,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_units = p.full_tiles + p.split_tiles * p.parts;
+  const int num_units = p.slices > 1 ? p.tiles_m * p.tiles_n * p.slices
+                                     : p.full_tiles + p.split_tiles * p.parts;
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
@@ -156,10 +166,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Unit w = unit_of(u, p);
+      const Unit w = unit_of(u, p, nk);
       const int tm = w.tm, tn = w.tn;
       const int boxes = w.n_w / 64;   // B boxes (64 columns each) this unit needs
-      for (int kt = 0; kt < nk; ++kt, ++it) {
+      for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
         const uint32_t s = it % S;
         const uint32_t ph = (it / S) & 1u;
         ok = warp_wait(smem_u32(&bars->empty[s]), ph ^ 1u, p, bars, kFaultTcProducerWait);
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int local = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
-      const Unit w = unit_of(u, p);
+      const Unit w = unit_of(u, p, nk);
       const uint32_t idesc = instr_desc(kAbType, BM, (uint32_t)w.n_w);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + b * BN;
-      for (int kt = 0; kt < nk; ++kt, ++it) {
+      for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
         const uint32_t s = it % S;
         const uint32_t ph = (it / S) & 1u;
         ok = warp_wait(smem_u32(&bars->full[s]), ph, p, bars, kFaultTcMmaWait);
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             //    (leading offset), 8-row k groups 1024 bytes apart (stride).
             const uint64_t ad = smem_desc(a0 + k * UMMA_K * 2, 16, 1024);
             const uint64_t bd = smem_desc(b0 + k * UMMA_K * 128, kBBoxBytes, 1024);
-            mma_f16(d_tmem, ad, bd, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+            mma_f16(d_tmem, ad, bd, idesc, (kt > w.kb || k > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&bars->empty[s]));   // frees the stage when the MMAs finish
         }
@@ -255,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ++nstore;
     };
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++local) {
-      const Unit w = unit_of(u, p);
+      const Unit w = unit_of(u, p, nk);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
       if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
@@ -273,7 +283,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
         }
-        store_box(r0, r1, w.tm, w.tn, w.n_off + c * kTcEpiCols);
+        if (w.slice < 0) {
+          store_box(r0, r1, w.tm, w.tn, w.n_off + c * kTcEpiCols);
+        } else {
+          // Split-K: this lane's row of the FP32 partial, columns beyond the
+          // workspace width (ldw >= N, a multiple of 4) left out.
+          const int grow = w.tm * BM + q * 32 + lane;
+          const int gcol = w.tn * BN + c * kTcEpiCols;
+          if (grow < p.M) {
+            float* dst = p.ws + (long long)w.slice * p.M * p.ldw + (long long)grow * p.ldw + gcol;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (gcol + 4 * j + 3 < p.ldw) {
+                const uint32_t* src = j < 8 ? &r0[j * 4] : &r1[(j - 8) * 4];
+                *reinterpret_cast<uint4*>(dst + 4 * j) = make_uint4(src[0], src[1], src[2], src[3]);
+              }
+            }
+          }
+        }
       }
     }
     if (lane == 0) tma_store_wait_all<0>();

@@ -41,6 +41,14 @@ struct SgemmParams {
   // two addends the result does not depend on their order.
   int full_tiles;
   int split_kt;
+  // Split-K mode (slices > 1): CTA u computes k-slice u % slices of tile
+  // u / slices (k-tiles [s*nk/slices, (s+1)*nk/slices)) and stores its FP32
+  // partial tile at ws + s * M * ldw (row-major, leading dimension ldw);
+  // splitk_reduce then sums the slices in slice order into C.  full_tiles
+  // and split_kt are unused in this mode.
+  int slices;
+  float* ws;
+  long long ldw;
   int c_vec4;        // C rows may be written with 16-byte stores
   unsigned* fault;   // device fault word
   unsigned long long timeout_ns;
@@ -91,6 +99,13 @@ constexpr int kTcSmemBytes =
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n;
+  // Split-K mode (single-CTA kernel only, slices > 1): unit u is k-slice
+  // u % slices of tile u / slices, stored as an FP32 partial tile at
+  // ws + s * M * ldw; splitk_reduce sums the slices.  The column-split
+  // fields below are unused in this mode.
+  int slices;
+  float* ws;
+  long long ldw;
   // Work units: tiles [0, full_tiles) whole (128 x 256); each later tile
   // as `parts` consecutive units of 128 x (256 / parts) columns, each over
   // the full K range.
@@ -163,6 +178,25 @@ cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap*
 // size elem_bytes = 2 or 4): the K == 0 product.
 cudaError_t launch_zero_fill(void* C, int M, int N, long long ldc, int elem_bytes,
                              cudaStream_t stream);
+
+// ---------------------------------------------------------------- split-K reduce
+
+// C[i][j] = sum over s of ws[s * M * ldw + i * ldw + j], in slice order,
+// rounded once to the element type of C (elem: 0 = FP32, 1 = FP16,
+// 2 = BF16).
+cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
+                                 void* C, long long ldc, int elem, cudaStream_t stream);
+
+// Split-K slice count for a grid of `tiles` output tiles over `slots` CTA
+// slots and `nk` k-tiles: slices of at least 4 k-tiles, at most 32, when
+// the tiles fill no more than half of the slots.
+inline int splitk_slices(int tiles, int slots, int nk) {
+  if (tiles <= 0 || 2 * tiles > slots) return 1;
+  int s = slots / tiles;
+  if (s > nk / 4) s = nk / 4;
+  if (s > 32) s = 32;
+  return s >= 2 ? s : 1;
+}
 
 // ---------------------------------------------------------------- self test
 

@@ -109,18 +109,25 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int lane = tid & 31;
   const int warp = tid >> 5;
 
-  // Work unit of this CTA: a whole tile, or one of the two k-pieces of a
-  // split tile (consecutive CTAs), in grouped raster order.
+  // Work unit of this CTA: a whole tile; one of the two k-pieces of a split
+  // tile (consecutive CTAs) that add into C; or, in split-K mode, one
+  // k-slice of a tile that is stored to the workspace.
   int tile, k_begin, k_end;
-  bool add_into_c;
+  bool add_into_c = false;
+  float* part = nullptr;   // split-K: this slice's FP32 partial, row-major (ldw)
   {
     const int nk_all = (p.K + BK - 1) / BK;
     const int b = blockIdx.x;
-    if (b < p.full_tiles) {
+    if (p.slices > 1) {
+      tile = b / p.slices;
+      const int sl = b - tile * p.slices;
+      k_begin = sl * nk_all / p.slices;
+      k_end = (sl + 1) * nk_all / p.slices;
+      part = p.ws + (long long)sl * p.M * p.ldw;
+    } else if (b < p.full_tiles) {
       tile = b;
       k_begin = 0;
       k_end = nk_all;
-      add_into_c = false;
     } else {
       const int j = b - p.full_tiles;
       tile = p.full_tiles + (j >> 1);
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   for (int i = 0; i < 8; ++i) {
     const int gm = m0 + a_row0 + 4 * i;
     if (gm >= p.M) continue;
-    float* crow = p.C + (long long)gm * p.ldc;
+    float* crow = part != nullptr ? part + (long long)gm * p.ldw : p.C + (long long)gm * p.ldc;
+    const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int gn = n0 + b_col0 + 32 * h;
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       const float2 hi = unpack_pair(acc[i][2 * h + 1]);
       const float v0 = lo.x, v1 = lo.y, v2 = hi.x, v3 = hi.y;
       if (add_into_c) {
-        if (p.c_vec4 && gn + 3 < p.N) {
+        if (vec4 && gn + 3 < p.N) {
           atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
         } else {
           if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
@@ -302,7 +310,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
           if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
         }
-      } else if (p.c_vec4 && gn + 3 < p.N) {
+      } else if (vec4 && gn + 3 < p.N) {
         *reinterpret_cast<float4*>(crow + gn) = make_float4(v0, v1, v2, v3);
       } else {
         if (gn + 0 < p.N) crow[gn + 0] = v0;
@@ -338,13 +346,13 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
                                        sgemm_smem_bytes(TN));
   if (e != cudaSuccess) return e;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int split = tiles - p.full_tiles;
+  const int split = p.slices > 1 ? 0 : tiles - p.full_tiles;
   if (split > 0) {
     sgemm_zero_split_tiles<<<split, 256, 0, stream>>>(p, sgemm_bn(TN));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)(tiles + split));
+  const dim3 grid((unsigned)(p.slices > 1 ? tiles * p.slices : tiles + split));
   sgemm_kernel<kTma, TN, kMinBlocks>
       <<<grid, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
   return cudaGetLastError();

@@ -25,8 +25,14 @@
  *  - C is overwritten (no alpha / beta); columns j >= N of padded C rows are
  *    never written.
  *  - Every pointer is caller-owned DEVICE memory of the current device.  The
- *    library allocates no device memory and never synchronises: the work is
- *    queued on `stream` and the call returns.
+ *    work is queued on `stream` and the call returns without synchronising.
+ *  - Device memory: a call whose output has too few tiles to fill the GPU
+ *    and a long K runs as split-K and needs an FP32 workspace (at most
+ *    64 MiB, see gemm_plan_t.workspace_bytes).  The library owns one
+ *    workspace per (device, stream): it is allocated by the first call that
+ *    needs it and grown, after synchronising that stream, when a later call
+ *    needs more; it lives until the process exits.  Calls on different
+ *    streams never share a workspace.  All other calls allocate nothing.
  *  - Accumulation is FP32 in every type.  FP16 / BF16 results are rounded to
  *    nearest-even once, from the FP32 accumulator.
  *  - Errors: argument problems are reported synchronously, before anything
@@ -136,6 +142,11 @@ typedef struct gemm_plan_t {
                         tile, each over the full K range                  */
   int cluster_ctas;  /* FP16/BF16: 2 when CTA pairs (tcgen05 cta_group::2)
                         compute 256 x 256 tiles, else 1                   */
+  int splitk_slices; /* > 1: the grid is too small for the GPU, so each tile
+                        is computed as this many k-slices whose FP32 partial
+                        tiles go to a workspace, summed in slice order by a
+                        second kernel                                     */
+  long long workspace_bytes; /* device workspace that split-K needs        */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,

@@ -158,3 +158,45 @@ def test_f32_split_tail_integer_exact(dg):
     A, B = workloads.make(w)
     C = run_gemm(dg, A.cuda(), B.cuda())
     compare("f32", A, B, C, rows=workloads.sample_rows(w.M, 96, seed=62), exact=True)
+
+
+
+def _plan32(dg, M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)[1]
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 65536), (128, 1000, 9000), (1000, 1030, 777)])
+def test_f32_splitk(dg, shape):
+    M, N, K = shape
+    assert _plan32(dg, M, N, K).splitk_slices > 1
+    w = workloads.Workload(f"splitk{M}x{N}x{K}", "f32", M, N, K, "uniform", 91)
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare("f32", A, B, C, rows=workloads.sample_rows(M, 32, seed=91))
+    assert torch.equal(C, run_gemm(dg, A.cuda(), B.cuda()))
+
+
+def test_f32_splitk_integer_exact(dg):
+    # {-2..2}, K = 8192: partial sums stay below 2^24, so slices and their
+    # sum are exact.
+    w = workloads.Workload("splitk_int", "f32", 256, 384, 8192, "int", 92, -2, 2)
+    assert _plan32(dg, w.M, w.N, w.K).splitk_slices > 1
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare("f32", A, B, C, exact=True)
+
+
+def test_f32_splitk_padded_c_and_workspace_growth(dg):
+    # A small split-K call, then a larger one on the same stream (the
+    # workspace grows), with a padded C whose padding must stay untouched.
+    for (M, N, K) in [(64, 64, 4096), (700, 900, 3000)]:
+        assert _plan32(dg, M, N, K).splitk_slices > 1
+        w = workloads.Workload("splitk_pad", "f32", M, N, K, "uniform", 93)
+        A, B = workloads.make(w)
+        Cbuf = torch.full((M, N + 5), -7.0, device="cuda")
+        C = Cbuf[:, :N]
+        C.fill_(float("nan"))
+        run_gemm(dg, A.cuda(), B.cuda(), C)
+        compare("f32", A, B, C, rows=workloads.sample_rows(M, 32, seed=93))
+        assert torch.all(Cbuf[:, N:] == -7.0)

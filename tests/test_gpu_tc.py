@@ -139,7 +139,8 @@ def test_tc_split_tiles(dg, dtype, shape):
     # shows up.
     M, N, K = shape
     plan = _plan(dg, dtype, M, N, K)
-    assert plan.split_tiles > 0 and plan.split_pieces in (2, 4), (plan.split_tiles, plan.split_pieces)
+    assert (plan.split_tiles > 0 and plan.split_pieces in (2, 4)) or plan.splitk_slices > 1, \
+        (plan.split_tiles, plan.split_pieces, plan.splitk_slices)
     w = workloads.Workload(f"{dtype}_split", dtype, M, N, K, "normal", 71)
     A, B = workloads.make(w)
     C = run_gemm(dg, A.cuda(), B.cuda())
@@ -157,3 +158,41 @@ def test_bf16_split_integer_exact(dg):
     A, B = workloads.make(w)
     C = run_gemm(dg, A.cuda(), B.cuda())
     compare("bf16", A, B, C, rows=workloads.sample_rows(w.M, 96, seed=72), exact=True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(256, 256, 65536), (128, 1024, 8192), (300, 264, 20000)])
+def test_tc_splitk_skinny(dg, dtype, shape):
+    # Few output tiles and a long K: k-slices into an FP32 workspace, summed
+    # in slice order by a second kernel and rounded once.
+    M, N, K = shape
+    assert _plan(dg, dtype, M, N, K).splitk_slices > 1
+    w = workloads.Workload(f"{dtype}_splitk", dtype, M, N, K, "normal", 81)
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare(dtype, A, B, C, rows=workloads.sample_rows(M, 24, seed=81))
+    assert torch.equal(C, run_gemm(dg, A.cuda(), B.cuda()))
+
+
+def test_bf16_splitk_integer_rounded_exact(dg):
+    # {-1, 0, 1}, K = 4096: every FP32 partial and their sum are exact, so
+    # the output is the exact product rounded once to BF16.
+    w = workloads.Workload("bf16_splitk_int", "bf16", 256, 512, 4096, "int", 82, -1, 1)
+    assert _plan(dg, "bf16", w.M, w.N, w.K).splitk_slices > 1
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    compare("bf16", A, B, C, exact=True)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tc_splitk_padded_c(dg, dtype):
+    M, N, K = 200, 264, 4096
+    assert _plan(dg, dtype, M, N, K).splitk_slices > 1
+    w = workloads.Workload("splitk_pad", dtype, M, N, K, "uniform", 83)
+    A, B = workloads.make(w)
+    Cbuf = torch.full((M, N + 8), -3.0, dtype=A.dtype, device="cuda")
+    C = Cbuf[:, :N]
+    C.fill_(float("nan"))
+    run_gemm(dg, A.cuda(), B.cuda(), C)
+    compare(dtype, A, B, C)
+    assert torch.all(Cbuf[:, N:] == -3.0), "padding columns of C were written"

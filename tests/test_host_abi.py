@@ -100,7 +100,12 @@ def test_plan_paths():
     # a single k-tile cannot be split
     ok, p = dg.gemm_plan("f32", 1000, 1030, 32, FAKE, 32, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030, num_sms=152)
-    assert p.split_tiles == 0
+    assert p.split_tiles == 0 and p.splitk_slices == 1 and p.workspace_bytes == 0
+    # skinny: 4 tiles, K = 65536 -> 32 slices (the cap)
+    ok, p = dg.gemm_plan("f32", 256, 256, 65536, FAKE, 65536, FAKE + (1 << 34), 256,
+                         FAKE + (2 << 34), 256, num_sms=152)
+    assert (p.tiles, p.splitk_slices, p.ctas) == (4, 32, 128)
+    assert p.workspace_bytes == 32 * 256 * 256 * 4
     ok, p = dg.gemm_plan("f32", 2048, 2048, 2048, FAKE, 2048, FAKE + (1 << 30), 2048,
                          FAKE + (2 << 30), 2048, num_sms=152)
     assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles, p.split_tiles) == (256, 4, 128, 0)
@@ -112,8 +117,11 @@ def test_plan_paths():
     ok, p = dg.gemm_plan("f32", 1000, 1030, 777, FAKE, 777, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_CPASYNC
-    # 72 tiles fill less than half of the 304 slots: all split into k-halves
-    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 72 and p.ctas == 144
+    # 72 tiles fill less than half of the 304 slots: split-K, 4 slices of
+    # 6-7 k-tiles each into a 4 x 1000 x 1032 FP32 workspace
+    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 0
+    assert (p.splitk_slices, p.ctas) == (4, 288)
+    assert p.workspace_bytes == 4 * 1000 * 1032 * 4
     # misaligned base pointer (4-byte aligned only)
     ok, p = dg.gemm_plan("f32", 64, 64, 64, FAKE + 4, 64, FAKE + (1 << 30), 64,
                          FAKE + (2 << 30), 64)
@@ -137,11 +145,20 @@ def test_plan_paths():
         assert p.cluster_ctas == 2
         ok, p = dg.gemm_plan(dt, 2, 3, 4, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, num_sms=152)
         assert ok == dg.GEMM_OK and (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 1, 4, 4)
-        assert p.cluster_ctas == 1 and (p.block_m, p.block_n) == (128, 256)
-        # 4 tiles: every tile runs as 4 column parts on 16 CTAs
+        assert p.cluster_ctas == 1 and (p.block_m, p.block_n) == (128, 256) and p.splitk_slices == 1
+        # 4 tiles, 16 k-tiles: split-K, 4 slices of 4 k-tiles on 16 CTAs
         ok, p = dg.gemm_plan(dt, 256, 512, 1024, FAKE, 1024, FAKE + (1 << 30), 512,
                              FAKE + (2 << 30), 512, num_sms=152)
-        assert (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (4, 4, 4, 16)
+        assert (p.tiles, p.split_tiles, p.splitk_slices, p.ctas) == (4, 0, 4, 16)
+        assert p.workspace_bytes == 4 * 256 * 512 * 4
+        # K of 2 k-tiles is too short for split-K: 4 column parts instead
+        ok, p = dg.gemm_plan(dt, 256, 512, 128, FAKE, 128, FAKE + (1 << 30), 512,
+                             FAKE + (2 << 30), 512, num_sms=152)
+        assert (p.tiles, p.split_tiles, p.split_pieces, p.splitk_slices, p.ctas) == (4, 4, 4, 1, 16)
+        # skinny: 2 tiles, K = 65536 -> 32 slices
+        ok, p = dg.gemm_plan(dt, 256, 256, 65536, FAKE, 65536, FAKE + (1 << 34), 256,
+                             FAKE + (2 << 34), 256, num_sms=152)
+        assert (p.tiles, p.splitk_slices, p.ctas) == (2, 32, 64)
         # 8192^3: 1024 pair tiles = 13 x 76 + 36 -> 2 parts; the edge shape:
         # 204 pair tiles = 2 x 76 + 52 -> no split
         ok, p = dg.gemm_plan(dt, 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
