@@ -22,13 +22,14 @@ GEMM_ERR_MISALIGNED = 2
 GEMM_ERR_UNSUPPORTED_DEVICE = 3
 GEMM_ERR_LAUNCH = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
+GEMM_ERR_SCRATCH_LIMIT = 6
 
 PATH_NOOP, PATH_ZERO_FILL, PATH_SIMT_TMA, PATH_SIMT_CPASYNC, PATH_TC_TMA = range(5)
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 
 # Every symbol include/dense_gemm.h declares.
 EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_device_check",
-            "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout")
+            "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc")
 
 
 class GemmError(RuntimeError):
@@ -61,7 +62,7 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     i, vp = ctypes.c_int, ctypes.c_void_p
     gemm_args = [i, i, i, vp, i, vp, i, vp, i, vp]
-    for name in ("gemm_f32", "gemm_f16", "gemm_bf16"):
+    for name in ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_f32_noalloc"):
         fn = getattr(lib, name)
         fn.restype = i
         fn.argtypes = gemm_args
@@ -91,6 +92,12 @@ def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 
 def gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return load().gemm_bf16(M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_f32 for callers that cannot allocate device memory: split-K
+    partials go to the library's fixed 16 MiB device array."""
+    return load().gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
 def status_string(status: int) -> str:

@@ -451,6 +451,18 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
 
 }  // namespace
 
+namespace dgemm {
+
+// For other translation units of the library: the current device's fault
+// word (nullptr if the device is unsupported) and the bound of every wait.
+unsigned* current_fault_word() {
+  DeviceInfo* dev = nullptr;
+  return current_device(&dev) == GEMM_OK ? dev->fault : nullptr;
+}
+unsigned long long wait_bound_ns() { return wait_timeout_ns(); }
+
+}  // namespace dgemm
+
 extern "C" {
 
 gemm_status_t gemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
@@ -477,6 +489,8 @@ const char* gemm_status_string(gemm_status_t status) {
     case GEMM_ERR_UNSUPPORTED_DEVICE: return "no current CUDA device of compute capability 10.3";
     case GEMM_ERR_LAUNCH: return "kernel launch failed";
     case GEMM_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
+    case GEMM_ERR_SCRATCH_LIMIT:
+      return "split-K problem needs more scratch than the 16 MiB static array of gemm_f32_noalloc";
   }
   return "unknown status";
 }

@@ -49,7 +49,6 @@ constexpr int UMMA_K = 16;                         // K per tcgen05.mma (16-bit 
 constexpr uint32_t kABytes = BM * BK * 2;          // 16 KB
 constexpr uint32_t kBBoxBytes = 64 * BK * 2;       // one 64-column box of B: 8 KB
 constexpr uint32_t kBBytes = BN * BK * 2;          // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kEpiBufBytes = 32 * kTcEpiCols * 2;   // 4 KB
 constexpr uint32_t kTmemCols = 2 * BN;             // two accumulators
 constexpr int kEpiWarps = 4;

@@ -198,6 +198,13 @@ inline int splitk_slices(int tiles, int slots, int nk) {
   return s >= 2 ? s : 1;
 }
 
+// ---------------------------------------------------------------- shared state
+
+// The current device's fault word (nullptr if unsupported) and the bound of
+// every device-side wait, from the C-ABI translation unit.
+unsigned* current_fault_word();
+unsigned long long wait_bound_ns();
+
 // ---------------------------------------------------------------- self test
 
 // Waits on an mbarrier that nothing completes, with a `timeout_ns` bound; the

@@ -64,7 +64,9 @@ typedef enum gemm_status_t {
   GEMM_ERR_MISALIGNED = 2,         /* FP16/BF16: base or ld not 16-byte aligned */
   GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 / no device   */
   GEMM_ERR_LAUNCH = 4,             /* the CUDA launch itself failed              */
-  GEMM_ERR_DEVICE_TIMEOUT = 5      /* a kernel's bounded wait gave up            */
+  GEMM_ERR_DEVICE_TIMEOUT = 5,     /* a kernel's bounded wait gave up            */
+  GEMM_ERR_SCRATCH_LIMIT = 6       /* gemm_f32_noalloc: problem needs more
+                                      scratch than its static array holds      */
 } gemm_status_t;
 
 /*
@@ -100,6 +102,38 @@ gemm_status_t gemm_bf16(int M, int N, int K,
                         const gemm_bfloat16_t *B, int ldb,
                         gemm_bfloat16_t *C, int ldc,
                         cudaStream_t stream);
+
+/*
+ * FP32 GEMM that never allocates device memory.  The pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc, for example a serving process that reserves its whole memory
+ * budget at start-up and may not allocate afterwards, or code whose latency
+ * path cannot afford cudaMalloc's implicit synchronisation.  gemm_f32 needs a
+ * library-allocated workspace only for split-K problems (few output tiles,
+ * long K); this variant runs those with the same kernels but keeps the FP32
+ * partial tiles in one fixed, library-wide device array of 16 MiB instead.
+ *
+ * Same arguments, conventions and results as gemm_f32.  Problems that are
+ * not split-K go to gemm_f32 unchanged (it allocates nothing for them).
+ * A split-K problem whose partial tiles need more than 16 MiB
+ * (gemm_plan_t.workspace_bytes) is refused with GEMM_ERR_SCRATCH_LIMIT
+ * before anything is queued.
+ *  - Set-up: the first call on a device looks up the device address of the
+ *    array (cudaGetSymbolAddress) and that device's SM count, with the
+ *    device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps whatever the
+ *    last call wrote; nothing in it needs to start at zero (each slice is
+ *    fully written before it is read).  Calls whose work overlaps on the GPU
+ *    (different streams, no ordering between them) race on the array:
+ *    order them, e.g. keep them on one stream.
+ *  - The array stays allocated on every device that has loaded it until the
+ *    process exits.
+ */
+gemm_status_t gemm_f32_noalloc(int M, int N, int K,
+                               const float *A, int lda,
+                               const float *B, int ldb,
+                               float *C, int ldc,
+                               cudaStream_t stream);
 
 /* Static, never-null description of a status code. */
 const char *gemm_status_string(gemm_status_t status);

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(built):
 
 
 def test_status_strings():
-    for code in range(6):
+    for code in range(7):
         s = dg.status_string(code)
         assert s and s != "unknown status"
     assert dg.status_string(99) == "unknown status"
