@@ -18,6 +18,9 @@ marshals numpy arrays.  What it computes, with sources:
   (m.nxbn.cn, section 6.2) asks that correctness be judged against a
   high-precision reference with a tolerance, not by exact equality.
 * ``flops(M, N, K) = 2*M*N*K`` (m.lqnn.cn SGEMM article, section 1.1).
+* ``gemm_scaled``: ``alpha * (A @ B) + beta * C_in`` in double, the GEMM of
+  the m.lqnn.cn article's ``sgemm_tile_v2(..., alpha, beta)`` signature, with
+  the BLAS reading that ``beta == 0`` does not read C_in.
 
 Half and bfloat16 inputs are passed as their 16-bit patterns and decoded in C
 from the IEEE binary16 / bfloat16 bit layouts.
@@ -71,6 +74,12 @@ def _load():
         lib.oracle_f64_to_f16_rn.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_bf16_rn.restype = ctypes.c_uint16
         lib.oracle_f64_to_bf16_rn.argtypes = [ctypes.c_double]
+        lib.oracle_gemm_scaled_rows.restype = ctypes.c_int
+        lib.oracle_gemm_scaled_rows.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_int, i64p, dp, dp, ctypes.c_int64]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -141,6 +150,50 @@ def gemm(dtype: str, A: np.ndarray, B: np.ndarray, rows=None, with_scale: bool =
         ldc)
     if rc != 0:
         raise ValueError("oracle_gemm_rows rejected its arguments")
+    return C, S
+
+
+def gemm_scaled(dtype: str, alpha: float, A: np.ndarray, B: np.ndarray, beta: float,
+                C_in: np.ndarray | None, rows=None):
+    """Return (C, S) for alpha * (A @ B) + beta * C_in, in double.
+
+    C_in (M x N, same element type as A and B, row stride >= N) is not read
+    when beta == 0, and may then be None.  S = |alpha| sum|a b| + |beta| |c|
+    is the scale of the normalised error."""
+    code = _DTYPE_CODES[dtype]
+    A = _as_input(A, dtype)
+    B = _as_input(B, dtype)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    lda = A.strides[0] // A.itemsize if M > 0 else max(K, 1)
+    ldb = B.strides[0] // B.itemsize if K > 0 else max(N, 1)
+    if beta != 0:
+        C_in = _as_input(C_in, dtype)
+        if C_in.shape != (M, N):
+            raise ValueError("C_in must be M x N")
+        ldc_in = C_in.strides[0] // C_in.itemsize if M > 0 else max(N, 1)
+        c_ptr = C_in.ctypes.data if C_in.size else None
+    else:
+        ldc_in, c_ptr = max(N, 1), None
+    if rows is None:
+        nrows, rows_p, keep = M, None, None
+    else:
+        keep = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = int(keep.size)
+        rows_p = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    ldc = max(N, 1)
+    C = np.empty((nrows, N), dtype=np.float64)
+    S = np.empty((nrows, N), dtype=np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = _load().oracle_gemm_scaled_rows(
+        code, M, N, K, float(alpha),
+        A.ctypes.data if A.size else None, lda, B.ctypes.data if B.size else None, ldb,
+        float(beta), c_ptr, ldc_in, nrows, rows_p,
+        C.ctypes.data_as(dp) if C.size else None, S.ctypes.data_as(dp) if S.size else None, ldc)
+    if rc != 0:
+        raise ValueError("oracle_gemm_scaled_rows rejected its arguments")
     return C, S
 
 

@@ -23,6 +23,8 @@
  *   - GB300 GEMM roadmap (m.nxbn.cn), section 6.2: correctness is judged
  *     against a high-precision reference, not against another fast GEMM;
  *     S[i][j] is the scale for the normalised error |dC| / sum|a*b|.
+ *   - The scaled form alpha * A.B + beta * C (oracle_gemm_scaled_rows) is
+ *     documented beside its function.
  *
  * The only deviation from those kernels is the accumulator type: double
  * instead of float/half, so the oracle is exact up to one double rounding per
@@ -168,6 +170,41 @@ int oracle_gemm_rows(int dtype, int M, int N, int K,
                 c[j] += prod;
                 if (s) s[j] += fabs(prod);
             }
+        }
+    }
+    return 0;
+}
+
+/* The scaled update C_out = alpha * (A . B) + beta * C_in.  The m.lqnn.cn
+ * SGEMM article's tiled kernel sgemm_tile_v2 takes alpha and beta arguments
+ * (its listing leaves the beta term out), and the GB300 roadmap (m.nxbn.cn,
+ * section 7.1) argues for fusing such epilogue work into the GEMM.  Read as
+ * the usual BLAS convention: with beta == 0 the old C is not read (any
+ * value, NaN included, is ignored).  Everything in double:
+ *   C_out[r][j] = alpha * sum_k A[i][k] B[k][j] + beta * C_in[i][j]
+ *   S_out[r][j] = |alpha| * sum_k |A[i][k] B[k][j]| + |beta| * |C_in[i][j]|
+ * (S is the scale of the normalised error).  C_in has the element type
+ * `dtype` and leading dimension ldc_in; output row r is requested row i.
+ * Returns 0, or -1 on invalid arguments. */
+int oracle_gemm_scaled_rows(int dtype, int M, int N, int K, double alpha,
+                            const void *A, int64_t lda, const void *B, int64_t ldb,
+                            double beta, const void *C_in, int64_t ldc_in,
+                            int nrows, const int64_t *rows,
+                            double *C_out, double *S_out, int64_t ldc)
+{
+    if (beta != 0.0 && (C_in == NULL || ldc_in < N))
+        return -1;
+    int rc = oracle_gemm_rows(dtype, M, N, K, A, lda, B, ldb, nrows, rows, C_out, S_out, ldc);
+    if (rc != 0)
+        return rc;
+    for (int r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        for (int j = 0; j < N; ++j) {
+            double ab = C_out[(int64_t)r * ldc + j];
+            double c = beta != 0.0 ? load_elem(dtype, C_in, i * ldc_in + j) : 0.0;
+            C_out[(int64_t)r * ldc + j] = alpha * ab + beta * c;
+            if (S_out)
+                S_out[(int64_t)r * ldc + j] = fabs(alpha) * S_out[(int64_t)r * ldc + j] + fabs(beta) * fabs(c);
         }
     }
     return 0;

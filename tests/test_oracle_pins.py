@@ -347,3 +347,64 @@ def test_pins_reject_planted_slips(slip):
             return np.roll(C, 1, axis=0)
         raise AssertionError
     assert not _pins_pass(mutant)
+
+
+# ------------------------------------------------ scaled form alpha AB + beta C
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_scaled_reduces_to_plain_and_to_beta_c(dtype):
+    rng = np.random.default_rng(21)
+    A, At = _cast(rng.uniform(-1, 1, (5, 7)), dtype)
+    B, Bt = _cast(rng.uniform(-1, 1, (7, 6)), dtype)
+    Cin, Ct = _cast(rng.uniform(-1, 1, (5, 6)), dtype)
+    C0, S0 = oracle.gemm(dtype, A, B)
+    C1, S1 = oracle.gemm_scaled(dtype, 1.0, A, B, 0.0, None)
+    assert np.array_equal(C1, C0) and np.array_equal(S1, S0)
+    # alpha = 0: beta * C_in exactly (dyadic beta)
+    C2, S2 = oracle.gemm_scaled(dtype, 0.0, A, B, -0.75, Cin)
+    cin = Ct.to(torch.float64).numpy()
+    assert np.array_equal(C2, -0.75 * cin) and np.array_equal(S2, 0.75 * np.abs(cin))
+
+
+def test_scaled_beta_zero_ignores_nan_in_c():
+    A = np.ones((2, 3), np.float32)
+    B = np.ones((3, 2), np.float32)
+    Cin = np.full((2, 2), np.nan, np.float32)
+    C, _ = oracle.gemm_scaled("f32", 2.0, A, B, 0.0, Cin)
+    assert np.array_equal(C, np.full((2, 2), 6.0))
+
+
+def test_scaled_closed_form():
+    # A[i][k] = i + 2k, B[k][j] = k - 3j, C_in[i][j] = i - j, alpha = 2,
+    # beta = -3: C = 2 (i S1 - 3 i j K + 2 S2 - 6 j S1) - 3 (i - j), with the
+    # sums S1, S2 of the plain closed form above.
+    M, N, K = 4, 5, 9
+    i = np.arange(M)[:, None]
+    jj = np.arange(N)[None, :]
+    k = np.arange(K)
+    A = (i + 2 * k[None, :]).astype(np.float32)
+    B = (k[:, None] - 3 * np.arange(N)[None, :]).astype(np.float32)
+    Cin = (i - jj).astype(np.float32)
+    S1, S2 = K * (K - 1) // 2, (K - 1) * K * (2 * K - 1) // 6
+    expect = 2 * (i * S1 - 3 * i * jj * K + 2 * S2 - 6 * jj * S1) - 3 * (i - jj)
+    C, _ = oracle.gemm_scaled("f32", 2.0, A, B, -3.0, Cin)
+    assert np.array_equal(C, expect.astype(np.float64))
+
+
+def test_scaled_brute_force_and_rows():
+    rng = np.random.default_rng(22)
+    A = rng.uniform(-1, 1, (3, 4)).astype(np.float32)
+    B = rng.uniform(-1, 1, (4, 2)).astype(np.float32)
+    Cin = rng.uniform(-1, 1, (3, 2)).astype(np.float32)
+    alpha, beta = 1.5, -0.25
+    Cx, Sx = _exact(A.astype(float).tolist(), B.astype(float).tolist())
+    C, S = oracle.gemm_scaled("f32", alpha, A, B, beta, Cin)
+    u = Fraction(1, 2 ** 50)
+    for a in range(3):
+        for b in range(2):
+            exact = Fraction(alpha) * Cx[a][b] + Fraction(beta) * Fraction(float(Cin[a, b]))
+            scale = abs(Fraction(alpha)) * Sx[a][b] + abs(Fraction(beta)) * abs(Fraction(float(Cin[a, b])))
+            assert abs(Fraction(C[a, b]) - exact) <= u * scale
+            assert abs(Fraction(S[a, b]) - scale) <= u * scale
+    Cr, Sr = oracle.gemm_scaled("f32", alpha, A, B, beta, Cin, rows=[2, 0])
+    assert np.array_equal(Cr, C[[2, 0]]) and np.array_equal(Sr, S[[2, 0]])
