@@ -8,6 +8,10 @@ CUDA-event time on the launching stream; L2 is flushed (a 512 MiB write)
 before each GEMM, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--alpha a --beta b]
+
+--alpha/--beta time the scaled form C := alpha * A.B + beta * C through the
+*_ex entry points instead (the fused epilogue; beta != 0 reads the old C).
 
 --impl reference times the CPU oracle (plain FP64 triple loop) on a bounded
 row sample of the same workloads.  Under torchrun (N > 1) every rank runs
@@ -140,22 +144,35 @@ def run_ours(args, ws, rank, local):
     for name in args.workloads:
         w = workloads.WORKLOADS[name]
         A, B = workloads.make(w)
-        cases.append({"w": w, "A_cpu": A, "B_cpu": B, "A": A.to(dev), "B": B.to(dev),
-                      "C": torch.empty((w.M, w.N), dtype=A.dtype, device=dev)})
+        # The old C (read only when beta != 0): uniform[-1, 1], seed 7.
+        C_cpu = (torch.rand((w.M, w.N), generator=torch.Generator().manual_seed(7)) * 2 - 1
+                 ).to(A.dtype)
+        cases.append({"w": w, "A_cpu": A, "B_cpu": B, "C_cpu": C_cpu, "A": A.to(dev),
+                      "B": B.to(dev), "C": C_cpu.to(dev)})
+    scaled = args.alpha != 1.0 or args.beta != 0.0
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     # This library's kernel launches per step: one per GEMM, plus the
-    # zeroing launch of an FP32 GEMM whose last wave is split along K.
+    # zeroing launch of an FP32 GEMM whose last wave is split along K and
+    # the reduction launch of a split-K GEMM.
     launches_per_step = 0
     for c in cases:
         w = c["w"]
-        _, plan = dg.gemm_plan(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K,
-                               c["B"].data_ptr(), w.N, c["C"].data_ptr(), w.N, sms)
-        launches_per_step += 1 + (1 if (w.dtype == "f32" and plan.split_tiles) else 0)
+        _, plan = dg.gemm_plan_ex(w.dtype, w.M, w.N, w.K, args.alpha, c["A"].data_ptr(), w.K,
+                                  c["B"].data_ptr(), w.N, args.beta, c["C"].data_ptr(), w.N,
+                                  sms)
+        if plan.path == dg.PATH_NOOP:
+            continue
+        launches_per_step += 1 + (1 if (w.dtype == "f32" and plan.split_tiles) else 0) + (
+            1 if plan.splitk_slices > 1 else 0)
 
     def launch(c, s=sptr):
         w = c["w"]
-        st = dg.gemm(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K, c["B"].data_ptr(), w.N,
-                     c["C"].data_ptr(), w.N, s)
+        if scaled:
+            st = dg.gemm_ex(w.dtype, w.M, w.N, w.K, args.alpha, c["A"].data_ptr(), w.K,
+                            c["B"].data_ptr(), w.N, args.beta, c["C"].data_ptr(), w.N, s)
+        else:
+            st = dg.gemm(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K, c["B"].data_ptr(),
+                         w.N, c["C"].data_ptr(), w.N, s)
         if st != dg.GEMM_OK:
             raise RuntimeError(f"{w.name}: {dg.status_string(st)}")
 
@@ -248,27 +265,38 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": "SGEMM FP32 4096^3 (uniform[-1,1], seed 2) + GEMM FP16 4096^3 "
                                "(normal/sqrt(K), seed 3), row-major, lda=K, ldb=ldc=N",
                    "l2": "flushed (512 MiB write) before each GEMM, outside the timed events",
-                   "parallelism": f"replicas{ws}"},
+                   "parallelism": f"replicas{ws}",
+                   "epilogue": {"alpha": args.alpha, "beta": args.beta}},
         "per_kernel": per_kernel, "roofline": roofline, "roofline_tensor": roofline_tensor,
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "device": {"name": props.name, "sms": sms},
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cases, args.cpu_seconds, check=True)
+        if args.beta != 0.0:
+            # One call on the seeded old C, so the sample check sees a single update.
+            for c in cases:
+                c["C"].copy_(c["C_cpu"])
+                launch(c)
+            torch.cuda.synchronize(dev)
+        out["cpu_baseline"] = cpu_baseline(cases, args.cpu_seconds, check=True,
+                                           alpha=args.alpha, beta=args.beta)
     return out
 
 
 def run_e2e(dg, cases, dev, stream, args):
     """Same step through the public C ABI with inputs in pinned host memory:
-    host->device copies of A and B and the device->host read of C are inside
-    the timed events."""
+    host->device copies of A and B (and of the old C when beta != 0) and the
+    device->host read of C are inside the timed events."""
     host = []
     for c in cases:
         host.append({"A": c["A_cpu"].pin_memory(), "B": c["B_cpu"].pin_memory(),
+                     "C_in": c["C_cpu"].pin_memory(),
                      "C": torch.empty(c["C"].shape, dtype=c["C"].dtype).pin_memory()})
     sptr = stream.cuda_stream
+    scaled = args.alpha != 1.0 or args.beta != 0.0
+    read_c = args.beta != 0.0
     h2d = sum(h["A"].numel() * h["A"].element_size() + h["B"].numel() * h["B"].element_size()
-              for h in host)
+              + (h["C_in"].numel() * h["C_in"].element_size() if read_c else 0) for h in host)
     d2h = sum(h["C"].numel() * h["C"].element_size() for h in host)
 
     def step():
@@ -276,8 +304,14 @@ def run_e2e(dg, cases, dev, stream, args):
             w = c["w"]
             c["A"].copy_(h["A"], non_blocking=True)
             c["B"].copy_(h["B"], non_blocking=True)
-            st = dg.gemm(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K, c["B"].data_ptr(),
-                         w.N, c["C"].data_ptr(), w.N, sptr)
+            if read_c:
+                c["C"].copy_(h["C_in"], non_blocking=True)
+            if scaled:
+                st = dg.gemm_ex(w.dtype, w.M, w.N, w.K, args.alpha, c["A"].data_ptr(), w.K,
+                                c["B"].data_ptr(), w.N, args.beta, c["C"].data_ptr(), w.N, sptr)
+            else:
+                st = dg.gemm(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K, c["B"].data_ptr(),
+                             w.N, c["C"].data_ptr(), w.N, sptr)
             if st != dg.GEMM_OK:
                 raise RuntimeError(dg.status_string(st))
             h["C"].copy_(c["C"], non_blocking=True)
@@ -334,10 +368,12 @@ def load_traffic(workload_name):
 
 # ------------------------------------------------------------ CPU oracle
 
-def cpu_baseline(cases, seconds, check=False):
+def cpu_baseline(cases, seconds, check=False, alpha=1.0, beta=0.0):
     """Time the oracle, as it stands, on a bounded row sample of each
     workload (rows chosen so the whole leg takes about `seconds`).  With
-    check=True the sampled GPU rows are also compared with the oracle's."""
+    check=True the sampled GPU rows are also compared with the oracle's
+    alpha * A.B + beta * C_in (the case's "C" must hold one such call's
+    result on the old C "C_cpu")."""
     import oracle
     from oracle import normalized_error
     tol = {"f32": 1e-5, "f16": 2e-3, "bf16": 1e-2}
@@ -358,6 +394,10 @@ def cpu_baseline(cases, seconds, check=False):
         t0 = time.perf_counter()
         ref, S = oracle.gemm(w.dtype, a, b, rows=rows, with_scale=check)
         dt = time.perf_counter() - t0
+        if check and (alpha != 1.0 or beta != 0.0):
+            # Scaled reference for the check (outside the timed sample).
+            c_in = workloads.to_numpy_bits(c["C_cpu"]) if beta != 0.0 else None
+            ref, S = oracle.gemm_scaled(w.dtype, alpha, a, b, beta, c_in, rows=rows)
         fl = 2 * nrows * w.N * w.K
         total_flops += fl
         total_s += dt
@@ -416,6 +456,8 @@ def main():
                     help="time budget of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--alpha", type=float, default=1.0, help="scale of A.B (default 1)")
+    ap.add_argument("--beta", type=float, default=0.0, help="scale of the old C (default 0)")
     ap.add_argument("--workloads", default=",".join(STEP_WORKLOADS),
                     help="comma-separated workload names (default: the 4096^3 step)")
     args = ap.parse_args()

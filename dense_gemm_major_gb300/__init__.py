@@ -29,7 +29,8 @@ DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 
 # Every symbol include/dense_gemm.h declares.
 EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_device_check",
-            "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc")
+            "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
+            "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex")
 
 
 class GemmError(RuntimeError):
@@ -66,6 +67,13 @@ def load() -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = i
         fn.argtypes = gemm_args
+    f = ctypes.c_float
+    for name in ("gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex"):
+        fn = getattr(lib, name)
+        fn.restype = i
+        fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+    lib.gemm_plan_ex.restype = i
+    lib.gemm_plan_ex.argtypes = [i, i, i, i, f, vp, i, vp, i, f, vp, i, i, ctypes.POINTER(Plan)]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_status_string.argtypes = [i]
     lib.gemm_device_check.restype = i
@@ -100,6 +108,27 @@ def gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return load().gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream)
 
 
+def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_f16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_f16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_plan_ex(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms=152):
+    """Returns (status, Plan) of a scaled call."""
+    plan = Plan()
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = load().gemm_plan_ex(code, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms,
+                             ctypes.byref(plan))
+    return st, plan
+
+
 def status_string(status: int) -> str:
     return load().gemm_status_string(int(status)).decode()
 
@@ -131,10 +160,15 @@ def gemm_selftest_timeout(timeout_us: int, stream=0) -> int:
 
 
 _ENTRY = {"f32": gemm_f32, "f16": gemm_f16, "bf16": gemm_bf16}
+_ENTRY_EX = {"f32": gemm_f32_ex, "f16": gemm_f16_ex, "bf16": gemm_bf16_ex}
 
 
 def gemm(dtype: str, M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return _ENTRY[dtype](M, N, K, A, lda, B, ldb, C, ldc, stream)
+
+
+def gemm_ex(dtype: str, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return _ENTRY_EX[dtype](M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 # ------------------------------------------------------------ torch wrapper
@@ -150,10 +184,11 @@ def _ld(t, rows, cols):
     return t.stride(0) if rows > 1 else max(cols, t.stride(0), 1)
 
 
-def matmul(A, B, out=None, stream=None):
-    """C = A @ B for row-major CUDA tensors of one dtype (float32, float16,
-    bfloat16), queued on ``stream`` (default: torch's current stream).
-    Row-padded views (row stride > width) are accepted for A, B and out."""
+def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
+    """out = alpha * (A @ B) + beta * out for row-major CUDA tensors of one
+    dtype (float32, float16, bfloat16), queued on ``stream`` (default:
+    torch's current stream).  Row-padded views (row stride > width) are
+    accepted for A, B and out; beta != 0 needs ``out``."""
     import torch
     if A.device.type != "cuda" or B.device.type != "cuda":
         raise ValueError("operands must be CUDA tensors")
@@ -165,13 +200,19 @@ def matmul(A, B, out=None, stream=None):
     if K != K2:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     if out is None:
+        if beta != 0:
+            raise ValueError("beta != 0 needs an existing out")
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
     elif out.shape != (M, N) or out.dtype != A.dtype:
         raise ValueError("out has the wrong shape or dtype")
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
-    st = gemm(code, M, N, K, A.data_ptr(), _ld(A, M, K), B.data_ptr(), _ld(B, K, N),
-              out.data_ptr(), _ld(out, M, N), stream)
+    if alpha == 1.0 and beta == 0.0:
+        st = gemm(code, M, N, K, A.data_ptr(), _ld(A, M, K), B.data_ptr(), _ld(B, K, N),
+                  out.data_ptr(), _ld(out, M, N), stream)
+    else:
+        st = gemm_ex(code, M, N, K, float(alpha), A.data_ptr(), _ld(A, M, K), B.data_ptr(),
+                     _ld(B, K, N), float(beta), out.data_ptr(), _ld(out, M, N), stream)
     if st != GEMM_OK:
         raise GemmError(st, f"gemm_{code}")
     return out

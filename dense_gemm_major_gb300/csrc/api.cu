@@ -188,6 +188,16 @@ bool tc_split_disabled() {
   return v;
 }
 
+// Measurement override: DENSE_GEMM_TC_GROUP=<n> sets the FP16/BF16 tile rows
+// per rasterisation group (0 = default).
+int tc_group_override() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_TC_GROUP");
+    return s != nullptr ? std::atoi(s) : 0;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_TC_KERNEL=single|pair forces the FP16/BF16
 // kernel (0 = no override, 1 = single CTAs, 2 = CTA pairs).
 int forced_tc_kernel() {
@@ -215,8 +225,9 @@ int forced_sgemm_tn() {
   return v;
 }
 
-gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
-                        int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
+gemm_status_t plan_impl(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
+                        const void* B, int ldb, float beta, const void* C, int ldc, int num_sms,
+                        gemm_plan_t* plan) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
@@ -228,7 +239,8 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   const int es = dtype == 0 ? 4 : 2;
   if (C == nullptr || ldc < N) return GEMM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(C) % es) != 0) return GEMM_ERR_INVALID_ARG;
-  if (K == 0) {
+  if (K == 0 || alpha == 0.f) {
+    // C := beta * C (zeros when beta == 0); A and B are not read.
     plan->path = GEMM_PATH_ZERO_FILL;
     plan->threads = 256;
     return GEMM_OK;
@@ -286,9 +298,14 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
     const int slots = (tn == 8 && forced_sgemm_tn() != 9 ? 2 : 1) * sms;
     const int rem = plan->tiles % slots;
     const int nk = ceil_div(K, dgemm::kSgemmBK);
+    // With beta == 0 the k-halves add into zeroed C; with beta != 0 they
+    // store FP32 partials to a workspace that a fixup kernel combines.
     plan->split_tiles = (rem > 0 && 2 * rem <= slots && nk >= 2) ? rem : 0;
     plan->split_pieces = plan->split_tiles ? 2 : 1;
     plan->splitk_slices = 1;
+    if (plan->split_tiles && beta != 0.f)
+      plan->workspace_bytes =
+          (long long)plan->split_tiles * 2 * dgemm::kSgemmBM * plan->block_n * 4;
     plan->ctas = plan->tiles + plan->split_tiles;
     return GEMM_OK;
   }
@@ -349,23 +366,22 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, const void* A, int lda, 
   return GEMM_OK;
 }
 
-gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const void* B, int ldb,
-                  void* C, int ldc, cudaStream_t stream) {
+gemm_status_t run(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
+                  const void* B, int ldb, float beta, void* C, int ldc, cudaStream_t stream) {
   gemm_plan_t plan;
-  gemm_status_t st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, 1, &plan);
+  gemm_status_t st = plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, &plan);
   if (st != GEMM_OK) return st;
   if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
   DeviceInfo* dev = nullptr;
   st = current_device(&dev);
   if (st != GEMM_OK) return st;
   // Re-plan with the device's SM count (validation above needs no device).
-  st = plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, dev->sms, &plan);
+  st = plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms, &plan);
   if (st != GEMM_OK) return st;
-  const int es = dtype == 0 ? 4 : 2;
   cudaError_t e = cudaSuccess;
 
   if (plan.path == GEMM_PATH_ZERO_FILL) {
-    e = dgemm::launch_zero_fill(C, M, N, ldc, es, stream);
+    e = dgemm::launch_scale_c(C, M, N, ldc, dtype, beta, stream);
   } else if (dtype == 0) {
     dgemm::SgemmParams p;
     p.M = M;
@@ -389,6 +405,12 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
       if (st != GEMM_OK) return st;
     }
+    if (p.slices == 1 && plan.split_tiles > 0 && plan.workspace_bytes > 0) {
+      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.tail_ws);
+      if (st != GEMM_OK) return st;
+    }
+    p.alpha = alpha;
+    p.beta = beta;
     p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
@@ -405,7 +427,7 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     }
     e = dgemm::launch_sgemm(p, tn, tma, &tmA, &tmB, stream);
     if (e == cudaSuccess && p.slices > 1)
-      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, stream);
+      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, alpha, beta, stream);
   } else {
     const CUtensorMapDataType dt =
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -423,6 +445,7 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     p.K = K;
     p.tiles_m = ceil_div(M, plan.block_m);
     p.tiles_n = ceil_div(N, plan.block_n);
+    p.group_m = tc_group_override() > 0 ? tc_group_override() : dgemm::kTcGroupM;
     p.full_tiles = plan.tiles - plan.split_tiles;
     p.split_tiles = plan.split_tiles;
     p.parts = plan.split_pieces;
@@ -433,6 +456,10 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
       if (st != GEMM_OK) return st;
     }
+    p.alpha = alpha;
+    p.beta = beta;
+    p.c_in = C;
+    p.ldc = ldc;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
     if (plan.cluster_ctas == 2)
@@ -440,7 +467,8 @@ gemm_status_t run(int dtype, int M, int N, int K, const void* A, int lda, const 
     else
       e = dgemm::launch_gemm_tc(dtype, p, &tmA, &tmB, &tmC, plan.ctas, stream);
     if (e == cudaSuccess && p.slices > 1)
-      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, dtype, stream);
+      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, dtype, alpha, beta,
+                                      stream);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -467,18 +495,36 @@ extern "C" {
 
 gemm_status_t gemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                        float* C, int ldc, cudaStream_t stream) {
-  return run(0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run(0, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
 }
 
 gemm_status_t gemm_f16(int M, int N, int K, const gemm_half_t* A, int lda, const gemm_half_t* B,
                        int ldb, gemm_half_t* C, int ldc, cudaStream_t stream) {
-  return run(1, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run(1, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
 }
 
 gemm_status_t gemm_bf16(int M, int N, int K, const gemm_bfloat16_t* A, int lda,
                         const gemm_bfloat16_t* B, int ldb, gemm_bfloat16_t* C, int ldc,
                         cudaStream_t stream) {
-  return run(2, M, N, K, A, lda, B, ldb, C, ldc, stream);
+  return run(2, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
+}
+
+gemm_status_t gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda,
+                          const float* B, int ldb, float beta, float* C, int ldc,
+                          cudaStream_t stream) {
+  return run(0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_f16_ex(int M, int N, int K, float alpha, const gemm_half_t* A, int lda,
+                          const gemm_half_t* B, int ldb, float beta, gemm_half_t* C, int ldc,
+                          cudaStream_t stream) {
+  return run(1, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_bf16_ex(int M, int N, int K, float alpha, const gemm_bfloat16_t* A, int lda,
+                           const gemm_bfloat16_t* B, int ldb, float beta, gemm_bfloat16_t* C,
+                           int ldc, cudaStream_t stream) {
+  return run(2, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 const char* gemm_status_string(gemm_status_t status) {
@@ -520,7 +566,13 @@ gemm_status_t gemm_device_check(cudaStream_t stream, unsigned* fault_bits) {
 
 gemm_status_t gemm_plan(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
                         int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
-  return plan_impl(dtype, M, N, K, A, lda, B, ldb, C, ldc, num_sms, plan);
+  return plan_impl(dtype, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, num_sms, plan);
+}
+
+gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
+                           const void* B, int ldb, float beta, const void* C, int ldc,
+                           int num_sms, gemm_plan_t* plan) {
+  return plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms, plan);
 }
 
 int gemm_smem_layout_offset(int layout, int row, int col) {

@@ -1,5 +1,6 @@
-// Small kernels around the GEMM path: the K == 0 product (C := 0) and the
-// self-test of the bounded mbarrier wait.
+// Small kernels around the GEMM path: the K == 0 / alpha == 0 product
+// (C := beta * C), the split-K slice reduction, and the self-test of the
+// bounded mbarrier wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -8,19 +9,6 @@
 
 namespace dgemm {
 namespace {
-
-// Grid-stride zero fill of an M x N row-major block with leading dimension
-// ldc; elements of a row are contiguous, rows may be padded.
-template <typename T>
-__global__ void zero_fill_kernel(T* C, int M, int N, long long ldc) {
-  const long long total = (long long)M * N;
-  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    const long long i = idx / N;
-    const long long j = idx - i * N;
-    C[i * ldc + j] = T(0);
-  }
-}
 
 // One thread waits on a freshly initialised mbarrier that expects one
 // arrival which never comes.  The bounded wait gives up after timeout_ns
@@ -49,8 +37,20 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
 // once.  Consecutive threads take consecutive columns (coalesced reads of
 // every slice and coalesced writes of C).
 template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int slices, int M, int N,
-                                     long long ldw, T* __restrict__ C, long long ldc) {
+                                     long long ldw, T* __restrict__ C, long long ldc, float alpha,
+                                     float beta) {
   const long long total = (long long)M * N;
   const long long slice_stride = (long long)M * ldw;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -60,41 +60,60 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int slices, i
     const float* src = ws + i * ldw + j;
     float acc = __ldg(src);
     for (int s = 1; s < slices; ++s) acc += __ldg(src + s * slice_stride);
-    C[i * ldc + j] = from_f32<T>(acc);
+    float v = alpha * acc;
+    if (beta != 0.f) v = fmaf(beta, to_f32<T>(C[i * ldc + j]), v);
+    C[i * ldc + j] = from_f32<T>(v);
+  }
+}
+
+template <typename T>
+__global__ void scale_c_kernel(T* C, int M, int N, long long ldc, float beta) {
+  const long long total = (long long)M * N;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long i = idx / N;
+    const long long j = idx - i * N;
+    T* c = C + i * ldc + j;
+    *c = beta == 0.f ? T(0) : from_f32<T>(beta * to_f32<T>(*c));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
-                                 void* C, long long ldc, int elem, cudaStream_t stream) {
+                                 void* C, long long ldc, int elem, float alpha, float beta,
+                                 cudaStream_t stream) {
   const long long total = (long long)M * N;
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   if (elem == 0)
     splitk_reduce_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<float*>(C), ldc);
+        ws, slices, M, N, ldw, static_cast<float*>(C), ldc, alpha, beta);
   else if (elem == 1)
     splitk_reduce_kernel<__half><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<__half*>(C), ldc);
+        ws, slices, M, N, ldw, static_cast<__half*>(C), ldc, alpha, beta);
   else
     splitk_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<__nv_bfloat16*>(C), ldc);
+        ws, slices, M, N, ldw, static_cast<__nv_bfloat16*>(C), ldc, alpha, beta);
   return cudaGetLastError();
 }
 
-cudaError_t launch_zero_fill(void* C, int M, int N, long long ldc, int elem_bytes,
-                             cudaStream_t stream) {
+cudaError_t launch_scale_c(void* C, int M, int N, long long ldc, int elem, float beta,
+                           cudaStream_t stream) {
   const long long total = (long long)M * N;
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
-  if (elem_bytes == 4)
-    zero_fill_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc);
+  if (elem == 0)
+    scale_c_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<float*>(C), M, N, ldc,
+                                                                beta);
+  else if (elem == 1)
+    scale_c_kernel<__half><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<__half*>(C), M, N,
+                                                                 ldc, beta);
   else
-    zero_fill_kernel<unsigned short>
-        <<<(unsigned)blocks, 256, 0, stream>>>(static_cast<unsigned short*>(C), M, N, ldc);
+    scale_c_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
   return cudaGetLastError();
 }
 

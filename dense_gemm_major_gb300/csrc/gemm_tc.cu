@@ -96,7 +96,7 @@ __device__ __forceinline__ Unit unit_of(int u, const TcParams& p, int nk) {
     w.n_w = BN / p.parts;
     w.n_off = part * w.n_w;
   }
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kTcGroupM, w.tm, w.tn);
+  grouped_tile(tile, p.tiles_m, p.tiles_n, p.group_m, w.tm, w.tn);
   return w;
 }
 
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t r0[32], r1[32];
         tmem_ld32(t_row + c * kTcEpiCols, r0);
         tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
-        tmem_ld_wait();
+        tmem_ld_wait(r0, r1);
         if (c == chunks - 1) {
           // The accumulator buffer is free for the next unit's MMAs.
           tc_fence_before();
@@ -283,6 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
         }
         if (w.slice < 0) {
+          if (p.alpha != 1.f || p.beta != 0.f)
+            scale_row64<T>(r0, r1, p.alpha, p.beta, static_cast<const T*>(p.c_in), p.ldc, p.M,
+                           p.N, w.tm * BM + q * 32 + lane, w.tn * BN + w.n_off + c * kTcEpiCols);
           store_box(r0, r1, w.tm, w.tn, w.n_off + c * kTcEpiCols);
         } else {
           // Split-K: this lane's row of the FP32 partial, columns beyond the

@@ -95,7 +95,7 @@ __device__ __forceinline__ Unit unit_of(int u, const TcParams& p) {
     w.n_w = BN / p.parts;
     w.n_off = (j % p.parts) * w.n_w;
   }
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kTcGroupM, w.tm, w.tn);
+  grouped_tile(tile, p.tiles_m, p.tiles_n, p.group_m, w.tm, w.tn);
   return w;
 }
 
@@ -255,13 +255,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         uint32_t r0[32], r1[32];
         tmem_ld32(t_row + c * kTcEpiCols, r0);
         tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
-        tmem_ld_wait();
+        tmem_ld_wait(r0, r1);
         if (c == chunks - 1) {
           // This CTA's half of the accumulator is drained.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[b]), 0));
         }
+        if (p.alpha != 1.f || p.beta != 0.f)
+          scale_row64<T>(r0, r1, p.alpha, p.beta, static_cast<const T*>(p.c_in), p.ldc, p.M, p.N,
+                         row0 + lane, w.tn * BN + w.n_off + c * kTcEpiCols);
         unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
         if (lane == 0) tma_store_wait_read<1>();
         __syncwarp();

@@ -36,11 +36,16 @@ struct SgemmParams {
   int tiles_m, tiles_n;
   // Tiles [0, full_tiles) are computed whole and stored.  Each tile t >=
   // full_tiles is computed as two pieces (k-tiles [0, split_kt) and
-  // [split_kt, nk)) by consecutive CTAs that add their FP32 partial sums
-  // into C, which must hold zeros for those tiles beforehand; with exactly
-  // two addends the result does not depend on their order.
+  // [split_kt, nk)) by consecutive CTAs.  With tail_ws == nullptr (only when
+  // beta = 0) both add alpha times their FP32 partial sums into C, which is
+  // zeroed first; with exactly two addends the result does not depend on
+  // their order.  Otherwise piece h of split tile j stores its partial sum
+  // at tail_ws + (2 * j + h) * BM * BN (row-major, leading dimension BN) and
+  // a fixup kernel writes alpha * (piece 0 + piece 1) + beta * C, in that
+  // order, so the result is again independent of scheduling.
   int full_tiles;
   int split_kt;
+  float* tail_ws = nullptr;
   // Split-K mode (slices > 1): CTA u computes k-slice u % slices of tile
   // u / slices (k-tiles [s*nk/slices, (s+1)*nk/slices)) and stores its FP32
   // partial tile at ws + s * M * ldw (row-major, leading dimension ldw);
@@ -49,6 +54,10 @@ struct SgemmParams {
   int slices;
   float* ws;
   long long ldw;
+  // C := alpha * (A.B) + beta * C; the old C is read only when beta != 0
+  // (in split-K mode splitk_reduce applies alpha and beta; for split tiles
+  // with tail_ws the fixup kernel does).
+  float alpha = 1.f, beta = 0.f;
   int c_vec4;        // C rows may be written with 16-byte stores
   unsigned* fault;   // device fault word
   unsigned long long timeout_ns;
@@ -89,7 +98,7 @@ constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
 constexpr int kTcStages = 4;
 constexpr int kTcThreads = 192;          // producer warp, MMA warp, 4 epilogue warps
-constexpr int kTcGroupM = 8;             // tile rows per rasterisation group
+constexpr int kTcGroupM = 8;             // default tile rows per rasterisation group
 constexpr int kTcEpiCols = 64;           // columns per epilogue store box
 constexpr int kTcSmemBytes =
     kTcStages * (kTcBM * kTcBK + kTcBK * kTcBN) * 2   // A and B ring
@@ -99,6 +108,7 @@ constexpr int kTcSmemBytes =
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n;
+  int group_m;        // tile rows per rasterisation group
   // Split-K mode (single-CTA kernel only, slices > 1): unit u is k-slice
   // u % slices of tile u / slices, stored as an FP32 partial tile at
   // ws + s * M * ldw; splitk_reduce sums the slices.  The column-split
@@ -106,6 +116,12 @@ struct TcParams {
   int slices;
   float* ws;
   long long ldw;
+  // C := alpha * (A.B) + beta * C: the epilogue reads the old C (c_in,
+  // leading dimension ldc, elements of the output type) when beta != 0.
+  // Split-K units leave both to splitk_reduce.
+  float alpha = 1.f, beta = 0.f;
+  const void* c_in = nullptr;
+  long long ldc;
   // Work units: tiles [0, full_tiles) whole (128 x 256); each later tile
   // as `parts` consecutive units of 128 x (256 / parts) columns, each over
   // the full K range.
@@ -172,20 +188,19 @@ cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap*
                                 const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,
                                 cudaStream_t stream);
 
-// ---------------------------------------------------------------- zero fill
-
-// C[i][j] = 0 for i < M, j < N (row-major, leading dimension ldc, element
-// size elem_bytes = 2 or 4): the K == 0 product.
-cudaError_t launch_zero_fill(void* C, int M, int N, long long ldc, int elem_bytes,
-                             cudaStream_t stream);
-
 // ---------------------------------------------------------------- split-K reduce
 
-// C[i][j] = sum over s of ws[s * M * ldw + i * ldw + j], in slice order,
-// rounded once to the element type of C (elem: 0 = FP32, 1 = FP16,
-// 2 = BF16).
+// C[i][j] = alpha * (sum over s of ws[s * M * ldw + i * ldw + j], in slice
+// order) + beta * C[i][j], rounded once to the element type of C (elem:
+// 0 = FP32, 1 = FP16, 2 = BF16); C is read only when beta != 0.
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
-                                 void* C, long long ldc, int elem, cudaStream_t stream);
+                                 void* C, long long ldc, int elem, float alpha, float beta,
+                                 cudaStream_t stream);
+
+// C := beta * C on an M x N block (C is not read when beta == 0): the
+// product when K == 0 or alpha == 0.
+cudaError_t launch_scale_c(void* C, int M, int N, long long ldc, int elem, float beta,
+                           cudaStream_t stream);
 
 // Split-K slice count for a grid of `tiles` output tiles over `slots` CTA
 // slots and `nk` k-tiles: slices of at least 4 k-tiles, at most 32, when

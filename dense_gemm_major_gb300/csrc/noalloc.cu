@@ -100,12 +100,14 @@ extern "C" gemm_status_t gemm_f32_noalloc(int M, int N, int K, const float* A, i
   p.slices = plan.splitk_slices;
   p.ws = dev->scratch;
   p.ldw = ((long long)N + 3) / 4 * 4;
+  p.alpha = 1.f;
+  p.beta = 0.f;
   p.c_vec4 = 0;
   p.fault = fault;
   p.timeout_ns = dgemm::wait_bound_ns();
   cudaError_t e = dgemm::launch_sgemm(p, 8, /*use_tma=*/false, nullptr, nullptr, stream);
   if (e == cudaSuccess)
-    e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, stream);
+    e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, 1.f, 0.f, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

@@ -110,11 +110,11 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int warp = tid >> 5;
 
   // Work unit of this CTA: a whole tile; one of the two k-pieces of a split
-  // tile (consecutive CTAs) that add into C; or, in split-K mode, one
-  // k-slice of a tile that is stored to the workspace.
+  // tile (consecutive CTAs) that add into C or store to the tail workspace;
+  // or, in split-K mode, one k-slice of a tile that is stored to the
+  // workspace.  (Where the result goes is decoded again in the epilogue, so
+  // that it holds no registers across the main loop.)
   int tile, k_begin, k_end;
-  bool add_into_c = false;
-  float* part = nullptr;   // split-K: this slice's FP32 partial, row-major (ldw)
   {
     const int nk_all = (p.K + BK - 1) / BK;
     const int b = blockIdx.x;
@@ -123,7 +123,6 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       const int sl = b - tile * p.slices;
       k_begin = sl * nk_all / p.slices;
       k_end = (sl + 1) * nk_all / p.slices;
-      part = p.ws + (long long)sl * p.M * p.ldw;
     } else if (b < p.full_tiles) {
       tile = b;
       k_begin = 0;
@@ -133,7 +132,6 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       tile = p.full_tiles + (j >> 1);
       k_begin = (j & 1) ? p.split_kt : 0;
       k_end = (j & 1) ? nk_all : p.split_kt;
-      add_into_c = true;
     }
   }
   int tm, tn;
@@ -287,13 +285,81 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     return;
   }
 
+  // Destination: unscaled FP32 partial sums go to
+  // part[(gm - part_m0) * part_ld + gn - part_n0]; add_into_c pieces add
+  // into C; everything else is stored to C.
+  float* part = nullptr;
+  long long part_ld = 0;
+  int part_m0 = 0, part_n0 = 0;
+  bool add_into_c = false;
+  {
+    const int b = blockIdx.x;
+    if (p.slices > 1) {
+      part = p.ws + (long long)(b % p.slices) * p.M * p.ldw;
+      part_ld = p.ldw;
+    } else if (b >= p.full_tiles) {
+      if (p.tail_ws != nullptr) {
+        part = p.tail_ws + (long long)(b - p.full_tiles) * (BM * BN);
+        part_ld = BN;
+        part_m0 = m0;
+        part_n0 = n0;
+      } else {
+        add_into_c = true;
+      }
+    }
+  }
+
+  // Scaling pass, C := alpha * (A.B) + beta * C, applied to the
+  // accumulators in place before any store (partial sums for a workspace
+  // stay unscaled).  The old C of one row (TN values) is loaded at once so
+  // that those loads overlap instead of each waiting behind a store.
+  if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
+    const bool vec4c = p.c_vec4 != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int gm = m0 + a_row0 + 4 * i;
+      const float* crow = p.C + (long long)gm * p.ldc;
+      float4 old[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int gn = n0 + b_col0 + 32 * h;
+        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.beta != 0.f && gm < p.M) {
+          if (vec4c && gn + 3 < p.N) {
+            c = *reinterpret_cast<const float4*>(crow + gn);
+          } else {
+            if (gn + 0 < p.N) c.x = crow[gn + 0];
+            if (gn + 1 < p.N) c.y = crow[gn + 1];
+            if (gn + 2 < p.N) c.z = crow[gn + 2];
+            if (gn + 3 < p.N) c.w = crow[gn + 3];
+          }
+        }
+        old[h] = c;
+      }
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+        const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+        // (A column past N got c = 0 and is never stored.)
+        const auto upd = [&](float v, float cv) {
+          return p.beta != 0.f ? fmaf(p.beta, cv, p.alpha * v) : p.alpha * v;
+        };
+        acc[i][2 * h + 0] = pack_pair(upd(lo.x, old[h].x), upd(lo.y, old[h].y));
+        acc[i][2 * h + 1] = pack_pair(upd(hi.x, old[h].z), upd(hi.y, old[h].w));
+      }
+    }
+  }
+
   // Epilogue: each store instruction of a warp covers four full 128-byte row
   // segments of C.
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int gm = m0 + a_row0 + 4 * i;
     if (gm >= p.M) continue;
-    float* crow = part != nullptr ? part + (long long)gm * p.ldw : p.C + (long long)gm * p.ldc;
+    // Column gn of this row is crow[gn - cshift].
+    float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
+                                  : p.C + (long long)gm * p.ldc;
+    const int cshift = part_n0;
     const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
@@ -311,13 +377,55 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
         }
       } else if (vec4 && gn + 3 < p.N) {
-        *reinterpret_cast<float4*>(crow + gn) = make_float4(v0, v1, v2, v3);
+        *reinterpret_cast<float4*>(crow + gn - cshift) = make_float4(v0, v1, v2, v3);
       } else {
-        if (gn + 0 < p.N) crow[gn + 0] = v0;
-        if (gn + 1 < p.N) crow[gn + 1] = v1;
-        if (gn + 2 < p.N) crow[gn + 2] = v2;
-        if (gn + 3 < p.N) crow[gn + 3] = v3;
+        if (gn + 0 < p.N) crow[gn + 0 - cshift] = v0;
+        if (gn + 1 < p.N) crow[gn + 1 - cshift] = v1;
+        if (gn + 2 < p.N) crow[gn + 2 - cshift] = v2;
+        if (gn + 3 < p.N) crow[gn + 3 - cshift] = v3;
       }
+    }
+  }
+}
+
+// Writes C := alpha * (piece 0 + piece 1) + beta * C on the split tiles
+// [full_tiles, tiles_m * tiles_n) from their two partial sums in tail_ws.
+// Block (j, y) takes 2048 consecutive elements (2048 / bn rows) of split tile
+// j, 8 per thread at a stride of 256; every thread issues all its loads
+// before its first store, so the loads overlap.
+constexpr int kFixupElems = 2048;
+__global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int bn) {
+  const int j = (int)blockIdx.x;
+  int tm, tn;
+  grouped_tile(p.full_tiles + j, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
+  const int rows = min(BM, p.M - tm * BM);
+  const int cols = min(bn, p.N - tn * bn);
+  const float* __restrict__ p0 = p.tail_ws + (long long)(2 * j) * (BM * bn);
+  const float* __restrict__ p1 = p0 + BM * bn;
+  float* __restrict__ c0 = p.C + (long long)(tm * BM) * p.ldc + tn * bn;
+  const int first = (int)blockIdx.y * kFixupElems;
+  constexpr int kPer = kFixupElems / 256;
+  float v[kPer], old[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int idx = first + (int)threadIdx.x + 256 * q;
+    const int r = idx / bn;
+    const int c = idx - r * bn;
+    v[q] = 0.f;
+    old[q] = 0.f;
+    if (r < rows && c < cols) {
+      v[q] = p0[idx] + p1[idx];
+      if (p.beta != 0.f) old[q] = c0[(long long)r * p.ldc + c];
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int idx = first + (int)threadIdx.x + 256 * q;
+    const int r = idx / bn;
+    const int c = idx - r * bn;
+    if (r < rows && c < cols) {
+      const float a = p.alpha * v[q];
+      c0[(long long)r * p.ldc + c] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
     }
   }
 }
@@ -347,7 +455,7 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
   if (e != cudaSuccess) return e;
   const int tiles = p.tiles_m * p.tiles_n;
   const int split = p.slices > 1 ? 0 : tiles - p.full_tiles;
-  if (split > 0) {
+  if (split > 0 && p.tail_ws == nullptr) {
     sgemm_zero_split_tiles<<<split, 256, 0, stream>>>(p, sgemm_bn(TN));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -355,6 +463,10 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
   const dim3 grid((unsigned)(p.slices > 1 ? tiles * p.slices : tiles + split));
   sgemm_kernel<kTma, TN, kMinBlocks>
       <<<grid, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || split == 0 || p.tail_ws == nullptr) return e;
+  const dim3 fixup_grid((unsigned)split, (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
+  sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN));
   return cudaGetLastError();
 }
 

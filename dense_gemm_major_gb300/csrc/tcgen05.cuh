@@ -88,8 +88,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Waits for this thread's tcgen05.ld loads into r0 and r1.  tcgen05.ld writes
+// its registers asynchronously, so the wait names them as read-write
+// operands: no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r0[0]), "+r"(r0[1]), "+r"(r0[2]), "+r"(r0[3]), "+r"(r0[4]), "+r"(r0[5]),
+        "+r"(r0[6]), "+r"(r0[7]), "+r"(r0[8]), "+r"(r0[9]), "+r"(r0[10]), "+r"(r0[11]),
+        "+r"(r0[12]), "+r"(r0[13]), "+r"(r0[14]), "+r"(r0[15]), "+r"(r0[16]), "+r"(r0[17]),
+        "+r"(r0[18]), "+r"(r0[19]), "+r"(r0[20]), "+r"(r0[21]), "+r"(r0[22]), "+r"(r0[23]),
+        "+r"(r0[24]), "+r"(r0[25]), "+r"(r0[26]), "+r"(r0[27]), "+r"(r0[28]), "+r"(r0[29]),
+        "+r"(r0[30]), "+r"(r0[31])
+      :
+      : "memory");
+  asm volatile(
+      ""
+      : "+r"(r1[0]), "+r"(r1[1]), "+r"(r1[2]), "+r"(r1[3]), "+r"(r1[4]), "+r"(r1[5]),
+        "+r"(r1[6]), "+r"(r1[7]), "+r"(r1[8]), "+r"(r1[9]), "+r"(r1[10]), "+r"(r1[11]),
+        "+r"(r1[12]), "+r"(r1[13]), "+r"(r1[14]), "+r"(r1[15]), "+r"(r1[16]), "+r"(r1[17]),
+        "+r"(r1[18]), "+r"(r1[19]), "+r"(r1[20]), "+r"(r1[21]), "+r"(r1[22]), "+r"(r1[23]),
+        "+r"(r1[24]), "+r"(r1[25]), "+r"(r1[26]), "+r"(r1[27]), "+r"(r1[28]), "+r"(r1[29]),
+        "+r"(r1[30]), "+r"(r1[31])
+      :
+      : "memory");
 }
 
 template <typename T>
@@ -103,6 +125,63 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------ epilogue scaling
+
+template <typename T>
+__device__ __forceinline__ float elem_to_f32(T v);
+template <>
+__device__ __forceinline__ float elem_to_f32<__half>(__half v) { return __half2float(v); }
+template <>
+__device__ __forceinline__ float elem_to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ float2 pair_to_f32(uint32_t bits);
+template <>
+__device__ __forceinline__ float2 pair_to_f32<__half>(uint32_t bits) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&bits));
+}
+template <>
+__device__ __forceinline__ float2 pair_to_f32<__nv_bfloat16>(uint32_t bits) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bits));
+}
+
+// v := alpha * v + beta * C_old on the 64 FP32 accumulator values (bits in
+// r0[0..31], r1[0..31]) of row `row`, columns col..col+63.  The old C
+// (element type T, leading dimension ldc) is read only when beta != 0, and
+// only inside M x N; 16-byte loads where a group of 8 is in bounds.
+template <typename T>
+__device__ __forceinline__ void scale_row64(uint32_t (&r0)[32], uint32_t (&r1)[32], float alpha,
+                                            float beta, const T* c_in, long long ldc, int M,
+                                            int N, int row, int col) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    r0[j] = __float_as_uint(alpha * __uint_as_float(r0[j]));
+    r1[j] = __float_as_uint(alpha * __uint_as_float(r1[j]));
+  }
+  if (beta == 0.f || row >= M) return;
+  const T* src = c_in + (long long)row * ldc + col;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t* dst = g < 4 ? &r0[g * 8] : &r1[(g - 4) * 8];
+    float old[8];
+    if (col + 8 * g + 8 <= N) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * g);
+      const float2 a = pair_to_f32<T>(raw.x), b = pair_to_f32<T>(raw.y);
+      const float2 c = pair_to_f32<T>(raw.z), d = pair_to_f32<T>(raw.w);
+      old[0] = a.x; old[1] = a.y; old[2] = b.x; old[3] = b.y;
+      old[4] = c.x; old[5] = c.y; old[6] = d.x; old[7] = d.y;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        old[e] = (col + 8 * g + e < N) ? elem_to_f32<T>(src[8 * g + e]) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[e] = __float_as_uint(fmaf(beta, old[e], __uint_as_float(dst[e])));
+  }
 }
 
 // ------------------------------------------------------------ CTA pairs

@@ -135,6 +135,37 @@ gemm_status_t gemm_f32_noalloc(int M, int N, int K,
                                float *C, int ldc,
                                cudaStream_t stream);
 
+/*
+ * Scaled forms: C := alpha * (A . B) + beta * C, with the conventions of
+ * the plain entry points otherwise.  The m.lqnn.cn SGEMM article's tiled
+ * kernel takes alpha and beta arguments (its listing leaves the beta term
+ * out); the GB300 roadmap (m.nxbn.cn, section 7.1) argues for fusing such
+ * epilogue work into the GEMM instead of a separate pass over C.
+ *  - alpha * acc + beta * C_old is formed in FP32 (one FMA) from the FP32
+ *    accumulator and rounded once to the output type.
+ *  - beta == 0: the old C is not read (NaN or Inf there is ignored).
+ *  - alpha == 0 or K == 0: C := beta * C and A, B are not read (they may be
+ *    NULL); beta == 0 as well gives zeros.
+ *  - gemm_f32_ex with beta != 0 does not split a last partial wave of tiles
+ *    into k-halves (they add into C, which would then not start at zero).
+ * alpha = 1, beta = 0 is exactly the plain entry point.
+ */
+gemm_status_t gemm_f32_ex(int M, int N, int K, float alpha,
+                          const float *A, int lda,
+                          const float *B, int ldb, float beta,
+                          float *C, int ldc,
+                          cudaStream_t stream);
+gemm_status_t gemm_f16_ex(int M, int N, int K, float alpha,
+                          const gemm_half_t *A, int lda,
+                          const gemm_half_t *B, int ldb, float beta,
+                          gemm_half_t *C, int ldc,
+                          cudaStream_t stream);
+gemm_status_t gemm_bf16_ex(int M, int N, int K, float alpha,
+                           const gemm_bfloat16_t *A, int lda,
+                           const gemm_bfloat16_t *B, int ldb, float beta,
+                           gemm_bfloat16_t *C, int ldc,
+                           cudaStream_t stream);
+
 /* Static, never-null description of a status code. */
 const char *gemm_status_string(gemm_status_t status);
 
@@ -155,7 +186,7 @@ gemm_status_t gemm_device_check(cudaStream_t stream, unsigned *fault_bits);
  */
 enum {
   GEMM_PATH_NOOP = 0,          /* M == 0 or N == 0                   */
-  GEMM_PATH_ZERO_FILL = 1,     /* K == 0: C := 0                     */
+  GEMM_PATH_ZERO_FILL = 1,     /* K == 0 or alpha == 0: C := beta*C  */
   GEMM_PATH_SIMT_TMA = 2,      /* FP32 SIMT, TMA-staged tiles        */
   GEMM_PATH_SIMT_CPASYNC = 3,  /* FP32 SIMT, 4-byte cp.async tiles   */
   GEMM_PATH_TC_TMA = 4         /* FP16/BF16 tcgen05, TMA in and out  */
@@ -185,6 +216,10 @@ typedef struct gemm_plan_t {
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,
                         const void *C, int ldc, int num_sms, gemm_plan_t *plan);
+/* The plan of a scaled call (gemm_*_ex); gemm_plan is alpha = 1, beta = 0. */
+gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha,
+                           const void *A, int lda, const void *B, int ldb, float beta,
+                           const void *C, int ldc, int num_sms, gemm_plan_t *plan);
 
 /*
  * Shared-memory layout of the kernels' operand tiles, as an element offset

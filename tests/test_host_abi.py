@@ -292,3 +292,31 @@ def test_naive_row_major_a_tile_would_conflict():
     # bank conflict: the check above is able to see one.
     addrs = [4 * (_lane_rc(l)[0] * 32 + 0) for l in range(32)]
     assert _wavefronts(addrs, 16) == 4
+
+
+def test_scaled_plans():
+    # alpha == 0 or K == 0: C := beta * C, A and B may be null
+    ok, p = dg.gemm_plan_ex("f32", 64, 64, 32, 0.0, 0, 32, 0, 64, 2.0, FAKE, 64, 152)
+    assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
+    ok, p = dg.gemm_plan_ex("bf16", 64, 64, 0, 1.0, 0, 0, 0, 64, 0.5, FAKE, 64, 152)
+    assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
+    # The SGEMM's last partial wave is split into k-halves either way; with
+    # beta != 0 the halves go through a workspace of two FP32 tiles each
+    # (56 tiles x 2 x 128 x 256 x 4 bytes), with beta == 0 they add into C.
+    args = (4096, 4096, 4096, 1.0, FAKE, 4096, FAKE + (1 << 30), 4096)
+    ok, p0 = dg.gemm_plan_ex("f32", *args, 0.0, FAKE + (2 << 30), 4096, 152)
+    ok, p1 = dg.gemm_plan_ex("f32", *args, 0.5, FAKE + (2 << 30), 4096, 152)
+    assert p0.split_tiles == 56 and p1.split_tiles == 56 and p1.ctas == 512 + 56
+    assert p0.workspace_bytes == 0 and p1.workspace_bytes == 56 * 2 * 128 * 256 * 4
+    # FP16/BF16 plans do not depend on alpha and beta
+    for dt in ("f16", "bf16"):
+        ok, q0 = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
+                              FAKE + (2 << 30), 4096, 152)
+        ok, q1 = dg.gemm_plan_ex(dt, *args, -1.0, FAKE + (2 << 30), 4096, 152)
+        assert (q0.split_tiles, q0.ctas, q0.cluster_ctas) == (q1.split_tiles, q1.ctas, q1.cluster_ctas)
+    # the scaled entry points validate like the plain ones
+    for dt in ("f32", "f16", "bf16"):
+        assert dg.gemm_ex(dt, -1, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 0.0, FAKE + 8192, 4, 0) \
+            == dg.GEMM_ERR_INVALID_ARG
+        assert dg.gemm_ex(dt, 4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 1.0, FAKE + 16, 4, 0) \
+            == dg.GEMM_ERR_INVALID_ARG
