@@ -21,6 +21,10 @@ marshals numpy arrays.  What it computes, with sources:
 * ``gemm_scaled``: ``alpha * (A @ B) + beta * C_in`` in double, the GEMM of
   the m.lqnn.cn article's ``sgemm_tile_v2(..., alpha, beta)`` signature, with
   the BLAS reading that ``beta == 0`` does not read C_in.
+* ``op_a="T"`` / ``op_b="T"``: the operand is passed as stored transposed
+  (A as K x M, B as N x K) and the product uses its transpose; ``op_b="T"``
+  is the column-major B (``B[k + col*K]``) of the m.lqnn.cn article,
+  section 3.1.
 
 Half and bfloat16 inputs are passed as their 16-bit patterns and decoded in C
 from the IEEE binary16 / bfloat16 bit layouts.
@@ -80,6 +84,17 @@ def _load():
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_int, i64p, dp, dp, ctypes.c_int64]
+        lib.oracle_gemm_op_rows.restype = ctypes.c_int
+        lib.oracle_gemm_op_rows.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_int, i64p, dp, dp, ctypes.c_int64]
+        lib.oracle_gemm_scaled_op_rows.restype = ctypes.c_int
+        lib.oracle_gemm_scaled_op_rows.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_int, i64p, dp, dp, ctypes.c_int64]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         _lib = lib
@@ -106,94 +121,108 @@ def _as_input(x: np.ndarray, dtype: str) -> np.ndarray:
         raise TypeError(f"oracle expects {np.dtype(want).name} data for {dtype}, got {x.dtype}")
     if x.ndim != 2:
         raise ValueError("oracle operands are 2-D row-major arrays")
-    if x.size and (x.strides[1] != x.itemsize or x.strides[0] % x.itemsize):
+    # (A dimension of extent 1 may report any stride.)
+    if x.size and ((x.shape[1] > 1 and x.strides[1] != x.itemsize)
+                   or (x.shape[0] > 1 and x.strides[0] % x.itemsize)):
         raise ValueError("oracle operands must be row-major with unit column stride")
     return x
 
 
-def gemm(dtype: str, A: np.ndarray, B: np.ndarray, rows=None, with_scale: bool = True):
-    """Return (C, S) as float64 arrays for the requested rows of A @ B.
+_OPS = {"N": 0, "T": 1}
 
-    ``A`` is M x K and ``B`` is K x N, row-major; a view with a row stride
-    larger than its width is accepted (that is the leading dimension).  For
-    "f16" / "bf16" the arrays hold uint16 bit patterns.  ``rows`` selects
-    output rows (any order, repeats allowed); None means all M rows.
-    ``S`` is None when ``with_scale`` is False.
-    """
-    code = _DTYPE_CODES[dtype]
-    A = _as_input(A, dtype)
-    B = _as_input(B, dtype)
-    M, K = A.shape
-    K2, N = B.shape
+
+def _shape_of(A, B, op_a, op_b):
+    """(M, N, K, lda, ldb) of op(A) . op(B) from the stored arrays."""
+    a_rows, a_cols = A.shape
+    b_rows, b_cols = B.shape
+    M, K = (a_cols, a_rows) if op_a else (a_rows, a_cols)
+    K2, N = (b_cols, b_rows) if op_b else (b_rows, b_cols)
     if K != K2:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
-    lda = A.strides[0] // A.itemsize if M > 0 else max(K, 1)
-    ldb = B.strides[0] // B.itemsize if K > 0 else max(N, 1)
+    # (numpy reports an arbitrary row stride for an array of one row.)
+    lda = A.strides[0] // A.itemsize if a_rows > 1 else max(a_cols, 1)
+    ldb = B.strides[0] // B.itemsize if b_rows > 1 else max(b_cols, 1)
+    return M, N, K, lda, ldb
+
+
+def _rows_arg(rows, M):
     if rows is None:
-        nrows, rows_p, keep = M, None, None
-    else:
-        keep = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
-        nrows = int(keep.size)
-        rows_p = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        return M, None, None
+    keep = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return int(keep.size), keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), keep
+
+
+def gemm(dtype: str, A: np.ndarray, B: np.ndarray, rows=None, with_scale: bool = True,
+         op_a: str = "N", op_b: str = "N"):
+    """Return (C, S) as float64 arrays for the requested rows of op(A) @ op(B).
+
+    With op "N" ``A`` is M x K and ``B`` is K x N as stored; with op "T" the
+    array holds the transpose (A as K x M, B as N x K).  Arrays are
+    row-major; a view with a row stride larger than its width is accepted
+    (that is the leading dimension).  For "f16" / "bf16" the arrays hold
+    uint16 bit patterns.  ``rows`` selects output rows (any order, repeats
+    allowed); None means all M rows.  ``S`` is None when ``with_scale`` is
+    False.
+    """
+    code = _DTYPE_CODES[dtype]
+    oa, ob = _OPS[op_a], _OPS[op_b]
+    A = _as_input(A, dtype)
+    B = _as_input(B, dtype)
+    M, N, K, lda, ldb = _shape_of(A, B, oa, ob)
+    nrows, rows_p, keep = _rows_arg(rows, M)
     ldc = max(N, 1)
     C = np.empty((nrows, N), dtype=np.float64)
     S = np.empty((nrows, N), dtype=np.float64) if with_scale else None
     lib = _load()
     dp = ctypes.POINTER(ctypes.c_double)
-    rc = lib.oracle_gemm_rows(
-        code, M, N, K,
+    rc = lib.oracle_gemm_op_rows(
+        code, oa, ob, M, N, K,
         A.ctypes.data if A.size else None, lda,
         B.ctypes.data if B.size else None, ldb,
         nrows, rows_p,
         C.ctypes.data_as(dp) if C.size else None,
         S.ctypes.data_as(dp) if (S is not None and S.size) else None,
         ldc)
+    del keep
     if rc != 0:
-        raise ValueError("oracle_gemm_rows rejected its arguments")
+        raise ValueError("oracle_gemm_op_rows rejected its arguments")
     return C, S
 
 
 def gemm_scaled(dtype: str, alpha: float, A: np.ndarray, B: np.ndarray, beta: float,
-                C_in: np.ndarray | None, rows=None):
-    """Return (C, S) for alpha * (A @ B) + beta * C_in, in double.
+                C_in: np.ndarray | None, rows=None, op_a: str = "N", op_b: str = "N"):
+    """Return (C, S) for alpha * (op(A) @ op(B)) + beta * C_in, in double.
 
-    C_in (M x N, same element type as A and B, row stride >= N) is not read
-    when beta == 0, and may then be None.  S = |alpha| sum|a b| + |beta| |c|
-    is the scale of the normalised error."""
+    A, B and the ops are as for ``gemm``.  C_in (M x N, same element type as
+    A and B, row stride >= N) is not read when beta == 0, and may then be
+    None.  S = |alpha| sum|a b| + |beta| |c| is the scale of the normalised
+    error."""
     code = _DTYPE_CODES[dtype]
+    oa, ob = _OPS[op_a], _OPS[op_b]
     A = _as_input(A, dtype)
     B = _as_input(B, dtype)
-    M, K = A.shape
-    K2, N = B.shape
-    if K != K2:
-        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
-    lda = A.strides[0] // A.itemsize if M > 0 else max(K, 1)
-    ldb = B.strides[0] // B.itemsize if K > 0 else max(N, 1)
+    M, N, K, lda, ldb = _shape_of(A, B, oa, ob)
     if beta != 0:
         C_in = _as_input(C_in, dtype)
         if C_in.shape != (M, N):
             raise ValueError("C_in must be M x N")
-        ldc_in = C_in.strides[0] // C_in.itemsize if M > 0 else max(N, 1)
+        ldc_in = C_in.strides[0] // C_in.itemsize if M > 1 else max(N, 1)
         c_ptr = C_in.ctypes.data if C_in.size else None
     else:
         ldc_in, c_ptr = max(N, 1), None
-    if rows is None:
-        nrows, rows_p, keep = M, None, None
-    else:
-        keep = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
-        nrows = int(keep.size)
-        rows_p = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    nrows, rows_p, keep = _rows_arg(rows, M)
     ldc = max(N, 1)
     C = np.empty((nrows, N), dtype=np.float64)
     S = np.empty((nrows, N), dtype=np.float64)
     dp = ctypes.POINTER(ctypes.c_double)
-    rc = _load().oracle_gemm_scaled_rows(
-        code, M, N, K, float(alpha),
+    rc = _load().oracle_gemm_scaled_op_rows(
+        code, oa, ob, M, N, K, float(alpha),
         A.ctypes.data if A.size else None, lda, B.ctypes.data if B.size else None, ldb,
         float(beta), c_ptr, ldc_in, nrows, rows_p,
         C.ctypes.data_as(dp) if C.size else None, S.ctypes.data_as(dp) if S.size else None, ldc)
+    del keep
     if rc != 0:
-        raise ValueError("oracle_gemm_scaled_rows rejected its arguments")
+        raise ValueError("oracle_gemm_scaled_op_rows rejected its arguments")
     return C, S
 
 

@@ -25,15 +25,18 @@
  *     S[i][j] is the scale for the normalised error |dC| / sum|a*b|.
  *   - The scaled form alpha * A.B + beta * C (oracle_gemm_scaled_rows) is
  *     documented beside its function.
+ *   - Transposed storage of an operand (op = 1, oracle_gemm_op_rows) is
+ *     documented beside its function.
  *
  * The only deviation from those kernels is the accumulator type: double
  * instead of float/half, so the oracle is exact up to one double rounding per
  * add.  Half (IEEE binary16) and bfloat16 inputs are decoded to double from
  * their bit layouts by the functions below; no CUDA header is used.
  *
- * Element (i,k) of A is A[i*lda + k]; element (k,j) of B is B[k*ldb + j];
- * element (r,j) of the output is C[r*ldc + j].  Every pointer is host memory
- * owned by the caller.
+ * Element (i,k) of A is A[i*lda + k]; element (k,j) of B is B[k*ldb + j]
+ * (or, for an operand stored transposed, see a_index / b_index); element
+ * (r,j) of the output is C[r*ldc + j].  Every pointer is host memory owned
+ * by the caller.
  */
 #include <math.h>
 #include <stdint.h>
@@ -132,20 +135,41 @@ static double load_elem(int dtype, const void *p, int64_t idx)
     return oracle_bf16_to_f64(((const uint16_t *)p)[idx]);
 }
 
-/* Computes rows rows[0..nrows-1] of C and S (all M rows in order when rows is
- * NULL; then nrows must equal M).  Output row r (the r-th requested row) is
- * written to C[r*ldc ...] and S[r*ldc ...]; S may be NULL.
- * Returns 0, or -1 on invalid arguments.  K == 0 yields C = S = 0. */
-int oracle_gemm_rows(int dtype, int M, int N, int K,
-                     const void *A, int64_t lda, const void *B, int64_t ldb,
-                     int nrows, const int64_t *rows,
-                     double *C, double *S, int64_t ldc)
+/* Operand storage.  op(A) is the M x K matrix the product uses and op(B)
+ * the K x N one:
+ *   op_a == 0: element (i,k) of op(A) is A[i*lda + k]  (A stored M x K)
+ *   op_a == 1: element (i,k) of op(A) is A[k*lda + i]  (A stored K x M)
+ *   op_b == 0: element (k,j) of op(B) is B[k*ldb + j]  (B stored K x N)
+ *   op_b == 1: element (k,j) of op(B) is B[j*ldb + k]  (B stored N x K)
+ * op_b == 1 with ldb == K is the column-major B of the m.lqnn.cn SGEMM
+ * article, section 3.1 (its baseline kernel indexes B[k + col*K]); op_a == 1
+ * is the same storage for A. */
+static int64_t a_index(int op_a, int64_t i, int64_t k, int64_t lda)
+{
+    return op_a ? k * lda + i : i * lda + k;
+}
+
+static int64_t b_index(int op_b, int64_t k, int64_t j, int64_t ldb)
+{
+    return op_b ? j * ldb + k : k * ldb + j;
+}
+
+/* Computes rows rows[0..nrows-1] of C = op(A) . op(B) and of S (all M rows
+ * in order when rows is NULL; then nrows must equal M).  Output row r (the
+ * r-th requested row) is written to C[r*ldc ...] and S[r*ldc ...]; S may be
+ * NULL.  Returns 0, or -1 on invalid arguments.  K == 0 yields C = S = 0. */
+int oracle_gemm_op_rows(int dtype, int op_a, int op_b, int M, int N, int K,
+                        const void *A, int64_t lda, const void *B, int64_t ldb,
+                        int nrows, const int64_t *rows,
+                        double *C, double *S, int64_t ldc)
 {
     if (M < 0 || N < 0 || K < 0 || nrows < 0 || dtype < 0 || dtype > 2)
         return -1;
+    if ((op_a != 0 && op_a != 1) || (op_b != 0 && op_b != 1))
+        return -1;
     if (rows == NULL && nrows != M)
         return -1;
-    if (K > 0 && (lda < K || ldb < N))
+    if (K > 0 && (lda < (op_a ? M : K) || ldb < (op_b ? K : N)))
         return -1;
     if (ldc < N)
         return -1;
@@ -164,9 +188,9 @@ int oracle_gemm_rows(int dtype, int M, int N, int K,
             if (s) s[j] = 0.0;
         }
         for (int k = 0; k < K; ++k) {
-            double a = load_elem(dtype, A, i * lda + k);
+            double a = load_elem(dtype, A, a_index(op_a, i, k, lda));
             for (int j = 0; j < N; ++j) {
-                double prod = a * load_elem(dtype, B, (int64_t)k * ldb + j);
+                double prod = a * load_elem(dtype, B, b_index(op_b, k, j, ldb));
                 c[j] += prod;
                 if (s) s[j] += fabs(prod);
             }
@@ -175,7 +199,16 @@ int oracle_gemm_rows(int dtype, int M, int N, int K,
     return 0;
 }
 
-/* The scaled update C_out = alpha * (A . B) + beta * C_in.  The m.lqnn.cn
+/* Both operands as stored (op_a = op_b = 0). */
+int oracle_gemm_rows(int dtype, int M, int N, int K,
+                     const void *A, int64_t lda, const void *B, int64_t ldb,
+                     int nrows, const int64_t *rows,
+                     double *C, double *S, int64_t ldc)
+{
+    return oracle_gemm_op_rows(dtype, 0, 0, M, N, K, A, lda, B, ldb, nrows, rows, C, S, ldc);
+}
+
+/* The scaled update C_out = alpha * (op(A) . op(B)) + beta * C_in.  The m.lqnn.cn
  * SGEMM article's tiled kernel sgemm_tile_v2 takes alpha and beta arguments
  * (its listing leaves the beta term out), and the GB300 roadmap (m.nxbn.cn,
  * section 7.1) argues for fusing such epilogue work into the GEMM.  Read as
@@ -186,15 +219,17 @@ int oracle_gemm_rows(int dtype, int M, int N, int K,
  * (S is the scale of the normalised error).  C_in has the element type
  * `dtype` and leading dimension ldc_in; output row r is requested row i.
  * Returns 0, or -1 on invalid arguments. */
-int oracle_gemm_scaled_rows(int dtype, int M, int N, int K, double alpha,
-                            const void *A, int64_t lda, const void *B, int64_t ldb,
-                            double beta, const void *C_in, int64_t ldc_in,
-                            int nrows, const int64_t *rows,
-                            double *C_out, double *S_out, int64_t ldc)
+int oracle_gemm_scaled_op_rows(int dtype, int op_a, int op_b, int M, int N, int K,
+                               double alpha, const void *A, int64_t lda,
+                               const void *B, int64_t ldb,
+                               double beta, const void *C_in, int64_t ldc_in,
+                               int nrows, const int64_t *rows,
+                               double *C_out, double *S_out, int64_t ldc)
 {
     if (beta != 0.0 && (C_in == NULL || ldc_in < N))
         return -1;
-    int rc = oracle_gemm_rows(dtype, M, N, K, A, lda, B, ldb, nrows, rows, C_out, S_out, ldc);
+    int rc = oracle_gemm_op_rows(dtype, op_a, op_b, M, N, K, A, lda, B, ldb, nrows, rows,
+                                 C_out, S_out, ldc);
     if (rc != 0)
         return rc;
     for (int r = 0; r < nrows; ++r) {
@@ -208,6 +243,17 @@ int oracle_gemm_scaled_rows(int dtype, int M, int N, int K, double alpha,
         }
     }
     return 0;
+}
+
+/* Both operands as stored (op_a = op_b = 0). */
+int oracle_gemm_scaled_rows(int dtype, int M, int N, int K, double alpha,
+                            const void *A, int64_t lda, const void *B, int64_t ldb,
+                            double beta, const void *C_in, int64_t ldc_in,
+                            int nrows, const int64_t *rows,
+                            double *C_out, double *S_out, int64_t ldc)
+{
+    return oracle_gemm_scaled_op_rows(dtype, 0, 0, M, N, K, alpha, A, lda, B, ldb, beta,
+                                      C_in, ldc_in, nrows, rows, C_out, S_out, ldc);
 }
 
 /* Number of threads the parallel loop above uses. */

@@ -4,6 +4,7 @@ pages' printed numbers, invariants), chosen so that a plausible slip in it --
 a dropped term, a wrong sign or index, a transposed operand, a wrong decode or
 rounding -- fails at least one of them.  The last group plants such slips on
 purpose and checks that the pins catch them."""
+import ctypes
 import os
 from fractions import Fraction
 
@@ -408,3 +409,159 @@ def test_scaled_brute_force_and_rows():
             assert abs(Fraction(S[a, b]) - scale) <= u * scale
     Cr, Sr = oracle.gemm_scaled("f32", alpha, A, B, beta, Cin, rows=[2, 0])
     assert np.array_equal(Cr, C[[2, 0]]) and np.array_equal(Sr, S[[2, 0]])
+
+
+# ------------------------------------------------ transposed operand storage
+
+OPS = [("N", "N"), ("T", "N"), ("N", "T"), ("T", "T")]
+
+
+def _store(X, op):
+    """The array a caller passes for logical operand X under `op`."""
+    return np.ascontiguousarray(X.T) if op == "T" else np.ascontiguousarray(X)
+
+
+@pytest.mark.parametrize("op_a,op_b", OPS)
+def test_op_closed_form_polynomial_entries(op_a, op_b):
+    # The polynomial closed form above, with the operands stored transposed
+    # where op says so; M, N, K all differ so a swapped extent cannot pass.
+    for (M, N, K) in [(3, 5, 7), (6, 2, 1), (4, 9, 33)]:
+        i = np.arange(M)[:, None]
+        k = np.arange(K)
+        A = (i + 2 * k[None, :]).astype(np.float32)
+        B = (k[:, None] - 3 * np.arange(N)[None, :]).astype(np.float32)
+        C, _ = oracle.gemm("f32", _store(A, op_a), _store(B, op_b), op_a=op_a, op_b=op_b)
+        S1 = K * (K - 1) // 2
+        S2 = (K - 1) * K * (2 * K - 1) // 6
+        jj = np.arange(N)[None, :]
+        expect = i * S1 - 3 * i * jj * K + 2 * S2 - 6 * jj * S1
+        assert np.array_equal(C, expect.astype(np.float64)), (op_a, op_b, M, N, K)
+
+
+def test_op_column_major_b_index_of_the_pages():
+    # The m.lqnn.cn SGEMM article (section 3.1) stores B column-major and
+    # reads element (k, col) as B[k + col*K].  Build that flat buffer
+    # directly from the index formula and hand it over as op_b = "T" with
+    # ldb = K; the rank-one closed form C = (i+1)(j+1) K(K+1)(2K+1)/6 of
+    # A[i][k] = (i+1)(k+1), B[k][j] = (k+1)(j+1) must come out.
+    M, N, K = 3, 5, 6
+    flat = np.zeros(K * N, np.float32)
+    for col in range(N):
+        for k in range(K):
+            flat[k + col * K] = (k + 1) * (col + 1)
+    A = (np.arange(1, M + 1)[:, None] * np.arange(1, K + 1)[None, :]).astype(np.float32)
+    C, _ = oracle.gemm("f32", A, flat.reshape(N, K), op_b="T")
+    expect = np.outer(np.arange(1, M + 1), np.arange(1, N + 1)) * (K * (K + 1) * (2 * K + 1) // 6)
+    assert np.array_equal(C, expect.astype(np.float64))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("op_a,op_b", OPS)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 3, 4), (3, 2, 9)])
+def test_op_brute_force_exact_rationals(dtype, op_a, op_b, shape):
+    # Exact rational brute force on the logical operands, the oracle fed
+    # the stored (possibly transposed) arrays.
+    M, N, K = shape
+    rng = np.random.default_rng(M * 100 + N * 10 + K + 7)
+    A, At = _cast(rng.uniform(-1, 1, (M, K)), dtype)
+    B, Bt = _cast(rng.uniform(-1, 1, (K, N)), dtype)
+    Cx, Sx = _exact(At.to(torch.float64).tolist(), Bt.to(torch.float64).tolist())
+    C, S = oracle.gemm(dtype, _store(A, op_a), _store(B, op_b), op_a=op_a, op_b=op_b)
+    u = Fraction(1, 2 ** 53)
+    gamma = K * u / (1 - K * u)
+    for i in range(M):
+        for j in range(N):
+            assert abs(Fraction(C[i, j]) - Cx[i][j]) <= gamma * Sx[i][j]
+            assert abs(Fraction(S[i, j]) - Sx[i][j]) <= gamma * Sx[i][j]
+
+
+def test_op_padded_leading_dimensions_and_rows():
+    # Transposed storage with padded rows (lda > M, ldb > K), row sampling.
+    M, N, K = 5, 4, 6
+    i = np.arange(M)[:, None]
+    k = np.arange(K)
+    A = (i + 2 * k[None, :]).astype(np.float32)
+    B = (k[:, None] - 3 * np.arange(N)[None, :]).astype(np.float32)
+    Apad = np.full((K, M + 3), np.nan, np.float32)
+    Apad[:, :M] = A.T
+    Bpad = np.full((N, K + 5), np.nan, np.float32)
+    Bpad[:, :K] = B.T
+    C, _ = oracle.gemm("f32", Apad[:, :M], Bpad[:, :K], op_a="T", op_b="T")
+    S1, S2 = K * (K - 1) // 2, (K - 1) * K * (2 * K - 1) // 6
+    jj = np.arange(N)[None, :]
+    expect = (i * S1 - 3 * i * jj * K + 2 * S2 - 6 * jj * S1).astype(np.float64)
+    assert np.array_equal(C, expect)
+    Cr, _ = oracle.gemm("f32", Apad[:, :M], Bpad[:, :K], rows=[4, 1], op_a="T", op_b="T")
+    assert np.array_equal(Cr, expect[[4, 1]])
+
+
+def test_op_leading_dimension_checks():
+    # The C entry rejects a leading dimension shorter than the stored row.
+    lib = oracle._load()
+    a = np.zeros(64, np.float32)
+    c = np.zeros(64, np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    call = lambda oa, ob, lda, ldb: lib.oracle_gemm_op_rows(
+        0, oa, ob, 4, 3, 2, a.ctypes.data, lda, a.ctypes.data, ldb, 4, None,
+        c.ctypes.data_as(dp), None, 3)
+    assert call(0, 0, 2, 3) == 0 and call(0, 0, 1, 3) == -1 and call(0, 0, 2, 2) == -1
+    assert call(1, 0, 4, 3) == 0 and call(1, 0, 3, 3) == -1     # op_a T: lda >= M
+    assert call(0, 1, 2, 2) == 0 and call(0, 1, 2, 1) == -1     # op_b T: ldb >= K
+    assert call(2, 0, 4, 3) == -1
+
+
+def test_op_scaled_closed_form():
+    # Scaled form with both operands transposed: the closed form of
+    # test_scaled_closed_form.
+    M, N, K = 4, 5, 9
+    i = np.arange(M)[:, None]
+    jj = np.arange(N)[None, :]
+    k = np.arange(K)
+    A = (i + 2 * k[None, :]).astype(np.float32)
+    B = (k[:, None] - 3 * np.arange(N)[None, :]).astype(np.float32)
+    Cin = (i - jj).astype(np.float32)
+    S1, S2 = K * (K - 1) // 2, (K - 1) * K * (2 * K - 1) // 6
+    expect = 2 * (i * S1 - 3 * i * jj * K + 2 * S2 - 6 * jj * S1) - 3 * (i - jj)
+    C, _ = oracle.gemm_scaled("f32", 2.0, _store(A, "T"), _store(B, "T"), -3.0, Cin,
+                              op_a="T", op_b="T")
+    assert np.array_equal(C, expect.astype(np.float64))
+
+
+def _op_pins_pass(gemm_op):
+    """Closed-form and brute-force pins for every op pair against an
+    implementation gemm_op(A_stored, B_stored, op_a, op_b) -> C."""
+    try:
+        for op_a, op_b in OPS:
+            M, N, K = 3, 5, 7
+            i = np.arange(M)[:, None]
+            k = np.arange(K)
+            A = (i + 2 * k[None, :]).astype(np.float32)
+            B = (k[:, None] - 3 * np.arange(N)[None, :]).astype(np.float32)
+            S1, S2 = K * (K - 1) // 2, (K - 1) * K * (2 * K - 1) // 6
+            jj = np.arange(N)[None, :]
+            got = gemm_op(_store(A, op_a), _store(B, op_b), op_a, op_b)
+            if not np.array_equal(got, (i * S1 - 3 * i * jj * K + 2 * S2 - 6 * jj * S1).astype(float)):
+                return False
+        return True
+    except (ValueError, IndexError):
+        return False
+
+
+def test_op_pins_accept_the_oracle():
+    assert _op_pins_pass(lambda A, B, oa, ob: oracle.gemm("f32", A, B, op_a=oa, op_b=ob)[0])
+
+
+@pytest.mark.parametrize("slip", ["op_ignored", "ops_swapped", "a_reshaped"])
+def test_op_pins_reject_planted_slips(slip):
+    def mutant(A, B, oa, ob):
+        if slip == "op_ignored":        # transposed storage read as if not transposed
+            return oracle.gemm("f32", A, B)[0]
+        if slip == "ops_swapped":       # op_a applied to B and op_b to A
+            return oracle.gemm("f32", A, B, op_a=ob, op_b=oa)[0]
+        if slip == "a_reshaped":        # A[i*lda + k] read with lda = M on a K x M buffer
+            if oa == "T":
+                K, M = A.shape
+                A = np.ascontiguousarray(A).reshape(M, K)
+            return oracle.gemm("f32", A, B, op_b=ob)[0]
+        raise AssertionError
+    assert not _op_pins_pass(mutant)
