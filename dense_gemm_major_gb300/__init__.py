@@ -30,7 +30,13 @@ DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 # Every symbol include/dense_gemm.h declares.
 EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_device_check",
             "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
-            "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex")
+            "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
+            "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op")
+
+# Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
+# (A as K x M, B as N x K).
+OP_N, OP_T = 0, 1
+_OP_CODES = {"N": OP_N, "T": OP_T, OP_N: OP_N, OP_T: OP_T}
 
 
 class GemmError(RuntimeError):
@@ -74,6 +80,13 @@ def load() -> ctypes.CDLL:
         fn.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     lib.gemm_plan_ex.restype = i
     lib.gemm_plan_ex.argtypes = [i, i, i, i, f, vp, i, vp, i, f, vp, i, i, ctypes.POINTER(Plan)]
+    for name in ("gemm_f32_op", "gemm_f16_op", "gemm_bf16_op"):
+        fn = getattr(lib, name)
+        fn.restype = i
+        fn.argtypes = [i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+    lib.gemm_plan_op.restype = i
+    lib.gemm_plan_op.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, i,
+                                 ctypes.POINTER(Plan)]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_status_string.argtypes = [i]
     lib.gemm_device_check.restype = i
@@ -158,6 +171,29 @@ def gemm_smem_layout_offset(layout: int, row: int, col: int) -> int:
 def gemm_selftest_timeout(timeout_us: int, stream=0) -> int:
     return load().gemm_selftest_timeout(timeout_us, stream)
 
+def gemm_plan_op(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms=152):
+    """Returns (status, Plan) of a call with operand storages."""
+    plan = Plan()
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = load().gemm_plan_op(code, _OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B,
+                             ldb, beta, C, ldc, num_sms, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_f32_op(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_f32_op(_OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B, ldb,
+                              beta, C, ldc, stream)
+
+
+def gemm_f16_op(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_f16_op(_OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B, ldb,
+                              beta, C, ldc, stream)
+
+
+def gemm_bf16_op(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
+    return load().gemm_bf16_op(_OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B,
+                               ldb, beta, C, ldc, stream)
+
 
 _ENTRY = {"f32": gemm_f32, "f16": gemm_f16, "bf16": gemm_bf16}
 _ENTRY_EX = {"f32": gemm_f32_ex, "f16": gemm_f16_ex, "bf16": gemm_bf16_ex}
@@ -169,6 +205,14 @@ def gemm(dtype: str, M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 
 def gemm_ex(dtype: str, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     return _ENTRY_EX[dtype](M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+_ENTRY_OP = {"f32": gemm_f32_op, "f16": gemm_f16_op, "bf16": gemm_bf16_op}
+
+
+def gemm_op(dtype: str, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+            stream=0) -> int:
+    return _ENTRY_OP[dtype](op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 # ------------------------------------------------------------ torch wrapper
@@ -184,11 +228,26 @@ def _ld(t, rows, cols):
     return t.stride(0) if rows > 1 else max(cols, t.stride(0), 1)
 
 
+def _operand(t, rows, cols):
+    """(op, ld) of a rows x cols operand: row-major (unit column stride) as
+    op N, or a transposed view of a row-major array (unit row stride) as
+    op T, read where it is without a copy."""
+    if t.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    if cols <= 1 or t.stride(1) == 1:
+        return OP_N, _ld(t, rows, cols)
+    if rows <= 1 or t.stride(0) == 1:
+        return OP_T, t.stride(1) if cols > 1 else max(rows, 1)
+    raise ValueError("operands must have a unit row or column stride")
+
+
 def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
-    """out = alpha * (A @ B) + beta * out for row-major CUDA tensors of one
-    dtype (float32, float16, bfloat16), queued on ``stream`` (default:
-    torch's current stream).  Row-padded views (row stride > width) are
-    accepted for A, B and out; beta != 0 needs ``out``."""
+    """out = alpha * (A @ B) + beta * out for CUDA tensors of one dtype
+    (float32, float16, bfloat16), queued on ``stream`` (default: torch's
+    current stream).  A and B may be row-major or transposed views of
+    row-major arrays (e.g. ``X.t()``), which are read in place (op T); out
+    is row-major.  Row-padded views (row stride > width) are accepted;
+    beta != 0 needs ``out``."""
     import torch
     if A.device.type != "cuda" or B.device.type != "cuda":
         raise ValueError("operands must be CUDA tensors")
@@ -207,12 +266,14 @@ def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
         raise ValueError("out has the wrong shape or dtype")
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
-    if alpha == 1.0 and beta == 0.0:
-        st = gemm(code, M, N, K, A.data_ptr(), _ld(A, M, K), B.data_ptr(), _ld(B, K, N),
+    op_a, lda = _operand(A, M, K)
+    op_b, ldb = _operand(B, K, N)
+    if op_a == OP_N and op_b == OP_N and alpha == 1.0 and beta == 0.0:
+        st = gemm(code, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
                   out.data_ptr(), _ld(out, M, N), stream)
     else:
-        st = gemm_ex(code, M, N, K, float(alpha), A.data_ptr(), _ld(A, M, K), B.data_ptr(),
-                     _ld(B, K, N), float(beta), out.data_ptr(), _ld(out, M, N), stream)
+        st = gemm_op(code, op_a, op_b, M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(),
+                     ldb, float(beta), out.data_ptr(), _ld(out, M, N), stream)
     if st != GEMM_OK:
         raise GemmError(st, f"gemm_{code}")
     return out

@@ -225,12 +225,14 @@ int forced_sgemm_tn() {
   return v;
 }
 
-gemm_status_t plan_impl(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
-                        const void* B, int ldb, float beta, const void* C, int ldc, int num_sms,
-                        gemm_plan_t* plan) {
+gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
+                        const void* A, int lda, const void* B, int ldb, float beta, const void* C,
+                        int ldc, int num_sms, gemm_plan_t* plan) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
+  if ((op_a != GEMM_OP_N && op_a != GEMM_OP_T) || (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
+    return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) {
     plan->path = GEMM_PATH_NOOP;
@@ -246,17 +248,23 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, float alpha, const void*
     return GEMM_OK;
   }
   if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_ARG;
-  if (lda < K || ldb < N) return GEMM_ERR_INVALID_ARG;
+  // Stored shapes: A is M x K (op N) or K x M (op T); B is K x N or N x K.
+  const int a_rows = op_a ? K : M, a_cols = op_a ? M : K;
+  const int b_rows = op_b ? N : K, b_cols = op_b ? K : N;
+  if (lda < a_cols || ldb < b_cols) return GEMM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(A) % es) != 0 || (reinterpret_cast<uintptr_t>(B) % es) != 0)
     return GEMM_ERR_INVALID_ARG;
   const uint64_t cbytes = span_bytes(M, N, ldc, es);
-  if (overlap(A, span_bytes(M, K, lda, es), C, cbytes) ||
-      overlap(B, span_bytes(K, N, ldb, es), C, cbytes))
+  if (overlap(A, span_bytes(a_rows, a_cols, lda, es), C, cbytes) ||
+      overlap(B, span_bytes(b_rows, b_cols, ldb, es), C, cbytes))
     return GEMM_ERR_INVALID_ARG;
 
   const int sms = num_sms > 0 ? num_sms : 1;
   if (dtype == 0) {
-    const bool tma = aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
+    // TMA cannot transpose 4-byte elements: a transposed operand is staged
+    // by the transposing cp.async loaders.
+    const bool tma = !op_a && !op_b && aligned16(A) && aligned16(B) && (lda % 4 == 0) &&
+                     (ldb % 4 == 0);
     plan->path = tma ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
     // With the last partial wave split into k-halves, the wide tile (8 x 16
     // per thread, one CTA per SM) is at least as fast as the narrow one (8 x 8,
@@ -366,17 +374,20 @@ gemm_status_t plan_impl(int dtype, int M, int N, int K, float alpha, const void*
   return GEMM_OK;
 }
 
-gemm_status_t run(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
-                  const void* B, int ldb, float beta, void* C, int ldc, cudaStream_t stream) {
+gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alpha, const void* A,
+                  int lda, const void* B, int ldb, float beta, void* C, int ldc,
+                  cudaStream_t stream) {
   gemm_plan_t plan;
-  gemm_status_t st = plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, &plan);
+  gemm_status_t st =
+      plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, &plan);
   if (st != GEMM_OK) return st;
   if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
   DeviceInfo* dev = nullptr;
   st = current_device(&dev);
   if (st != GEMM_OK) return st;
   // Re-plan with the device's SM count (validation above needs no device).
-  st = plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms, &plan);
+  st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms,
+                 &plan);
   if (st != GEMM_OK) return st;
   cudaError_t e = cudaSuccess;
 
@@ -387,6 +398,8 @@ gemm_status_t run(int dtype, int M, int N, int K, float alpha, const void* A, in
     p.M = M;
     p.N = N;
     p.K = K;
+    p.op_a = op_a;
+    p.op_b = op_b;
     p.A = static_cast<const float*>(A);
     p.lda = lda;
     p.B = static_cast<const float*>(B);
@@ -432,10 +445,19 @@ gemm_status_t run(int dtype, int M, int N, int K, float alpha, const void* A, in
     const CUtensorMapDataType dt =
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     alignas(64) CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2, dgemm::kTcBK,
-                   dgemm::kTcBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb * 2, 64, dgemm::kTcBK,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+    // A: {K, M} with 64 x 128 boxes, or as stored K x M ({M, K}, 64 x 64
+    // boxes); B: {N, K} with 64 x 64 boxes, or as stored N x K ({K, N}).
+    const bool enc_a =
+        op_a ? encode_2d(&tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda * 2, 64,
+                         dgemm::kTcBK, CU_TENSOR_MAP_SWIZZLE_128B)
+             : encode_2d(&tmA, dt, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda * 2, dgemm::kTcBK,
+                         dgemm::kTcBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool enc_b =
+        op_b ? encode_2d(&tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb * 2, dgemm::kTcBK,
+                         64, CU_TENSOR_MAP_SWIZZLE_128B)
+             : encode_2d(&tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb * 2, 64,
+                         dgemm::kTcBK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!enc_a || !enc_b ||
         !encode_2d(&tmC, dt, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * 2, dgemm::kTcEpiCols,
                    32, CU_TENSOR_MAP_SWIZZLE_128B))
       return GEMM_ERR_LAUNCH;
@@ -443,6 +465,8 @@ gemm_status_t run(int dtype, int M, int N, int K, float alpha, const void* A, in
     p.M = M;
     p.N = N;
     p.K = K;
+    p.op_a = op_a;
+    p.op_b = op_b;
     p.tiles_m = ceil_div(M, plan.block_m);
     p.tiles_n = ceil_div(N, plan.block_n);
     p.group_m = tc_group_override() > 0 ? tc_group_override() : dgemm::kTcGroupM;
@@ -495,36 +519,54 @@ extern "C" {
 
 gemm_status_t gemm_f32(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                        float* C, int ldc, cudaStream_t stream) {
-  return run(0, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
+  return run(0, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
 }
 
 gemm_status_t gemm_f16(int M, int N, int K, const gemm_half_t* A, int lda, const gemm_half_t* B,
                        int ldb, gemm_half_t* C, int ldc, cudaStream_t stream) {
-  return run(1, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
+  return run(1, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
 }
 
 gemm_status_t gemm_bf16(int M, int N, int K, const gemm_bfloat16_t* A, int lda,
                         const gemm_bfloat16_t* B, int ldb, gemm_bfloat16_t* C, int ldc,
                         cudaStream_t stream) {
-  return run(2, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
+  return run(2, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream);
 }
 
 gemm_status_t gemm_f32_ex(int M, int N, int K, float alpha, const float* A, int lda,
                           const float* B, int ldb, float beta, float* C, int ldc,
                           cudaStream_t stream) {
-  return run(0, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return run(0, GEMM_OP_N, GEMM_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 gemm_status_t gemm_f16_ex(int M, int N, int K, float alpha, const gemm_half_t* A, int lda,
                           const gemm_half_t* B, int ldb, float beta, gemm_half_t* C, int ldc,
                           cudaStream_t stream) {
-  return run(1, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return run(1, GEMM_OP_N, GEMM_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 gemm_status_t gemm_bf16_ex(int M, int N, int K, float alpha, const gemm_bfloat16_t* A, int lda,
                            const gemm_bfloat16_t* B, int ldb, float beta, gemm_bfloat16_t* C,
                            int ldc, cudaStream_t stream) {
-  return run(2, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+  return run(2, GEMM_OP_N, GEMM_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_f32_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
+                          const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                          int ldc, cudaStream_t stream) {
+  return run(0, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_f16_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
+                          const gemm_half_t* A, int lda, const gemm_half_t* B, int ldb, float beta,
+                          gemm_half_t* C, int ldc, cudaStream_t stream) {
+  return run(1, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+}
+
+gemm_status_t gemm_bf16_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
+                           const gemm_bfloat16_t* A, int lda, const gemm_bfloat16_t* B, int ldb,
+                           float beta, gemm_bfloat16_t* C, int ldc, cudaStream_t stream) {
+  return run(2, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
 }
 
 const char* gemm_status_string(gemm_status_t status) {
@@ -566,13 +608,22 @@ gemm_status_t gemm_device_check(cudaStream_t stream, unsigned* fault_bits) {
 
 gemm_status_t gemm_plan(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
                         int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
-  return plan_impl(dtype, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, num_sms, plan);
+  return plan_impl(dtype, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc,
+                   num_sms, plan);
 }
 
 gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
                            const void* B, int ldb, float beta, const void* C, int ldc,
                            int num_sms, gemm_plan_t* plan) {
-  return plan_impl(dtype, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms, plan);
+  return plan_impl(dtype, GEMM_OP_N, GEMM_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                   num_sms, plan);
+}
+
+gemm_status_t gemm_plan_op(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
+                           float alpha, const void* A, int lda, const void* B, int ldb,
+                           float beta, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
+  return plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms,
+                   plan);
 }
 
 int gemm_smem_layout_offset(int layout, int row, int col) {
@@ -580,10 +631,10 @@ int gemm_smem_layout_offset(int layout, int row, int col) {
     if (row < 0 || row >= dgemm::kSgemmBM || col < 0 || col >= dgemm::kSgemmBK) return -1;
     return dgemm::sgemm_smem_offset(0, 0, row, col);
   }
-  if (layout == 1 || layout == 2) {
-    const int bn = dgemm::sgemm_bn(layout == 1 ? 8 : 16);
+  if (layout >= 1 && layout <= 4) {
+    const int bn = dgemm::sgemm_bn(layout == 1 || layout == 3 ? 8 : 16);
     if (row < 0 || row >= dgemm::kSgemmBK || col < 0 || col >= bn) return -1;
-    return dgemm::sgemm_smem_offset(1, bn, row, col);
+    return dgemm::sgemm_smem_offset(layout <= 2 ? 1 : 2, bn, row, col);
   }
   return -1;
 }

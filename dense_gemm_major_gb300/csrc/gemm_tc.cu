@@ -31,6 +31,11 @@
 //    boxes; TMA clips rows and columns beyond M and N.
 //  * Every mbarrier wait is bounded; a wait that gives up records a fault,
 //    stops this CTA's roles, drains its copies and MMAs and frees TMEM.
+//  * Operands stored transposed (kAT: A stored K x M; kBT: B stored N x K,
+//    the column-major B of the m.lqnn.cn SGEMM article, section 3.1) need no
+//    copy: TMA reads them as stored and tcgen05.mma takes an MN-major A and
+//    a K-major B directly; only the TMA coordinates, the shared-memory
+//    descriptors and the instruction descriptor's major bits change.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -117,7 +122,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const T
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <typename T, uint32_t kAbType>
+template <typename T, uint32_t kAbType, bool kAT, bool kBT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -176,10 +181,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
           const uint32_t fb = smem_u32(&bars->full[s]);
           mbar_arrive_expect_tx(fb, kABytes + boxes * kBBoxBytes);
-          tma_load_2d(smem_u32(sA + s * kABytes), &tmA, fb, kt * BK, tm * BM);
+          const uint32_t adst = smem_u32(sA + s * kABytes);
+          if constexpr (!kAT) {
+            tma_load_2d(adst, &tmA, fb, kt * BK, tm * BM);
+          } else {   // A stored K x M: two 64-row (m) blocks, MN-major
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(adst + j * kBBoxBytes, &tmA, fb, tm * BM + j * 64, kt * BK);
+          }
           const uint32_t bdst = smem_u32(sB + s * kBBytes);
-          for (int j = 0; j < boxes; ++j)
-            tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, tn * BN + w.n_off + j * 64, kt * BK);
+          for (int j = 0; j < boxes; ++j) {
+            const int n = tn * BN + w.n_off + j * 64;
+            if constexpr (!kBT)
+              tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, n, kt * BK);
+            else   // B stored N x K: 64 rows (n) of 64 k each, K-major
+              tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, kt * BK, n);
+          }
           issued = it + 1;
         }
         __syncwarp();
@@ -193,7 +209,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
       const Unit w = unit_of(u, p, nk);
-      const uint32_t idesc = instr_desc(kAbType, BM, (uint32_t)w.n_w);
+      const uint32_t idesc = instr_desc(kAbType, BM, (uint32_t)w.n_w, kAT ? 1u : 0u,
+                                        kBT ? 0u : 1u);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
       ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
@@ -211,12 +228,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            // A: +32 bytes per 16 k inside the swizzled 128-byte rows;
-            //    8-row groups 1024 bytes apart.
-            // B: +16 rows (2048 bytes) per 16 k; 64-column blocks 8 KB apart
-            //    (leading offset), 8-row k groups 1024 bytes apart (stride).
-            const uint64_t ad = smem_desc(a0 + k * UMMA_K * 2, 16, 1024);
-            const uint64_t bd = smem_desc(b0 + k * UMMA_K * 128, kBBoxBytes, 1024);
+            // A K-major (MN-major when stored transposed), B MN-major
+            // (K-major when stored transposed).
+            const uint64_t ad = kAT ? mnmajor_desc(a0, k) : kmajor_desc(a0, k);
+            const uint64_t bd = kBT ? kmajor_desc(b0, k) : mnmajor_desc(b0, k);
             mma_f16(d_tmem, ad, bd, idesc, (kt > w.kb || k > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&bars->empty[s]));   // frees the stage when the MMAs finish
@@ -336,14 +351,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <typename T, uint32_t kAb>
+template <typename T, uint32_t kAb, bool kAT, bool kBT>
 cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                          const CUtensorMap* tmC, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, kAb>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, kAb, kAT, kBT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<T, kAb><<<grid, kTcThreads, kTcSmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
+  gemm_tc_kernel<T, kAb, kAT, kBT>
+      <<<grid, kTcThreads, kTcSmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
   return cudaGetLastError();
+}
+
+template <typename T, uint32_t kAb>
+cudaError_t launch_ops(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                       const CUtensorMap* tmC, int grid, cudaStream_t stream) {
+  if (p.op_a && p.op_b) return launch_typed<T, kAb, true, true>(p, tmA, tmB, tmC, grid, stream);
+  if (p.op_a) return launch_typed<T, kAb, true, false>(p, tmA, tmB, tmC, grid, stream);
+  if (p.op_b) return launch_typed<T, kAb, false, true>(p, tmA, tmB, tmC, grid, stream);
+  return launch_typed<T, kAb, false, false>(p, tmA, tmB, tmC, grid, stream);
 }
 
 }  // namespace
@@ -353,8 +378,8 @@ static_assert(sizeof(Barriers) <= 256, "barrier block must fit its reserved spac
 cudaError_t launch_gemm_tc(int dtype, const TcParams& p, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, const CUtensorMap* tmC, int grid,
                            cudaStream_t stream) {
-  if (dtype == 1) return launch_typed<__half, 0>(p, tmA, tmB, tmC, grid, stream);
-  return launch_typed<__nv_bfloat16, 1>(p, tmA, tmB, tmC, grid, stream);
+  if (dtype == 1) return launch_ops<__half, 0>(p, tmA, tmB, tmC, grid, stream);
+  return launch_ops<__nv_bfloat16, 1>(p, tmA, tmB, tmC, grid, stream);
 }
 
 }  // namespace dgemm

@@ -27,6 +27,9 @@
 //  * acc_empty (even CTA): both CTAs' epilogue warps arrive (8 arrivals).
 // The tiles of a last partial round run as two 128-column parts.  Every
 // wait is bounded; a wait that gives up records a fault and the roles unwind.
+// Operands stored transposed (kAT, kBT) are read as stored, as in the
+// single-CTA kernel: an MN-major A (two 64-row blocks per CTA) and a K-major
+// B (the CTA's 128 columns as 128 rows of 64 k).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -113,7 +116,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const T
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-template <typename T, uint32_t kAbType>
+template <typename T, uint32_t kAbType, bool kAT, bool kBT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -183,13 +186,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         if (lane == 0) {
           const uint32_t fb = mapa_shared(smem_u32(&bars->full[s]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * (kABytes + boxes * kBBoxBytes));
-          tma_load_2d_pair(smem_u32(sA + s * kABytes), &tmA, fb, kt * BK,
-                           w.tm * (2 * BM) + (int)rank * BM);
+          if (rank == 0)
+            mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * (kABytes + boxes * kBBoxBytes));
+          const uint32_t adst = smem_u32(sA + s * kABytes);
+          const int m = w.tm * (2 * BM) + (int)rank * BM;
+          if constexpr (!kAT) {
+            tma_load_2d_pair(adst, &tmA, fb, kt * BK, m);
+          } else {   // A stored K x M: two 64-row (m) blocks, MN-major
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d_pair(adst + j * kBBoxBytes, &tmA, fb, m + j * 64, kt * BK);
+          }
           const uint32_t bdst = smem_u32(sB + s * kBBytes);
-          for (int j = 0; j < boxes; ++j)
-            tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb,
-                             w.tn * BN + w.n_off + (int)rank * half + j * 64, kt * BK);
+          for (int j = 0; j < boxes; ++j) {
+            const int n = w.tn * BN + w.n_off + (int)rank * half + j * 64;
+            if constexpr (!kBT)
+              tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb, n, kt * BK);
+            else   // B stored N x K: 64 rows (n) of 64 k each, K-major
+              tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb, kt * BK, n);
+          }
           issued = it + 1;
         }
         __syncwarp();
@@ -203,7 +217,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = pair; u < num_units && ok; u += npairs, ++local) {
         const Unit w = unit_of(u, p);
-        const uint32_t idesc = instr_desc(kAbType, 2 * BM, (uint32_t)w.n_w);
+        const uint32_t idesc = instr_desc(kAbType, 2 * BM, (uint32_t)w.n_w, kAT ? 1u : 0u,
+                                          kBT ? 0u : 1u);
         const uint32_t b = local % kAccBufs;
         const uint32_t aph = (local / kAccBufs) & 1u;
         ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
@@ -221,8 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             const uint32_t b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint64_t ad = smem_desc(a0 + k * UMMA_K * 2, 16, 1024);
-              const uint64_t bd = smem_desc(b0 + k * UMMA_K * 128, kBBoxBytes, 1024);
+              const uint64_t ad = kAT ? mnmajor_desc(a0, k) : kmajor_desc(a0, k);
+              const uint64_t bd = kBT ? kmajor_desc(b0, k) : mnmajor_desc(b0, k);
               mma_f16_pair(d_tmem, ad, bd, idesc, (kt > 0 || k > 0) ? 1u : 0u);
             }
             // Both CTAs' stage s is free once these MMAs finish.
@@ -320,15 +335,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <typename T, uint32_t kAb>
+template <typename T, uint32_t kAb, bool kAT, bool kBT>
 cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                          const CUtensorMap* tmC, int pairs, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<T, kAb>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_pair_kernel<T, kAb, kAT, kBT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kTc2SmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_pair_kernel<T, kAb><<<2 * pairs, kTcThreads, kTc2SmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
+  gemm_tc_pair_kernel<T, kAb, kAT, kBT>
+      <<<2 * pairs, kTcThreads, kTc2SmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
   return cudaGetLastError();
+}
+
+template <typename T, uint32_t kAb>
+cudaError_t launch_ops(const TcParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                       const CUtensorMap* tmC, int pairs, cudaStream_t stream) {
+  if (p.op_a && p.op_b) return launch_typed<T, kAb, true, true>(p, tmA, tmB, tmC, pairs, stream);
+  if (p.op_a) return launch_typed<T, kAb, true, false>(p, tmA, tmB, tmC, pairs, stream);
+  if (p.op_b) return launch_typed<T, kAb, false, true>(p, tmA, tmB, tmC, pairs, stream);
+  return launch_typed<T, kAb, false, false>(p, tmA, tmB, tmC, pairs, stream);
 }
 
 }  // namespace
@@ -338,8 +363,8 @@ static_assert(sizeof(Barriers) <= 256, "barrier block must fit its reserved spac
 cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap* tmA,
                                 const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,
                                 cudaStream_t stream) {
-  if (dtype == 1) return launch_typed<__half, 0>(p, tmA, tmB, tmC, pairs, stream);
-  return launch_typed<__nv_bfloat16, 1>(p, tmA, tmB, tmC, pairs, stream);
+  if (dtype == 1) return launch_ops<__half, 0>(p, tmA, tmB, tmC, pairs, stream);
+  return launch_ops<__nv_bfloat16, 1>(p, tmA, tmB, tmC, pairs, stream);
 }
 
 }  // namespace dgemm

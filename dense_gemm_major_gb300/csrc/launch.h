@@ -27,6 +27,9 @@ constexpr int sgemm_smem_bytes(int tn) {
 
 struct SgemmParams {
   int M, N, K;
+  // op_a = 1: A stored K x M, element (i,k) at A[k*lda + i]; op_b = 1: B
+  // stored N x K, element (k,j) at B[j*ldb + k] (cp.async staging only).
+  int op_a = 0, op_b = 0;
   const float* A;
   long long lda;
   const float* B;
@@ -83,9 +86,13 @@ __host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, in
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream);
 
+// The kernels for p.op_a or p.op_b set (cp.async staging that transposes):
+// tn 16 or 8 (9 is run as 8), launched like launch_sgemm.
+cudaError_t launch_sgemm_op(const SgemmParams& p, int tn, cudaStream_t stream);
+
 // Element offset of (row, col) inside one stage of the FP32 A tile
-// (which = 0) or the B tile of a BN-wide configuration (which = 1); host
-// copy of the device layout.
+// (which = 0), the B tile of a BN-wide configuration (which = 1) or the B
+// tile of a transposed B (which = 2); host copy of the device layout.
 int sgemm_smem_offset(int which, int bn, int r, int c);
 
 // ---------------------------------------------------------------- FP16/BF16 tcgen05
@@ -107,6 +114,9 @@ constexpr int kTcSmemBytes =
 
 struct TcParams {
   int M, N, K;
+  // op_a = 1: A stored K x M (an MN-major tcgen05 operand); op_b = 1: B
+  // stored N x K (K-major).  The tensor maps describe the stored arrays.
+  int op_a = 0, op_b = 0;
   int tiles_m, tiles_n;
   int group_m;        // tile rows per rasterisation group
   // Split-K mode (single-CTA kernel only, slices > 1): unit u is k-slice
@@ -150,9 +160,10 @@ inline TcSplit tc_split(int tiles, int sms) {
   return sp;
 }
 
-// dtype: 1 = FP16, 2 = BF16.  tmA: A as {K, M} with 64 x 128 boxes;
-// tmB: B as {N, K} with 64 x 64 boxes; tmC: C as {N, M} with 64 x 32 boxes;
-// all 128-byte swizzled.  grid = number of persistent CTAs.
+// dtype: 1 = FP16, 2 = BF16.  tmA: A as {K, M} with 64 x 128 boxes (op_a:
+// as stored {M, K}, 64 x 64 boxes); tmB: B as {N, K} with 64 x 64 boxes
+// (op_b: as stored {K, N}, 64 x 64 boxes); tmC: C as {N, M} with 64 x 32
+// boxes; all 128-byte swizzled.  grid = number of persistent CTAs.
 cudaError_t launch_gemm_tc(int dtype, const TcParams& p, const CUtensorMap* tmA,
                            const CUtensorMap* tmB, const CUtensorMap* tmC, int grid,
                            cudaStream_t stream);

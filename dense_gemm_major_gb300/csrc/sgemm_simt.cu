@@ -1,479 +1,12 @@
-// FP32 SIMT SGEMM for sm_103a: C = A . B, all row-major, FP32 FFMA with FP32
-// accumulation (no TF32).
-//
-// Lineage on the pages, and what changed for GB300:
-//  * Block tiling with a register-blocked outer product, 8 x 8 outputs per
-//    thread and a 128 x 128 block tile ("[CUDA 优化实战] sgemm - 超越 cuBLAS",
-//    section 2 and its resource-sizing analysis; "GEMM：从朴素实现到 shared memory
-//    tiling 与寄存器分块", section 3; m.lqnn.cn SGEMM article, the v3 register
-//    micro-tile).  A wide configuration (8 x 16 per thread, 128 x 256 block
-//    tile, one CTA per SM) serves grids of one to two narrow waves.
-//  * Vector fragment loads from shared memory (wingedge777 section 3 reads A
-//    fragments as float4 after transposing A into shared memory).  Here A is
-//    not transposed: TMA cannot transpose 4-byte elements, so A stays
-//    K-contiguous and one LDS.64 returns two k-steps of one row; B fragments
-//    are LDS.128.  Measured on sm_103a with a shared-load probe: a wavefront
-//    delivers one distinct 16-byte chunk to each group of 4 consecutive
-//    lanes (broadcast within the group is free) and a 16-byte load costs at
-//    least 2 wavefronts.  Each 4-lane group is therefore a 2 x 2 block of the
-//    warp's 4 x 8 lane grid, so every fragment load costs the minimum, 8
-//    bytes per lane per wavefront (0.125 wavefronts per FFMA at 8 x 8 outputs
-//    per thread).
-//  * An XOR-swizzled shared-memory layout that makes every fragment read
-//    conflict-free (wingedge777 section 4's SWIZZLE_A idea; GB300 roadmap
-//    m.nxbn.cn section 3.3).  The A tile uses the pattern TMA's 128-byte
-//    swizzle writes: 16-byte chunk q of row m lives at chunk q ^ (m mod 8).
-//    A warp's four row groups are interleaved (thread row tr owns rows
-//    tr + 4i) so that its four distinct rows fall in four distinct chunks.
-//  * Coalesced 16-byte C stores: each warp writes whole 128-byte row segments
-//    (wingedge777 section 5's write-back re-mapping).
-//  * The outer product is issued as packed fma.rn.f32x2 (two FP32 FMAs per
-//    lane per instruction, each rounded like fmaf): scalar FFMA would need
-//    every issue slot of an SM sub-partition to reach the FFMA peak.
-//  * A multi-stage pipeline (wingedge777 section 6 double buffer; m.lqnn.cn v4
-//    cp.async double buffer; m.nxbn.cn section 3.1-3.2 three or four stages and
-//    TMA).  Here: a 3-stage ring filled by TMA (one thread issues both tile
-//    copies, completion on an mbarrier) or, when a base or leading dimension
-//    is not 16-byte aligned, by 4-byte cp.async with zero fill completing on
-//    the same mbarrier.  One __syncthreads per 32-deep k-tile releases a slot.
-//  * Tile rasterisation in groups of 16 tile rows, so that CTAs running at
-//    the same time share A rows and B columns in L2 (the grid shape of the
-//    library kernel noted in wingedge777 section "ncu 报告").
-#include "launch.h"
-#include "ptx.cuh"
+// FP32 SIMT SGEMM: launchers of the row-major (op N, N) kernels and the
+// host copy of the shared-memory layouts.  The kernel is in sgemm_simt.cuh.
+#include "sgemm_simt.cuh"
 
 namespace dgemm {
-namespace {
-
-constexpr int BM = kSgemmBM;
-constexpr int BK = kSgemmBK;
-constexpr int kAStageFloats = BM * BK;
-
-static_assert(BK == 32, "A tile rows must be 128 bytes for the 128-byte swizzle");
-static_assert(kSgemmThreads == 256, "thread mapping below assumes 8 warps");
-
-// Offset (in floats) of A element (m, k) inside one A stage: rows of 32
-// floats, 16-byte chunk index XOR-ed with the row index mod 8.
-__host__ __device__ constexpr int a_tile_offset(int m, int k) {
-  return m * BK + ((((k >> 2) ^ (m & 7))) << 2) + (k & 3);
-}
-
-// Offset (in floats) of B element (k, n) inside one B stage of width BN:
-// plain rows; a quarter warp always reads 8 consecutive 16-byte chunks of
-// one row.
-__host__ __device__ constexpr int b_tile_offset(int bn, int k, int n) { return k * bn + n; }
-
-// 16 bytes of shared memory as two packed float pairs (one LDS.128).
-__device__ __forceinline__ ulonglong2 lds128_pairs(const float* p) {
-  return *reinterpret_cast<const ulonglong2*>(p);
-}
-
-__device__ __forceinline__ unsigned long long pack_pair(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-
-// d.lo += a.lo * b.lo and d.hi += a.hi * b.hi, each one correctly rounded
-// FMA (the same result as fmaf), issued as one packed instruction: half the
-// issue slots of two scalar FFMA.
-__device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long a,
-                                      unsigned long long b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-
-template <bool kTma, int TN, int kMinBlocks>
-__global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
-    sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const SgemmParams p) {
-  constexpr int BN = sgemm_bn(TN);
-  constexpr int S = sgemm_stages(TN);
-  constexpr int kBStageFloats = BK * BN;
-  constexpr uint32_t kStageBytes = (kAStageFloats + kBStageFloats) * 4;
-  constexpr int NH = TN / 4;   // 16-byte column groups per thread
-
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ int s_abort;
-  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
-  float* sA = reinterpret_cast<float*>(base);
-  float* sB = sA + S * kAStageFloats;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * kBStageFloats);
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-
-  // Work unit of this CTA: a whole tile; one of the two k-pieces of a split
-  // tile (consecutive CTAs) that add into C or store to the tail workspace;
-  // or, in split-K mode, one k-slice of a tile that is stored to the
-  // workspace.  (Where the result goes is decoded again in the epilogue, so
-  // that it holds no registers across the main loop.)
-  int tile, k_begin, k_end;
-  {
-    const int nk_all = (p.K + BK - 1) / BK;
-    const int b = blockIdx.x;
-    if (p.slices > 1) {
-      tile = b / p.slices;
-      const int sl = b - tile * p.slices;
-      k_begin = sl * nk_all / p.slices;
-      k_end = (sl + 1) * nk_all / p.slices;
-    } else if (b < p.full_tiles) {
-      tile = b;
-      k_begin = 0;
-      k_end = nk_all;
-    } else {
-      const int j = b - p.full_tiles;
-      tile = p.full_tiles + (j >> 1);
-      k_begin = (j & 1) ? p.split_kt : 0;
-      k_end = (j & 1) ? nk_all : p.split_kt;
-    }
-  }
-  int tm, tn;
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int m0 = tm * BM;
-  const int n0 = tn * BN;
-  const int nk = k_end - k_begin;   // k-tiles of this unit
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), kTma ? 1u : kSgemmThreads);
-    s_abort = 0;
-    fence_mbar_init();
-    if constexpr (kTma) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-    }
-  }
-  __syncthreads();
-
-  // Stage k-tile kt (counted from k_begin) into ring slot s.
-  auto issue = [&](int kt, int s) {
-    const int k0 = (k_begin + kt) * BK;
-    const uint32_t bar = smem_u32(&full[s]);
-    if constexpr (kTma) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
-        tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
-      }
-    } else {
-      // A: a warp copies one 32-float row segment (k contiguous in memory).
-      const uint32_t a_dst = smem_u32(sA + s * kAStageFloats);
-      const int ka = tid & 31;
-      const int gk = k0 + ka;
-#pragma unroll
-      for (int j = 0; j < BM / 8; ++j) {
-        const int m = (tid >> 5) + 8 * j;
-        const int gm = m0 + m;
-        const bool v = (gm < p.M) && (gk < p.K);
-        const float* src = v ? p.A + (long long)gm * p.lda + gk : p.A;
-        cp_async_4(a_dst + 4u * a_tile_offset(m, ka), src, v);
-      }
-      // B: BN consecutive threads copy one BN-float row segment.
-      constexpr int kRowsPerPass = kSgemmThreads / BN;
-      const uint32_t b_dst = smem_u32(sB + s * kBStageFloats);
-      const int nb = tid % BN;
-      const int gn = n0 + nb;
-#pragma unroll
-      for (int j = 0; j < BK / kRowsPerPass; ++j) {
-        const int k = tid / BN + kRowsPerPass * j;
-        const int gk2 = k0 + k;
-        const bool v = (gk2 < p.K) && (gn < p.N);
-        const float* src = v ? p.B + (long long)gk2 * p.ldb + gn : p.B;
-        cp_async_4(b_dst + 4u * b_tile_offset(BN, k, nb), src, v);
-      }
-      cp_async_mbar_arrive_noinc(bar);
-    }
-  };
-
-  const int pre = nk < S ? nk : S;
-  for (int kt = 0; kt < pre; ++kt) issue(kt, kt);
-
-  // Thread -> output mapping.  Warp (warp_m, warp_n) owns a 32 x (BN/2)
-  // block; lane (tr, tc) owns rows tr + 4i (i < 8) and columns
-  // tc*4 + 32h + {0..3} (h < TN/4) of it.
-  // Each group of 4 consecutive lanes is a 2 x 2 block of (tr, tc): a
-  // shared-memory wavefront delivers one distinct 16-byte chunk to each
-  // 4-lane group, so a 16-byte fragment load costs the minimum 2 wavefronts
-  // only if the group touches at most 2 chunks (2 A rows, 2 B column groups).
-  const int warp_m = warp >> 1;
-  const int warp_n = warp & 1;
-  const int tr = ((lane >> 4) << 1) | ((lane >> 1) & 1);       // 0..3
-  const int tc = (((lane >> 2) & 3) << 1) | (lane & 1);        // 0..7
-  const int a_row0 = warp_m * 32 + tr;            // row for i = 0
-  const int b_col0 = warp_n * (BN / 2) + tc * 4;
-
-  // acc[i][j] holds columns (2j, 2j+1) of row i as a packed float pair.
-  unsigned long long acc[8][TN / 2];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
-
-  int kt = 0;
-  for (; kt < nk; ++kt) {
-    const int s = kt % S;
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((kt / S) & 1), p.timeout_ns,
-                                      &s_abort);
-    if (!ok) {
-      s_abort = 1;
-    } else {
-      const float* As = sA + s * kAStageFloats + a_row0 * BK;
-      const float* Bs = sB + s * kBStageFloats + b_col0;
-      // Row (a_row0 + 4i) mod 8 = tr + 4 (i mod 2), so k-quad kq of the
-      // thread's even rows sits in chunk kq ^ tr, of its odd rows in chunk
-      // kq ^ tr ^ 4.  Four base pointers cover (kq mod 4) ^ tr.
-      const float* a_base[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) a_base[q] = As + (((q ^ tr) & 3) << 2);
-#pragma unroll
-      for (int kq = 0; kq < BK / 4; ++kq) {
-        // A fragment: four k-steps of each of the thread's 8 rows.
-        float4 a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a[i] = *reinterpret_cast<const float4*>(a_base[kq & 3] + 4 * i * BK +
-                                                  (((kq & 4) ^ ((i & 1) << 2)) << 2));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float* brow = Bs + (kq * 4 + kk) * BN;
-          ulonglong2 b[NH];
-#pragma unroll
-          for (int h = 0; h < NH; ++h) b[h] = lds128_pairs(brow + 32 * h);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float av = (&a[i].x)[kk];
-            const unsigned long long aa = pack_pair(av, av);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              ffma2(acc[i][2 * h + 0], aa, b[h].x);
-              ffma2(acc[i][2 * h + 1], aa, b[h].y);
-            }
-          }
-        }
-      }
-    }
-    // Every thread is done with slot s (or some thread gave up).
-    if (__syncthreads_or(!ok)) break;
-    if (kt + S < nk) issue(kt + S, s);
-  }
-
-  if (kt < nk) {
-    // A wait gave up: record it, let this CTA's own copies land, and leave
-    // without writing C.
-    if (tid == 0) raise_fault(p.fault, kFaultSgemmFullWait);
-    if constexpr (kTma) {
-      if (tid == 0) {
-        const int issued = (kt + S < nk) ? kt + S : nk;
-        for (int t = kt; t < issued; ++t) {
-          if (!mbar_wait_bounded(smem_u32(&full[t % S]), (uint32_t)((t / S) & 1), p.timeout_ns,
-                                 nullptr)) {
-            raise_fault(p.fault, kFaultDrainWait);
-            break;
-          }
-        }
-      }
-    } else {
-      cp_async_wait_all();
-    }
-    __syncthreads();
-    return;
-  }
-
-  // Destination: unscaled FP32 partial sums go to
-  // part[(gm - part_m0) * part_ld + gn - part_n0]; add_into_c pieces add
-  // into C; everything else is stored to C.
-  float* part = nullptr;
-  long long part_ld = 0;
-  int part_m0 = 0, part_n0 = 0;
-  bool add_into_c = false;
-  {
-    const int b = blockIdx.x;
-    if (p.slices > 1) {
-      part = p.ws + (long long)(b % p.slices) * p.M * p.ldw;
-      part_ld = p.ldw;
-    } else if (b >= p.full_tiles) {
-      if (p.tail_ws != nullptr) {
-        part = p.tail_ws + (long long)(b - p.full_tiles) * (BM * BN);
-        part_ld = BN;
-        part_m0 = m0;
-        part_n0 = n0;
-      } else {
-        add_into_c = true;
-      }
-    }
-  }
-
-  // Scaling pass, C := alpha * (A.B) + beta * C, applied to the
-  // accumulators in place before any store (partial sums for a workspace
-  // stay unscaled).  The old C of one row (TN values) is loaded at once so
-  // that those loads overlap instead of each waiting behind a store.
-  if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
-    const bool vec4c = p.c_vec4 != 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int gm = m0 + a_row0 + 4 * i;
-      const float* crow = p.C + (long long)gm * p.ldc;
-      float4 old[NH];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const int gn = n0 + b_col0 + 32 * h;
-        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.beta != 0.f && gm < p.M) {
-          if (vec4c && gn + 3 < p.N) {
-            c = *reinterpret_cast<const float4*>(crow + gn);
-          } else {
-            if (gn + 0 < p.N) c.x = crow[gn + 0];
-            if (gn + 1 < p.N) c.y = crow[gn + 1];
-            if (gn + 2 < p.N) c.z = crow[gn + 2];
-            if (gn + 3 < p.N) c.w = crow[gn + 3];
-          }
-        }
-        old[h] = c;
-      }
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const float2 lo = unpack_pair(acc[i][2 * h + 0]);
-        const float2 hi = unpack_pair(acc[i][2 * h + 1]);
-        // (A column past N got c = 0 and is never stored.)
-        const auto upd = [&](float v, float cv) {
-          return p.beta != 0.f ? fmaf(p.beta, cv, p.alpha * v) : p.alpha * v;
-        };
-        acc[i][2 * h + 0] = pack_pair(upd(lo.x, old[h].x), upd(lo.y, old[h].y));
-        acc[i][2 * h + 1] = pack_pair(upd(hi.x, old[h].z), upd(hi.y, old[h].w));
-      }
-    }
-  }
-
-  // Epilogue: each store instruction of a warp covers four full 128-byte row
-  // segments of C.
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + a_row0 + 4 * i;
-    if (gm >= p.M) continue;
-    // Column gn of this row is crow[gn - cshift].
-    float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
-                                  : p.C + (long long)gm * p.ldc;
-    const int cshift = part_n0;
-    const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const int gn = n0 + b_col0 + 32 * h;
-      const float2 lo = unpack_pair(acc[i][2 * h + 0]);
-      const float2 hi = unpack_pair(acc[i][2 * h + 1]);
-      const float v0 = lo.x, v1 = lo.y, v2 = hi.x, v3 = hi.y;
-      if (add_into_c) {
-        if (vec4 && gn + 3 < p.N) {
-          atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
-        } else {
-          if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
-          if (gn + 1 < p.N) atomicAdd(crow + gn + 1, v1);
-          if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
-          if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
-        }
-      } else if (vec4 && gn + 3 < p.N) {
-        *reinterpret_cast<float4*>(crow + gn - cshift) = make_float4(v0, v1, v2, v3);
-      } else {
-        if (gn + 0 < p.N) crow[gn + 0 - cshift] = v0;
-        if (gn + 1 < p.N) crow[gn + 1 - cshift] = v1;
-        if (gn + 2 < p.N) crow[gn + 2 - cshift] = v2;
-        if (gn + 3 < p.N) crow[gn + 3 - cshift] = v3;
-      }
-    }
-  }
-}
-
-// Writes C := alpha * (piece 0 + piece 1) + beta * C on the split tiles
-// [full_tiles, tiles_m * tiles_n) from their two partial sums in tail_ws.
-// Block (j, y) takes 2048 consecutive elements (2048 / bn rows) of split tile
-// j, 8 per thread at a stride of 256; every thread issues all its loads
-// before its first store, so the loads overlap.
-constexpr int kFixupElems = 2048;
-__global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int bn) {
-  const int j = (int)blockIdx.x;
-  int tm, tn;
-  grouped_tile(p.full_tiles + j, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int rows = min(BM, p.M - tm * BM);
-  const int cols = min(bn, p.N - tn * bn);
-  const float* __restrict__ p0 = p.tail_ws + (long long)(2 * j) * (BM * bn);
-  const float* __restrict__ p1 = p0 + BM * bn;
-  float* __restrict__ c0 = p.C + (long long)(tm * BM) * p.ldc + tn * bn;
-  const int first = (int)blockIdx.y * kFixupElems;
-  constexpr int kPer = kFixupElems / 256;
-  float v[kPer], old[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = first + (int)threadIdx.x + 256 * q;
-    const int r = idx / bn;
-    const int c = idx - r * bn;
-    v[q] = 0.f;
-    old[q] = 0.f;
-    if (r < rows && c < cols) {
-      v[q] = p0[idx] + p1[idx];
-      if (p.beta != 0.f) old[q] = c0[(long long)r * p.ldc + c];
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = first + (int)threadIdx.x + 256 * q;
-    const int r = idx / bn;
-    const int c = idx - r * bn;
-    if (r < rows && c < cols) {
-      const float a = p.alpha * v[q];
-      c0[(long long)r * p.ldc + c] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
-    }
-  }
-}
-
-// Zeroes C on the split tiles [full_tiles, tiles_m * tiles_n), one CTA per
-// tile, before their two k-pieces add into it.
-__global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn) {
-  int tm, tn;
-  grouped_tile(p.full_tiles + (int)blockIdx.x, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int rows = min(BM, p.M - tm * BM);
-  const int cols = min(bn, p.N - tn * bn);
-  for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
-    const int r = idx / cols;
-    const int c = idx - r * cols;
-    p.C[(long long)(tm * BM + r) * p.ldc + tn * bn + c] = 0.f;
-  }
-}
-
-template <bool kTma, int TN, int kMinBlocks>
-cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                       cudaStream_t stream) {
-  // The attribute is per function; setting it on every call is cheap and
-  // keeps this correct for every device of the process.
-  cudaError_t e = cudaFuncSetAttribute(sgemm_kernel<kTma, TN, kMinBlocks>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       sgemm_smem_bytes(TN));
-  if (e != cudaSuccess) return e;
-  const int tiles = p.tiles_m * p.tiles_n;
-  const int split = p.slices > 1 ? 0 : tiles - p.full_tiles;
-  if (split > 0 && p.tail_ws == nullptr) {
-    sgemm_zero_split_tiles<<<split, 256, 0, stream>>>(p, sgemm_bn(TN));
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  const dim3 grid((unsigned)(p.slices > 1 ? tiles * p.slices : tiles + split));
-  sgemm_kernel<kTma, TN, kMinBlocks>
-      <<<grid, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || split == 0 || p.tail_ws == nullptr) return e;
-  const dim3 fixup_grid((unsigned)split, (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
-  sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN));
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream) {
+  if (p.op_a || p.op_b) return launch_sgemm_op(p, tn, stream);
   CUtensorMap none{};
   if (!use_tma) tmA = tmB = &none;
   if (tn == 16)
@@ -488,7 +21,8 @@ cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUten
 
 // Host-visible copy of the A / B stage layouts, for layout checks on the CPU.
 int sgemm_smem_offset(int which, int bn, int r, int c) {
-  return which == 0 ? a_tile_offset(r, c) : b_tile_offset(bn, r, c);
+  if (which == 0) return a_tile_offset(r, c);
+  return which == 1 ? b_tile_offset(bn, r, c) : bt_tile_offset(bn, r, c);
 }
 
 }  // namespace dgemm

@@ -26,15 +26,29 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor for kind::f16: FP32 accumulator, A and B of one
-// type (0 = FP16, 1 = BF16), A K-major, B N-major, M = m, N = n.
-__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, uint32_t m, uint32_t n) {
+// type (0 = FP16, 1 = BF16), M = m, N = n; a_mn / b_mn = 1 when that
+// operand is MN-major in shared memory (M or N contiguous), 0 when K-major.
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, uint32_t m, uint32_t n,
+                                                  uint32_t a_mn = 0, uint32_t b_mn = 1) {
   return (1u << 4)                 // D format: FP32
          | (ab_type << 7)          // A format
          | (ab_type << 10)         // B format
-         | (0u << 15)              // A major: K
-         | (1u << 16)              // B major: MN
+         | (a_mn << 15)            // A major
+         | (b_mn << 16)            // B major
          | ((n >> 3) << 17)
          | ((m >> 4) << 24);
+}
+
+// Shared-memory descriptors of one 16-deep k-step (k16 = 0..3) of a 64-deep
+// stage, 128-byte swizzled, 8-row groups 1024 bytes apart:
+//  * K-major (rows of 64 k, 128 bytes): +32 bytes per k-step;
+//  * MN-major (rows of 64 m or n, 128 bytes, one row per k; 64-wide blocks
+//    8 KB apart): +16 rows = 2048 bytes per k-step, leading offset 8 KB.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k16) {
+  return smem_desc(base + k16 * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k16) {
+  return smem_desc(base + k16 * 2048, 8192, 1024);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

@@ -146,8 +146,9 @@ gemm_status_t gemm_f32_noalloc(int M, int N, int K,
  *  - beta == 0: the old C is not read (NaN or Inf there is ignored).
  *  - alpha == 0 or K == 0: C := beta * C and A, B are not read (they may be
  *    NULL); beta == 0 as well gives zeros.
- *  - gemm_f32_ex with beta != 0 does not split a last partial wave of tiles
- *    into k-halves (they add into C, which would then not start at zero).
+ *  - gemm_f32_ex with beta != 0 computes the k-halves of a last partial
+ *    wave of tiles into the library's workspace (two FP32 tiles per split
+ *    tile, gemm_plan_t.workspace_bytes) and combines them in a fixed order.
  * alpha = 1, beta = 0 is exactly the plain entry point.
  */
 gemm_status_t gemm_f32_ex(int M, int N, int K, float alpha,
@@ -161,6 +162,46 @@ gemm_status_t gemm_f16_ex(int M, int N, int K, float alpha,
                           gemm_half_t *C, int ldc,
                           cudaStream_t stream);
 gemm_status_t gemm_bf16_ex(int M, int N, int K, float alpha,
+                           const gemm_bfloat16_t *A, int lda,
+                           const gemm_bfloat16_t *B, int ldb, float beta,
+                           gemm_bfloat16_t *C, int ldc,
+                           cudaStream_t stream);
+
+/*
+ * Storage of an operand.  The m.lqnn.cn SGEMM article (section 3.1) starts
+ * from a B stored column-major, element (k, col) at B[k + col*K], and speeds
+ * its kernel up by changing that layout outside the GEMM; these entry points
+ * take either storage as it is:
+ *   op_a == GEMM_OP_N: A stored M x K, element (i,k) at A[i*lda + k], lda >= K
+ *   op_a == GEMM_OP_T: A stored K x M, element (i,k) at A[k*lda + i], lda >= M
+ *   op_b == GEMM_OP_N: B stored K x N, element (k,j) at B[k*ldb + j], ldb >= N
+ *   op_b == GEMM_OP_T: B stored N x K, element (k,j) at B[j*ldb + k], ldb >= K
+ *                      (the article's column-major B when ldb == K)
+ * C is always stored M x N row-major (ldc >= N).
+ */
+typedef enum gemm_op_t { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+/*
+ * C := alpha * op(A) . op(B) + beta * C, with the conventions of the _ex
+ * entry points otherwise; (GEMM_OP_N, GEMM_OP_N) is exactly gemm_*_ex.
+ *  - FP16/BF16: both storages are read by TMA (a transposed A is an
+ *    MN-major and a transposed B a K-major tcgen05 operand); the 16-byte
+ *    alignment rule applies to lda and ldb in either storage.
+ *  - FP32: a transposed operand is staged with 4-byte cp.async (TMA cannot
+ *    transpose 4-byte elements), any alignment accepted.
+ *  - An op other than GEMM_OP_N / GEMM_OP_T is GEMM_ERR_INVALID_ARG.
+ */
+gemm_status_t gemm_f32_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
+                          const float *A, int lda,
+                          const float *B, int ldb, float beta,
+                          float *C, int ldc,
+                          cudaStream_t stream);
+gemm_status_t gemm_f16_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
+                          const gemm_half_t *A, int lda,
+                          const gemm_half_t *B, int ldb, float beta,
+                          gemm_half_t *C, int ldc,
+                          cudaStream_t stream);
+gemm_status_t gemm_bf16_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
                            const gemm_bfloat16_t *A, int lda,
                            const gemm_bfloat16_t *B, int ldb, float beta,
                            gemm_bfloat16_t *C, int ldc,
@@ -221,6 +262,12 @@ gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha,
                            const void *A, int lda, const void *B, int ldb, float beta,
                            const void *C, int ldc, int num_sms, gemm_plan_t *plan);
 
+/* The plan of a call with operand storages (gemm_*_op); gemm_plan_ex is
+ * op_a = op_b = GEMM_OP_N. */
+gemm_status_t gemm_plan_op(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
+                           float alpha, const void *A, int lda, const void *B, int ldb,
+                           float beta, const void *C, int ldc, int num_sms, gemm_plan_t *plan);
+
 /*
  * Shared-memory layout of the kernels' operand tiles, as an element offset
  * inside one stage (for host-side bank-conflict and bijectivity checks of
@@ -228,7 +275,9 @@ gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha,
  * layout: 0 = FP32 A tile (128 rows x 32 k, 128-byte XOR swizzle),
  *         1 = FP32 B tile of the narrow configuration (32 k x 128 columns),
  *         2 = FP32 B tile of the wide configuration (32 k x 256 columns);
- *         B tiles are unswizzled.
+ *         these B tiles are unswizzled;
+ *         3, 4 = the B tiles of the narrow / wide configuration for a B
+ *         stored transposed (16-byte chunk c of row k at c ^ ((k / 4) mod 8)).
  * Returns -1 for an unknown layout or out-of-range coordinates.
  */
 int gemm_smem_layout_offset(int layout, int row, int col);

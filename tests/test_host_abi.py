@@ -1,6 +1,7 @@
 """Host-side tests of the C ABI (no GPU needed): the library loads and
 exports every declared symbol, argument validation, path selection, and the
 shared-memory layouts' swizzle properties."""
+import ctypes
 import os
 import re
 
@@ -197,7 +198,7 @@ def test_a_tile_layout_is_the_tma_128b_swizzle_and_a_bijection():
             seen.add(off)
     assert len(seen) == 128 * 32
     assert dg.gemm_smem_layout_offset(0, 128, 0) == -1
-    assert dg.gemm_smem_layout_offset(3, 0, 0) == -1
+    assert dg.gemm_smem_layout_offset(5, 0, 0) == -1
 
 
 def _wavefronts(byte_addrs, width):
@@ -320,3 +321,116 @@ def test_scaled_plans():
             == dg.GEMM_ERR_INVALID_ARG
         assert dg.gemm_ex(dt, 4, 4, 4, 1.0, FAKE, 4, FAKE + 4096, 4, 1.0, FAKE + 16, 4, 0) \
             == dg.GEMM_ERR_INVALID_ARG
+
+
+# ------------------------------------------------ operands stored transposed
+
+def test_transposed_b_tiles_permute_chunks_within_rows():
+    for layout, bn in ((3, 128), (4, 256)):
+        for k in range(32):
+            offs = [dg.gemm_smem_layout_offset(layout, k, n) for n in range(bn)]
+            assert sorted(offs) == list(range(k * bn, (k + 1) * bn))
+            for n in range(0, bn, 4):     # 16-byte chunks stay whole and aligned
+                assert offs[n] % 4 == 0 and offs[n + 1:n + 4] == [offs[n] + 1, offs[n] + 2, offs[n] + 3]
+                assert (offs[n] - k * bn) // 32 == n // 32   # within its 128-byte segment
+        assert dg.gemm_smem_layout_offset(layout, 32, 0) == -1
+        assert dg.gemm_smem_layout_offset(layout, 0, bn) == -1
+
+
+def test_transposed_b_fragment_reads():
+    # The kernel reads B element (k, n = (BN/2) wn + 4 tc + 32 h) of a
+    # transposed-B tile at k BN + (BN/2) wn + 4 (tc ^ (k / 4)) + 32 h: that
+    # formula must agree with the layout, and the reads take 2 wavefronts.
+    for layout, bn in ((3, 128), (4, 256)):
+        for wn in range(2):
+            for k in range(32):
+                for h in range(bn // 64):
+                    addrs = []
+                    for l in range(32):
+                        tc = _lane_rc(l)[1]
+                        n = (bn // 2) * wn + 4 * tc + 32 * h
+                        kernel = k * bn + (bn // 2) * wn + 4 * (tc ^ (k >> 2)) + 32 * h
+                        assert dg.gemm_smem_layout_offset(layout, k, n) == kernel
+                        addrs.append(4 * kernel)
+                    assert _wavefronts(addrs, 16) == 2
+
+
+def _bt_copy(j, w, l, bn):
+    """(k, n) that lane l of warp w writes in copy j of a transposed B."""
+    return 4 * (l & 7) + (j & 3), 4 * ((bn // 32) * w + (j >> 2)) + (l >> 3)
+
+
+def _at_copy(j, w, l):
+    """(m, k) that lane l of warp w writes in copy j of a transposed A."""
+    idx = 16 * w + j
+    return 8 * (idx >> 3) + (l & 7), 4 * (idx & 7) + (l >> 3)
+
+
+def test_transposing_copies_cover_the_tiles_and_are_conflict_free():
+    seen = set()
+    for w in range(8):
+        for j in range(16):
+            mk = [_at_copy(j, w, l) for l in range(32)]
+            seen.update(mk)
+            assert _wavefronts([4 * dg.gemm_smem_layout_offset(0, m, k) for m, k in mk], 4) == 1
+    assert seen == {(m, k) for m in range(128) for k in range(32)}
+    for layout, bn in ((3, 128), (4, 256)):
+        seen = set()
+        for w in range(8):
+            for j in range(bn // 8):
+                kn = [_bt_copy(j, w, l, bn) for l in range(32)]
+                seen.update(kn)
+                assert _wavefronts([4 * dg.gemm_smem_layout_offset(layout, k, n) for k, n in kn],
+                                   4) == 1
+        assert seen == {(k, n) for k in range(32) for n in range(bn)}
+
+
+def test_transposing_b_copy_into_plain_rows_would_conflict():
+    # The same copy pattern into the unswizzled B tile puts 8 lanes on each
+    # bank: the swizzle of the transposed-B tile is what removes that.
+    kn = [_bt_copy(0, 0, l, 256) for l in range(32)]
+    assert _wavefronts([4 * dg.gemm_smem_layout_offset(2, k, n) for k, n in kn], 4) == 8
+
+
+def test_op_plans_and_validation():
+    M, N, K = 300, 200, 100
+    args = (FAKE, 0, FAKE + (1 << 24), 0)
+    def plan(dt, oa, ob, lda, ldb, alpha=1.0, beta=0.0):
+        return dg.gemm_plan_op(dt, oa, ob, M, N, K, alpha, FAKE, lda, FAKE + (1 << 24), ldb,
+                               beta, FAKE + (1 << 26), N, 152)
+    # leading dimensions: op N A needs lda >= K, op T A needs lda >= M;
+    # op N B needs ldb >= N, op T B needs ldb >= K
+    assert plan("f32", "N", "N", K, N)[0] == dg.GEMM_OK
+    assert plan("f32", "T", "N", M, N)[0] == dg.GEMM_OK
+    assert plan("f32", "T", "N", M - 1, N)[0] == dg.GEMM_ERR_INVALID_ARG
+    assert plan("f32", "N", "T", K, K)[0] == dg.GEMM_OK
+    assert plan("f32", "N", "T", K, K - 1)[0] == dg.GEMM_ERR_INVALID_ARG
+    assert plan("f32", "T", "T", M, K)[0] == dg.GEMM_OK
+    # an unknown op is an argument error
+    assert dg.load().gemm_plan_op(0, 2, 0, M, N, K, 1.0, FAKE, K, FAKE + (1 << 24), N, 0.0,
+                                  FAKE + (1 << 26), N, 152, ctypes.byref(dg.Plan())) \
+        == dg.GEMM_ERR_INVALID_ARG
+    # FP32: a transposed operand is staged by cp.async even when aligned
+    assert plan("f32", "N", "N", 104, 200)[1].path == dg.PATH_SIMT_TMA
+    assert plan("f32", "T", "N", 304, 200)[1].path == dg.PATH_SIMT_CPASYNC
+    assert plan("f32", "N", "T", 104, 104)[1].path == dg.PATH_SIMT_CPASYNC
+    # FP16/BF16: TMA either way; the stored row must be 16-byte aligned
+    for dt in ("f16", "bf16"):
+        st, p = plan(dt, "T", "T", 304, 104)
+        assert st == dg.GEMM_OK and p.path == dg.PATH_TC_TMA
+        assert plan(dt, "T", "N", 301, 200)[0] == dg.GEMM_ERR_MISALIGNED
+        assert plan(dt, "N", "T", 104, 100)[0] == dg.GEMM_ERR_MISALIGNED
+    # the same tiles and split as the row-major call
+    st0, p0 = dg.gemm_plan("bf16", 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
+                           FAKE + (2 << 30), 4096, 152)
+    st1, p1 = dg.gemm_plan_op("bf16", "T", "T", 4096, 4096, 4096, 1.0, FAKE, 4096,
+                              FAKE + (1 << 30), 4096, 0.0, FAKE + (2 << 30), 4096, 152)
+    assert (p0.tiles, p0.ctas, p0.split_tiles, p0.cluster_ctas) == \
+        (p1.tiles, p1.ctas, p1.split_tiles, p1.cluster_ctas)
+    # overlap uses the stored extent: A stored K x M spans (K-1) lda + M
+    A = FAKE
+    C = FAKE + 4 * ((K - 1) * M + M)          # just past A's last element
+    assert dg.gemm_plan_op("f32", "T", "N", M, N, K, 1.0, A, M, FAKE + (1 << 24), N, 0.0, C, N,
+                           152)[0] == dg.GEMM_OK
+    assert dg.gemm_plan_op("f32", "T", "N", M, N, K, 1.0, A, M, FAKE + (1 << 24), N, 0.0, C - 4,
+                           N, 152)[0] == dg.GEMM_ERR_INVALID_ARG
