@@ -24,7 +24,7 @@ GEMM_ERR_LAUNCH = 4
 GEMM_ERR_DEVICE_TIMEOUT = 5
 GEMM_ERR_SCRATCH_LIMIT = 6
 
-PATH_NOOP, PATH_ZERO_FILL, PATH_SIMT_TMA, PATH_SIMT_CPASYNC, PATH_TC_TMA = range(5)
+PATH_NOOP, PATH_ZERO_FILL, PATH_SIMT_TMA, PATH_SIMT_CPASYNC, PATH_TC_TMA, PATH_SIMT_MIXED = range(6)
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 
 # Every symbol include/dense_gemm.h declares.

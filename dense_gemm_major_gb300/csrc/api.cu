@@ -262,10 +262,15 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   const int sms = num_sms > 0 ? num_sms : 1;
   if (dtype == 0) {
     // TMA cannot transpose 4-byte elements: a transposed operand is staged
-    // by the transposing cp.async loaders.
-    const bool tma = !op_a && !op_b && aligned16(A) && aligned16(B) && (lda % 4 == 0) &&
-                     (ldb % 4 == 0);
-    plan->path = tma ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
+    // by the transposing cp.async loaders; with exactly one transposed, the
+    // other comes by TMA when it is 16-byte aligned.
+    const bool a16 = aligned16(A) && (lda % 4 == 0), b16 = aligned16(B) && (ldb % 4 == 0);
+    if (!op_a && !op_b)
+      plan->path = (a16 && b16) ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
+    else if (op_a != op_b && (op_a ? b16 : a16))
+      plan->path = GEMM_PATH_SIMT_MIXED;
+    else
+      plan->path = GEMM_PATH_SIMT_CPASYNC;
     // With the last partial wave split into k-halves, the wide tile (8 x 16
     // per thread, one CTA per SM) is at least as fast as the narrow one (8 x 8,
     // two CTAs per SM) once the narrow grid has more tiles than SMs (measured
@@ -427,17 +432,19 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
-    const bool tma = plan.path == GEMM_PATH_SIMT_TMA;
-    alignas(64) CUtensorMap tmA, tmB;
-    if (tma) {
-      if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
-                     (uint64_t)lda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
-                     (uint64_t)ldb * 4, (uint32_t)plan.block_n, dgemm::kSgemmBK,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-        return GEMM_ERR_LAUNCH;
-    }
+    const bool tma = plan.path == GEMM_PATH_SIMT_TMA || plan.path == GEMM_PATH_SIMT_MIXED;
+    alignas(64) CUtensorMap tmA{}, tmB{};
+    // (Mixed staging: only the operand that is not transposed has a map.)
+    if (tma && !op_a &&
+        !encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
+                   (uint64_t)lda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return GEMM_ERR_LAUNCH;
+    if (tma && !op_b &&
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
+                   (uint64_t)ldb * 4, (uint32_t)plan.block_n, dgemm::kSgemmBK,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return GEMM_ERR_LAUNCH;
     e = dgemm::launch_sgemm(p, tn, tma, &tmA, &tmB, stream);
     if (e == cudaSuccess && p.slices > 1)
       e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, alpha, beta, stream);

@@ -86,9 +86,12 @@ __host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, in
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream);
 
-// The kernels for p.op_a or p.op_b set (cp.async staging that transposes):
-// tn 16 or 8 (9 is run as 8), launched like launch_sgemm.
-cudaError_t launch_sgemm_op(const SgemmParams& p, int tn, cudaStream_t stream);
+// The kernels for p.op_a or p.op_b set: the transposed operand(s) staged
+// by transposing cp.async copies; with use_tma (exactly one operand
+// transposed, the other 16-byte aligned) the other operand by TMA through
+// its tensor map.  tn 16 or 8 (9 is run as 8), launched like launch_sgemm.
+cudaError_t launch_sgemm_op(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
+                            const CUtensorMap* tmB, cudaStream_t stream);
 
 // Element offset of (row, col) inside one stage of the FP32 A tile
 // (which = 0), the B tile of a BN-wide configuration (which = 1) or the B

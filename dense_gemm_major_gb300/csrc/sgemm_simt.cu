@@ -6,9 +6,9 @@ namespace dgemm {
 
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream) {
-  if (p.op_a || p.op_b) return launch_sgemm_op(p, tn, stream);
   CUtensorMap none{};
   if (!use_tma) tmA = tmB = &none;
+  if (p.op_a || p.op_b) return launch_sgemm_op(p, tn, use_tma, tmA, tmB, stream);
   if (tn == 16)
     return use_tma ? launch_cfg<true, 16, 1>(p, tmA, tmB, stream)
                    : launch_cfg<false, 16, 1>(p, tmA, tmB, stream);

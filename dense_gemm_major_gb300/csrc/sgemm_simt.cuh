@@ -108,16 +108,22 @@ __device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long 
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
-// kTA / kTB: A stored K x M / B stored N x K (cp.async staging only).
+// kTA / kTB: A stored K x M / B stored N x K, staged by the transposing
+// cp.async copies.  kTma: the operands that are not transposed come by TMA
+// (all others by cp.async); with one operand transposed the two kinds of
+// copy complete on the same mbarrier (1 TMA arrival + 256 cp.async ones).
 template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false>
 __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const SgemmParams p) {
-  static_assert(!(kTma && (kTA || kTB)), "TMA cannot stage a transposed FP32 operand");
+  static_assert(!(kTma && kTA && kTB), "with both operands transposed nothing is TMA-staged");
+  constexpr bool kCpA = !kTma || kTA;   // A staged by cp.async
+  constexpr bool kCpB = !kTma || kTB;   // B staged by cp.async
+  constexpr bool kAnyCp = kCpA || kCpB;
+  constexpr uint32_t kBarCount = (kTma ? 1u : 0u) + (kAnyCp ? (uint32_t)kSgemmThreads : 0u);
   constexpr int BN = sgemm_bn(TN);
   constexpr int S = sgemm_stages(TN);
   constexpr int kBStageFloats = BK * BN;
-  constexpr uint32_t kStageBytes = (kAStageFloats + kBStageFloats) * 4;
   constexpr int NH = TN / 4;   // 16-byte column groups per thread
 
   extern __shared__ unsigned char smem_raw[];
@@ -163,13 +169,11 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int nk = k_end - k_begin;   // k-tiles of this unit
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), kTma ? 1u : kSgemmThreads);
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), kBarCount);
     s_abort = 0;
     fence_mbar_init();
-    if constexpr (kTma) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-    }
+    if constexpr (!kCpA) tma_prefetch_desc(&tmA);
+    if constexpr (!kCpB) tma_prefetch_desc(&tmB);
   }
   __syncthreads();
 
@@ -179,13 +183,17 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     const uint32_t bar = smem_u32(&full[s]);
     if constexpr (kTma) {
       if (tid == 0) {
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
-        tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
+        mbar_arrive_expect_tx(bar, (kCpA ? 0u : kAStageFloats * 4u) +
+                                       (kCpB ? 0u : (uint32_t)kBStageFloats * 4u));
+        if constexpr (!kCpA) tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
+        if constexpr (!kCpB) tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
       }
-    } else {
+    }
+    if constexpr (kAnyCp) {
       const uint32_t a_dst = smem_u32(sA + s * kAStageFloats);
-      if constexpr (!kTA) {
+      if constexpr (!kCpA) {
+        // A comes by TMA.
+      } else if constexpr (!kTA) {
         // A: a warp copies one 32-float row segment (k contiguous in memory).
         const int ka = tid & 31;
         const int gk = k0 + ka;
@@ -213,7 +221,9 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
         }
       }
       const uint32_t b_dst = smem_u32(sB + s * kBStageFloats);
-      if constexpr (!kTB) {
+      if constexpr (!kCpB) {
+        // B comes by TMA.
+      } else if constexpr (!kTB) {
         // B: BN consecutive threads copy one BN-float row segment.
         constexpr int kRowsPerPass = kSgemmThreads / BN;
         const int nb = tid % BN;
@@ -323,6 +333,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     // A wait gave up: record it, let this CTA's own copies land, and leave
     // without writing C.
     if (tid == 0) raise_fault(p.fault, kFaultSgemmFullWait);
+    if constexpr (kAnyCp) cp_async_wait_all();
     if constexpr (kTma) {
       if (tid == 0) {
         const int issued = (kt + S < nk) ? kt + S : nk;
@@ -334,8 +345,6 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           }
         }
       }
-    } else {
-      cp_async_wait_all();
     }
     __syncthreads();
     return;

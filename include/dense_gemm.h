@@ -188,7 +188,9 @@ typedef enum gemm_op_t { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
  *    MN-major and a transposed B a K-major tcgen05 operand); the 16-byte
  *    alignment rule applies to lda and ldb in either storage.
  *  - FP32: a transposed operand is staged with 4-byte cp.async (TMA cannot
- *    transpose 4-byte elements), any alignment accepted.
+ *    transpose 4-byte elements), any alignment accepted; with exactly one
+ *    operand transposed the other is staged by TMA when its base and
+ *    leading dimension are 16-byte aligned (GEMM_PATH_SIMT_MIXED).
  *  - An op other than GEMM_OP_N / GEMM_OP_T is GEMM_ERR_INVALID_ARG.
  */
 gemm_status_t gemm_f32_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
@@ -230,7 +232,9 @@ enum {
   GEMM_PATH_ZERO_FILL = 1,     /* K == 0 or alpha == 0: C := beta*C  */
   GEMM_PATH_SIMT_TMA = 2,      /* FP32 SIMT, TMA-staged tiles        */
   GEMM_PATH_SIMT_CPASYNC = 3,  /* FP32 SIMT, 4-byte cp.async tiles   */
-  GEMM_PATH_TC_TMA = 4         /* FP16/BF16 tcgen05, TMA in and out  */
+  GEMM_PATH_TC_TMA = 4,        /* FP16/BF16 tcgen05, TMA in and out  */
+  GEMM_PATH_SIMT_MIXED = 5     /* FP32 SIMT, one operand stored transposed
+                                  (cp.async), the other by TMA         */
 };
 typedef struct gemm_plan_t {
   int path;

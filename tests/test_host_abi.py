@@ -410,10 +410,14 @@ def test_op_plans_and_validation():
     assert dg.load().gemm_plan_op(0, 2, 0, M, N, K, 1.0, FAKE, K, FAKE + (1 << 24), N, 0.0,
                                   FAKE + (1 << 26), N, 152, ctypes.byref(dg.Plan())) \
         == dg.GEMM_ERR_INVALID_ARG
-    # FP32: a transposed operand is staged by cp.async even when aligned
+    # FP32: a transposed operand is staged by cp.async; the other one by TMA
+    # when it is 16-byte aligned (mixed), else by cp.async too
     assert plan("f32", "N", "N", 104, 200)[1].path == dg.PATH_SIMT_TMA
-    assert plan("f32", "T", "N", 304, 200)[1].path == dg.PATH_SIMT_CPASYNC
-    assert plan("f32", "N", "T", 104, 104)[1].path == dg.PATH_SIMT_CPASYNC
+    assert plan("f32", "T", "N", 304, 200)[1].path == dg.PATH_SIMT_MIXED
+    assert plan("f32", "N", "T", 104, 104)[1].path == dg.PATH_SIMT_MIXED
+    assert plan("f32", "T", "N", 304, 201)[1].path == dg.PATH_SIMT_CPASYNC
+    assert plan("f32", "N", "T", 101, 104)[1].path == dg.PATH_SIMT_CPASYNC
+    assert plan("f32", "T", "T", 304, 104)[1].path == dg.PATH_SIMT_CPASYNC
     # FP16/BF16: TMA either way; the stored row must be 16-byte aligned
     for dt in ("f16", "bf16"):
         st, p = plan(dt, "T", "T", 304, 104)
