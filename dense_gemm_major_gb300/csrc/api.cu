@@ -305,21 +305,26 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     plan->threads = dgemm::kSgemmThreads;
     plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
     plan->smem_bytes = dgemm::sgemm_smem_bytes(tn);
-    // Wave quantisation: the tiles of a last partial wave (or of a grid that
-    // is a single partial wave) are split into two k-halves when twice their
-    // number still fits in one wave of CTA slots.
+    // Wave quantisation: with more tiles than resident CTAs the grid is
+    // one CTA per slot and each takes an equal share of the (tile, k-tile)
+    // iteration space (stream-K); a range boundary inside a tile cuts it
+    // into two pieces.  With beta == 0 the pieces add into zeroed C; with
+    // beta != 0 they store FP32 partials to a workspace (two tiles per
+    // boundary) that a fixup kernel combines.
     const int slots = (tn == 8 && forced_sgemm_tn() != 9 ? 2 : 1) * sms;
-    const int rem = plan->tiles % slots;
     const int nk = ceil_div(K, dgemm::kSgemmBK);
-    // With beta == 0 the k-halves add into zeroed C; with beta != 0 they
-    // store FP32 partials to a workspace that a fixup kernel combines.
-    plan->split_tiles = (rem > 0 && 2 * rem <= slots && nk >= 2) ? rem : 0;
+    // (A single wave of at most half the slots runs as two CTAs per tile:
+    // grid = 2 tiles puts every boundary in the middle of a tile.)
+    const int grid = plan->tiles > slots        ? slots
+                     : (2 * plan->tiles <= slots && nk >= 2) ? 2 * plan->tiles
+                                                             : plan->tiles;
+    plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles, nk, grid);
     plan->split_pieces = plan->split_tiles ? 2 : 1;
     plan->splitk_slices = 1;
     if (plan->split_tiles && beta != 0.f)
       plan->workspace_bytes =
-          (long long)plan->split_tiles * 2 * dgemm::kSgemmBM * plan->block_n * 4;
-    plan->ctas = plan->tiles + plan->split_tiles;
+          (long long)(grid - 1) * 2 * dgemm::kSgemmBM * plan->block_n * 4;
+    plan->ctas = grid;
     return GEMM_OK;
   }
   // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
@@ -414,8 +419,8 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     const int tn = plan.block_n == dgemm::sgemm_bn(16) ? 16 : (forced_sgemm_tn() == 9 ? 9 : 8);
     p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
     p.tiles_n = ceil_div(N, plan.block_n);
-    p.full_tiles = plan.tiles - plan.split_tiles;
-    p.split_kt = ceil_div(K, dgemm::kSgemmBK) / 2;
+    p.grid = plan.ctas;
+    p.split_tiles = plan.split_tiles;
     p.slices = plan.splitk_slices;
     p.ws = nullptr;
     p.ldw = ((long long)N + 3) / 4 * 4;

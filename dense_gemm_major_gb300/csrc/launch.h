@@ -37,23 +37,26 @@ struct SgemmParams {
   float* C;
   long long ldc;
   int tiles_m, tiles_n;
-  // Tiles [0, full_tiles) are computed whole and stored.  Each tile t >=
-  // full_tiles is computed as two pieces (k-tiles [0, split_kt) and
-  // [split_kt, nk)) by consecutive CTAs.  With tail_ws == nullptr (only when
-  // beta = 0) both add alpha times their FP32 partial sums into C, which is
-  // zeroed first; with exactly two addends the result does not depend on
-  // their order.  Otherwise piece h of split tile j stores its partial sum
-  // at tail_ws + (2 * j + h) * BM * BN (row-major, leading dimension BN) and
-  // a fixup kernel writes alpha * (piece 0 + piece 1) + beta * C, in that
-  // order, so the result is again independent of scheduling.
-  int full_tiles;
-  int split_kt;
+  // Stream-K schedule (slices == 1): CTA c of grid G (G <= tiles or
+  // G = 2 tiles) computes
+  // the k-tiles [c * total / G, (c + 1) * total / G) of the (tile, k-tile)
+  // iteration space, total = tiles * nk, as one unit per tile it touches.
+  // split_tiles tiles are cut by a range boundary into two pieces.  With
+  // tail_ws == nullptr (only when beta = 0) both pieces add alpha times
+  // their FP32 partial sums into C, which is zeroed first; with exactly two
+  // addends the result does not depend on their order.  Otherwise the
+  // pieces of the tile cut by boundary c store their partial sums at
+  // tail_ws + (2 (c - 1) + piece) * BM * BN (row-major, leading dimension
+  // BN) and a fixup kernel writes alpha * (piece 0 + piece 1) + beta * C, in
+  // that order, so the result is again independent of scheduling.
+  int grid;
+  int split_tiles;
   float* tail_ws = nullptr;
   // Split-K mode (slices > 1): CTA u computes k-slice u % slices of tile
   // u / slices (k-tiles [s*nk/slices, (s+1)*nk/slices)) and stores its FP32
   // partial tile at ws + s * M * ldw (row-major, leading dimension ldw);
-  // splitk_reduce then sums the slices in slice order into C.  full_tiles
-  // and split_kt are unused in this mode.
+  // splitk_reduce then sums the slices in slice order into C.  grid and
+  // split_tiles are unused in this mode.
   int slices;
   float* ws;
   long long ldw;
@@ -81,8 +84,9 @@ __host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, in
 
 // tn: 8 (narrow) or 16 (wide).  use_tma: A and B are staged by TMA
 // (16-byte aligned bases and strides); otherwise by 4-byte cp.async with
-// zero fill.  When p.full_tiles < tiles, first zeroes C on the split tiles
-// (one extra launch).  Returns the launch error.
+// zero fill.  When p.split_tiles > 0, first zeroes C on the cut tiles
+// (tail_ws == nullptr) or afterwards combines their pieces (one extra launch
+// either way).  Returns the launch error.
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream);
 
@@ -97,6 +101,18 @@ cudaError_t launch_sgemm_op(const SgemmParams& p, int tn, bool use_tma, const CU
 // (which = 0), the B tile of a BN-wide configuration (which = 1) or the B
 // tile of a transposed B (which = 2); host copy of the device layout.
 int sgemm_smem_offset(int which, int bn, int r, int c);
+
+// Stream-K schedule of `tiles` tiles of nk k-tiles each on `grid` CTAs
+// (grid <= tiles, or grid = 2 tiles): returns the number of tiles a range
+// boundary c * tiles * nk / grid cuts (the kernel's rule).
+inline int sgemm_streamk_cuts(int tiles, int nk, int grid) {
+  if (grid <= 1 || nk <= 0) return 0;
+  const long long total = (long long)tiles * nk;
+  int cuts = 0;
+  for (int c = 1; c < grid; ++c)
+    if (((long long)c * total / grid) % nk != 0) ++cuts;
+  return cuts;
+}
 
 // ---------------------------------------------------------------- FP16/BF16 tcgen05
 

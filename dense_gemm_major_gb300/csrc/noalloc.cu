@@ -95,8 +95,8 @@ extern "C" gemm_status_t gemm_f32_noalloc(int M, int N, int K, const float* A, i
   p.ldc = ldc;
   p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
   p.tiles_n = ceil_div(N, dgemm::sgemm_bn(8));
-  p.full_tiles = plan.tiles;
-  p.split_kt = 0;
+  p.grid = plan.ctas;
+  p.split_tiles = 0;
   p.slices = plan.splitk_slices;
   p.ws = dev->scratch;
   p.ldw = ((long long)N + 3) / 4 * 4;

@@ -137,37 +137,6 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int lane = tid & 31;
   const int warp = tid >> 5;
 
-  // Work unit of this CTA: a whole tile; one of the two k-pieces of a split
-  // tile (consecutive CTAs) that add into C or store to the tail workspace;
-  // or, in split-K mode, one k-slice of a tile that is stored to the
-  // workspace.  (Where the result goes is decoded again in the epilogue, so
-  // that it holds no registers across the main loop.)
-  int tile, k_begin, k_end;
-  {
-    const int nk_all = (p.K + BK - 1) / BK;
-    const int b = blockIdx.x;
-    if (p.slices > 1) {
-      tile = b / p.slices;
-      const int sl = b - tile * p.slices;
-      k_begin = sl * nk_all / p.slices;
-      k_end = (sl + 1) * nk_all / p.slices;
-    } else if (b < p.full_tiles) {
-      tile = b;
-      k_begin = 0;
-      k_end = nk_all;
-    } else {
-      const int j = b - p.full_tiles;
-      tile = p.full_tiles + (j >> 1);
-      k_begin = (j & 1) ? p.split_kt : 0;
-      k_end = (j & 1) ? nk_all : p.split_kt;
-    }
-  }
-  int tm, tn;
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int m0 = tm * BM;
-  const int n0 = tn * BN;
-  const int nk = k_end - k_begin;   // k-tiles of this unit
-
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), kBarCount);
     s_abort = 0;
@@ -176,88 +145,6 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     if constexpr (!kCpB) tma_prefetch_desc(&tmB);
   }
   __syncthreads();
-
-  // Stage k-tile kt (counted from k_begin) into ring slot s.
-  auto issue = [&](int kt, int s) {
-    const int k0 = (k_begin + kt) * BK;
-    const uint32_t bar = smem_u32(&full[s]);
-    if constexpr (kTma) {
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar, (kCpA ? 0u : kAStageFloats * 4u) +
-                                       (kCpB ? 0u : (uint32_t)kBStageFloats * 4u));
-        if constexpr (!kCpA) tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
-        if constexpr (!kCpB) tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
-      }
-    }
-    if constexpr (kAnyCp) {
-      const uint32_t a_dst = smem_u32(sA + s * kAStageFloats);
-      if constexpr (!kCpA) {
-        // A comes by TMA.
-      } else if constexpr (!kTA) {
-        // A: a warp copies one 32-float row segment (k contiguous in memory).
-        const int ka = tid & 31;
-        const int gk = k0 + ka;
-#pragma unroll
-        for (int j = 0; j < BM / 8; ++j) {
-          const int m = (tid >> 5) + 8 * j;
-          const int gm = m0 + m;
-          const bool v = (gm < p.M) && (gk < p.K);
-          const float* src = v ? p.A + (long long)gm * p.lda + gk : p.A;
-          cp_async_4(a_dst + 4u * a_tile_offset(m, ka), src, v);
-        }
-      } else {
-        // A stored K x M (m contiguous): copy j of warp w covers m = 8 g + (lane
-        // mod 8), k = 4 q + lane / 8 with g = (16 w + j) / 8, q = (16 w + j) mod 8.
-#pragma unroll
-        for (int j = 0; j < BM * BK / (32 * 8); ++j) {
-          const int idx = (BM * BK / (32 * 8)) * warp + j;
-          const int m = 8 * (idx >> 3) + (lane & 7);
-          const int k = 4 * (idx & 7) + (lane >> 3);
-          const int gm = m0 + m;
-          const int gk = k0 + k;
-          const bool v = (gm < p.M) && (gk < p.K);
-          const float* src = v ? p.A + (long long)gk * p.lda + gm : p.A;
-          cp_async_4(a_dst + 4u * a_tile_offset(m, k), src, v);
-        }
-      }
-      const uint32_t b_dst = smem_u32(sB + s * kBStageFloats);
-      if constexpr (!kCpB) {
-        // B comes by TMA.
-      } else if constexpr (!kTB) {
-        // B: BN consecutive threads copy one BN-float row segment.
-        constexpr int kRowsPerPass = kSgemmThreads / BN;
-        const int nb = tid % BN;
-        const int gn = n0 + nb;
-#pragma unroll
-        for (int j = 0; j < BK / kRowsPerPass; ++j) {
-          const int k = tid / BN + kRowsPerPass * j;
-          const int gk2 = k0 + k;
-          const bool v = (gk2 < p.K) && (gn < p.N);
-          const float* src = v ? p.B + (long long)gk2 * p.ldb + gn : p.B;
-          cp_async_4(b_dst + 4u * b_tile_offset(BN, k, nb), src, v);
-        }
-      } else {
-        // B stored N x K (k contiguous): copy j of warp w covers n = 4 g +
-        // lane / 8, k = 4 (lane mod 8) + kk with g = (BN/32) w + j / 4 and
-        // kk = j mod 4; the four copies of one g read the same four rows.
-        constexpr int kPer = BN * BK / (32 * 8);   // copies per thread
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-          const int n = 4 * ((BN / 32) * warp + (j >> 2)) + (lane >> 3);
-          const int k = 4 * (lane & 7) + (j & 3);
-          const int gn = n0 + n;
-          const int gk = k0 + k;
-          const bool v = (gn < p.N) && (gk < p.K);
-          const float* src = v ? p.B + (long long)gn * p.ldb + gk : p.B;
-          cp_async_4(b_dst + 4u * bt_tile_offset(BN, k, n), src, v);
-        }
-      }
-      cp_async_mbar_arrive_noinc(bar);
-    }
-  };
-
-  const int pre = nk < S ? nk : S;
-  for (int kt = 0; kt < pre; ++kt) issue(kt, kt);
 
   // Thread -> output mapping.  Warp (warp_m, warp_n) owns a 32 x (BN/2)
   // block; lane (tr, tc) owns rows tr + 4i (i < 8) and columns
@@ -273,98 +160,224 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int a_row0 = warp_m * 32 + tr;            // row for i = 0
   const int b_col0 = warp_n * (BN / 2) + tc * 4;
 
-  // acc[i][j] holds columns (2j, 2j+1) of row i as a packed float pair.
-  unsigned long long acc[8][TN / 2];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
-
-  int kt = 0;
-  for (; kt < nk; ++kt) {
-    const int s = kt % S;
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((kt / S) & 1), p.timeout_ns,
-                                      &s_abort);
-    if (!ok) {
-      s_abort = 1;
+  // Work of this CTA.  Split-K mode (slices > 1): one unit, k-slice
+  // b % slices of tile b / slices.  Otherwise the k-tiles
+  // [b * total / G, (b + 1) * total / G) of the (tile, k-tile) iteration
+  // space in tile-major order (total = tiles * nk_all, G = gridDim.x),
+  // as one unit per tile they touch (stream-K).  The host keeps
+  // G <= tiles, so each range covers at least one tile's worth of k-tiles,
+  // or G = 2 tiles, so each range is half a tile: either way a tile is cut
+  // into at most two pieces.  The ring's slot and phase
+  // follow the k-tiles this CTA has consumed over all its units (g0 + kt).
+  const int nk_all = (p.K + BK - 1) / BK;
+  const int b = blockIdx.x;
+  long long it, it_end;
+  if (p.slices > 1) {
+    it = 0;
+    it_end = 1;
+  } else {
+    const long long total = (long long)p.tiles_m * p.tiles_n * nk_all;
+    it = (long long)b * total / gridDim.x;
+    it_end = (long long)(b + 1) * total / gridDim.x;
+  }
+  int g0 = 0;
+  while (it < it_end) {
+    int tile, k_begin, k_end;
+    if (p.slices > 1) {
+      tile = b / p.slices;
+      const int sl = b - tile * p.slices;
+      k_begin = sl * nk_all / p.slices;
+      k_end = (sl + 1) * nk_all / p.slices;
+      it = it_end;
     } else {
-      const float* As = sA + s * kAStageFloats + a_row0 * BK;
-      // (A transposed-B tile has the thread's column chunk tc XOR-ed with kq.)
-      const float* Bs = sB + s * kBStageFloats + (kTB ? b_col0 - 4 * tc : b_col0);
-      // Row (a_row0 + 4i) mod 8 = tr + 4 (i mod 2), so k-quad kq of the
-      // thread's even rows sits in chunk kq ^ tr, of its odd rows in chunk
-      // kq ^ tr ^ 4.  Four base pointers cover (kq mod 4) ^ tr.
-      const float* a_base[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) a_base[q] = As + (((q ^ tr) & 3) << 2);
-#pragma unroll
-      for (int kq = 0; kq < BK / 4; ++kq) {
-        // A fragment: four k-steps of each of the thread's 8 rows.
-        float4 a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a[i] = *reinterpret_cast<const float4*>(a_base[kq & 3] + 4 * i * BK +
-                                                  (((kq & 4) ^ ((i & 1) << 2)) << 2));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float* brow = Bs + (kq * 4 + kk) * BN + (kTB ? ((tc ^ kq) << 2) : 0);
-          ulonglong2 b[NH];
-#pragma unroll
-          for (int h = 0; h < NH; ++h) b[h] = lds128_pairs(brow + 32 * h);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float av = (&a[i].x)[kk];
-            const unsigned long long aa = pack_pair(av, av);
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-              ffma2(acc[i][2 * h + 0], aa, b[h].x);
-              ffma2(acc[i][2 * h + 1], aa, b[h].y);
+      tile = (int)(it / nk_all);
+      k_begin = (int)(it - (long long)tile * nk_all);
+      const long long left = it_end - it;
+      k_end = left < nk_all - k_begin ? k_begin + (int)left : nk_all;
+      it += k_end - k_begin;
+    }
+    int tm, tn;
+    grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
+    const int m0 = tm * BM;
+    const int n0 = tn * BN;
+    const int nk = k_end - k_begin;   // k-tiles of this unit
+
+    // Stage k-tile kt (counted from k_begin) into ring slot s.
+    auto issue = [&](int kt, int s) {
+      const int k0 = (k_begin + kt) * BK;
+      const uint32_t bar = smem_u32(&full[s]);
+      if constexpr (kTma) {
+        if (tid == 0) {
+          mbar_arrive_expect_tx(bar, (kCpA ? 0u : kAStageFloats * 4u) +
+                                         (kCpB ? 0u : (uint32_t)kBStageFloats * 4u));
+          if constexpr (!kCpA) tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
+          if constexpr (!kCpB) tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
+        }
+      }
+      if constexpr (kAnyCp) {
+        const uint32_t a_dst = smem_u32(sA + s * kAStageFloats);
+        if constexpr (!kCpA) {
+          // A comes by TMA.
+        } else if constexpr (!kTA) {
+          // A: a warp copies one 32-float row segment (k contiguous in memory).
+          const int ka = tid & 31;
+          const int gk = k0 + ka;
+  #pragma unroll
+          for (int j = 0; j < BM / 8; ++j) {
+            const int m = (tid >> 5) + 8 * j;
+            const int gm = m0 + m;
+            const bool v = (gm < p.M) && (gk < p.K);
+            const float* src = v ? p.A + (long long)gm * p.lda + gk : p.A;
+            cp_async_4(a_dst + 4u * a_tile_offset(m, ka), src, v);
+          }
+        } else {
+          // A stored K x M (m contiguous): copy j of warp w covers m = 8 g + (lane
+          // mod 8), k = 4 q + lane / 8 with g = (16 w + j) / 8, q = (16 w + j) mod 8.
+  #pragma unroll
+          for (int j = 0; j < BM * BK / (32 * 8); ++j) {
+            const int idx = (BM * BK / (32 * 8)) * warp + j;
+            const int m = 8 * (idx >> 3) + (lane & 7);
+            const int k = 4 * (idx & 7) + (lane >> 3);
+            const int gm = m0 + m;
+            const int gk = k0 + k;
+            const bool v = (gm < p.M) && (gk < p.K);
+            const float* src = v ? p.A + (long long)gk * p.lda + gm : p.A;
+            cp_async_4(a_dst + 4u * a_tile_offset(m, k), src, v);
+          }
+        }
+        const uint32_t b_dst = smem_u32(sB + s * kBStageFloats);
+        if constexpr (!kCpB) {
+          // B comes by TMA.
+        } else if constexpr (!kTB) {
+          // B: BN consecutive threads copy one BN-float row segment.
+          constexpr int kRowsPerPass = kSgemmThreads / BN;
+          const int nb = tid % BN;
+          const int gn = n0 + nb;
+  #pragma unroll
+          for (int j = 0; j < BK / kRowsPerPass; ++j) {
+            const int k = tid / BN + kRowsPerPass * j;
+            const int gk2 = k0 + k;
+            const bool v = (gk2 < p.K) && (gn < p.N);
+            const float* src = v ? p.B + (long long)gk2 * p.ldb + gn : p.B;
+            cp_async_4(b_dst + 4u * b_tile_offset(BN, k, nb), src, v);
+          }
+        } else {
+          // B stored N x K (k contiguous): copy j of warp w covers n = 4 g +
+          // lane / 8, k = 4 (lane mod 8) + kk with g = (BN/32) w + j / 4 and
+          // kk = j mod 4; the four copies of one g read the same four rows.
+          constexpr int kPer = BN * BK / (32 * 8);   // copies per thread
+  #pragma unroll
+          for (int j = 0; j < kPer; ++j) {
+            const int n = 4 * ((BN / 32) * warp + (j >> 2)) + (lane >> 3);
+            const int k = 4 * (lane & 7) + (j & 3);
+            const int gn = n0 + n;
+            const int gk = k0 + k;
+            const bool v = (gn < p.N) && (gk < p.K);
+            const float* src = v ? p.B + (long long)gn * p.ldb + gk : p.B;
+            cp_async_4(b_dst + 4u * bt_tile_offset(BN, k, n), src, v);
+          }
+        }
+        cp_async_mbar_arrive_noinc(bar);
+      }
+    };
+
+    const int pre = nk < S ? nk : S;
+    for (int kt = 0; kt < pre; ++kt) issue(kt, (g0 + kt) % S);
+
+    // acc[i][j] holds columns (2j, 2j+1) of row i as a packed float pair.
+    unsigned long long acc[8][TN / 2];
+  #pragma unroll
+    for (int i = 0; i < 8; ++i)
+  #pragma unroll
+      for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
+
+    int kt = 0;
+    for (; kt < nk; ++kt) {
+      const int s = (g0 + kt) % S;
+      const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)(((g0 + kt) / S) & 1),
+                                        p.timeout_ns, &s_abort);
+      if (!ok) {
+        s_abort = 1;
+      } else {
+        const float* As = sA + s * kAStageFloats + a_row0 * BK;
+        // (A transposed-B tile has the thread's column chunk tc XOR-ed with kq.)
+        const float* Bs = sB + s * kBStageFloats + (kTB ? b_col0 - 4 * tc : b_col0);
+        // Row (a_row0 + 4i) mod 8 = tr + 4 (i mod 2), so k-quad kq of the
+        // thread's even rows sits in chunk kq ^ tr, of its odd rows in chunk
+        // kq ^ tr ^ 4.  Four base pointers cover (kq mod 4) ^ tr.
+        const float* a_base[4];
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) a_base[q] = As + (((q ^ tr) & 3) << 2);
+  #pragma unroll
+        for (int kq = 0; kq < BK / 4; ++kq) {
+          // A fragment: four k-steps of each of the thread's 8 rows.
+          float4 a[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i)
+            a[i] = *reinterpret_cast<const float4*>(a_base[kq & 3] + 4 * i * BK +
+                                                    (((kq & 4) ^ ((i & 1) << 2)) << 2));
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float* brow = Bs + (kq * 4 + kk) * BN + (kTB ? ((tc ^ kq) << 2) : 0);
+            ulonglong2 b[NH];
+  #pragma unroll
+            for (int h = 0; h < NH; ++h) b[h] = lds128_pairs(brow + 32 * h);
+  #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float av = (&a[i].x)[kk];
+              const unsigned long long aa = pack_pair(av, av);
+  #pragma unroll
+              for (int h = 0; h < NH; ++h) {
+                ffma2(acc[i][2 * h + 0], aa, b[h].x);
+                ffma2(acc[i][2 * h + 1], aa, b[h].y);
+              }
             }
           }
         }
       }
+      // Every thread is done with slot s (or some thread gave up).
+      if (__syncthreads_or(!ok)) break;
+      if (kt + S < nk) issue(kt + S, s);
     }
-    // Every thread is done with slot s (or some thread gave up).
-    if (__syncthreads_or(!ok)) break;
-    if (kt + S < nk) issue(kt + S, s);
-  }
 
-  if (kt < nk) {
-    // A wait gave up: record it, let this CTA's own copies land, and leave
-    // without writing C.
-    if (tid == 0) raise_fault(p.fault, kFaultSgemmFullWait);
-    if constexpr (kAnyCp) cp_async_wait_all();
-    if constexpr (kTma) {
-      if (tid == 0) {
-        const int issued = (kt + S < nk) ? kt + S : nk;
-        for (int t = kt; t < issued; ++t) {
-          if (!mbar_wait_bounded(smem_u32(&full[t % S]), (uint32_t)((t / S) & 1), p.timeout_ns,
-                                 nullptr)) {
-            raise_fault(p.fault, kFaultDrainWait);
-            break;
+    if (kt < nk) {
+      // A wait gave up: record it, let this CTA's own copies land, and leave
+      // without writing C.
+      if (tid == 0) raise_fault(p.fault, kFaultSgemmFullWait);
+      if constexpr (kAnyCp) cp_async_wait_all();
+      if constexpr (kTma) {
+        if (tid == 0) {
+          const int issued = (kt + S < nk) ? kt + S : nk;
+          for (int t = kt; t < issued; ++t) {
+            if (!mbar_wait_bounded(smem_u32(&full[(g0 + t) % S]), (uint32_t)(((g0 + t) / S) & 1),
+                                   p.timeout_ns, nullptr)) {
+              raise_fault(p.fault, kFaultDrainWait);
+              break;
+            }
           }
         }
       }
+      __syncthreads();
+      return;
     }
-    __syncthreads();
-    return;
-  }
 
-  // Destination: unscaled FP32 partial sums go to
-  // part[(gm - part_m0) * part_ld + gn - part_n0]; add_into_c pieces add
-  // into C; everything else is stored to C.
-  float* part = nullptr;
-  long long part_ld = 0;
-  int part_m0 = 0, part_n0 = 0;
-  bool add_into_c = false;
-  {
-    const int b = blockIdx.x;
+    // Destination: unscaled FP32 partial sums go to
+    // part[(gm - part_m0) * part_ld + gn - part_n0]; add_into_c pieces add
+    // into C; everything else is stored to C.
+    float* part = nullptr;
+    long long part_ld = 0;
+    int part_m0 = 0, part_n0 = 0;
+    bool add_into_c = false;
     if (p.slices > 1) {
       part = p.ws + (long long)(b % p.slices) * p.M * p.ldw;
       part_ld = p.ldw;
-    } else if (b >= p.full_tiles) {
+    } else if (k_begin != 0 || k_end != nk_all) {
+      // One of the two pieces of a tile cut by boundary cb (the first k-tile
+      // of CTA cb): piece 0 ends this CTA's range, piece 1 starts it.
       if (p.tail_ws != nullptr) {
-        part = p.tail_ws + (long long)(b - p.full_tiles) * (BM * BN);
+        const int piece = k_begin == 0 ? 0 : 1;
+        const int cb = piece == 0 ? b + 1 : b;
+        part = p.tail_ws + ((long long)(cb - 1) * 2 + piece) * (BM * BN);
         part_ld = BN;
         part_m0 = m0;
         part_n0 = n0;
@@ -372,100 +385,115 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
         add_into_c = true;
       }
     }
-  }
 
-  // Scaling pass, C := alpha * (A.B) + beta * C, applied to the
-  // accumulators in place before any store (partial sums for a workspace
-  // stay unscaled).  The old C of one row (TN values) is loaded at once so
-  // that those loads overlap instead of each waiting behind a store.
-  if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
-    const bool vec4c = p.c_vec4 != 0;
-#pragma unroll
+    // Scaling pass, C := alpha * (A.B) + beta * C, applied to the
+    // accumulators in place before any store (partial sums for a workspace
+    // stay unscaled).  The old C of one row (TN values) is loaded at once so
+    // that those loads overlap instead of each waiting behind a store.
+    if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
+      const bool vec4c = p.c_vec4 != 0;
+  #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + a_row0 + 4 * i;
+        const float* crow = p.C + (long long)gm * p.ldc;
+        float4 old[NH];
+  #pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int gn = n0 + b_col0 + 32 * h;
+          float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (p.beta != 0.f && gm < p.M) {
+            if (vec4c && gn + 3 < p.N) {
+              c = *reinterpret_cast<const float4*>(crow + gn);
+            } else {
+              if (gn + 0 < p.N) c.x = crow[gn + 0];
+              if (gn + 1 < p.N) c.y = crow[gn + 1];
+              if (gn + 2 < p.N) c.z = crow[gn + 2];
+              if (gn + 3 < p.N) c.w = crow[gn + 3];
+            }
+          }
+          old[h] = c;
+        }
+  #pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+          const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+          // (A column past N got c = 0 and is never stored.)
+          const auto upd = [&](float v, float cv) {
+            return p.beta != 0.f ? fmaf(p.beta, cv, p.alpha * v) : p.alpha * v;
+          };
+          acc[i][2 * h + 0] = pack_pair(upd(lo.x, old[h].x), upd(lo.y, old[h].y));
+          acc[i][2 * h + 1] = pack_pair(upd(hi.x, old[h].z), upd(hi.y, old[h].w));
+        }
+      }
+    }
+
+    // Epilogue: each store instruction of a warp covers four full 128-byte row
+    // segments of C.
+  #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int gm = m0 + a_row0 + 4 * i;
-      const float* crow = p.C + (long long)gm * p.ldc;
-      float4 old[NH];
-#pragma unroll
+      if (gm >= p.M) continue;
+      // Column gn of this row is crow[gn - cshift].
+      float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
+                                    : p.C + (long long)gm * p.ldc;
+      const int cshift = part_n0;
+      const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
+  #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const int gn = n0 + b_col0 + 32 * h;
-        float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.beta != 0.f && gm < p.M) {
-          if (vec4c && gn + 3 < p.N) {
-            c = *reinterpret_cast<const float4*>(crow + gn);
-          } else {
-            if (gn + 0 < p.N) c.x = crow[gn + 0];
-            if (gn + 1 < p.N) c.y = crow[gn + 1];
-            if (gn + 2 < p.N) c.z = crow[gn + 2];
-            if (gn + 3 < p.N) c.w = crow[gn + 3];
-          }
-        }
-        old[h] = c;
-      }
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
         const float2 lo = unpack_pair(acc[i][2 * h + 0]);
         const float2 hi = unpack_pair(acc[i][2 * h + 1]);
-        // (A column past N got c = 0 and is never stored.)
-        const auto upd = [&](float v, float cv) {
-          return p.beta != 0.f ? fmaf(p.beta, cv, p.alpha * v) : p.alpha * v;
-        };
-        acc[i][2 * h + 0] = pack_pair(upd(lo.x, old[h].x), upd(lo.y, old[h].y));
-        acc[i][2 * h + 1] = pack_pair(upd(hi.x, old[h].z), upd(hi.y, old[h].w));
-      }
-    }
-  }
-
-  // Epilogue: each store instruction of a warp covers four full 128-byte row
-  // segments of C.
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + a_row0 + 4 * i;
-    if (gm >= p.M) continue;
-    // Column gn of this row is crow[gn - cshift].
-    float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
-                                  : p.C + (long long)gm * p.ldc;
-    const int cshift = part_n0;
-    const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const int gn = n0 + b_col0 + 32 * h;
-      const float2 lo = unpack_pair(acc[i][2 * h + 0]);
-      const float2 hi = unpack_pair(acc[i][2 * h + 1]);
-      const float v0 = lo.x, v1 = lo.y, v2 = hi.x, v3 = hi.y;
-      if (add_into_c) {
-        if (vec4 && gn + 3 < p.N) {
-          atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
+        const float v0 = lo.x, v1 = lo.y, v2 = hi.x, v3 = hi.y;
+        if (add_into_c) {
+          if (vec4 && gn + 3 < p.N) {
+            atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
+          } else {
+            if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
+            if (gn + 1 < p.N) atomicAdd(crow + gn + 1, v1);
+            if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
+            if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
+          }
+        } else if (vec4 && gn + 3 < p.N) {
+          *reinterpret_cast<float4*>(crow + gn - cshift) = make_float4(v0, v1, v2, v3);
         } else {
-          if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
-          if (gn + 1 < p.N) atomicAdd(crow + gn + 1, v1);
-          if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
-          if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
+          if (gn + 0 < p.N) crow[gn + 0 - cshift] = v0;
+          if (gn + 1 < p.N) crow[gn + 1 - cshift] = v1;
+          if (gn + 2 < p.N) crow[gn + 2 - cshift] = v2;
+          if (gn + 3 < p.N) crow[gn + 3 - cshift] = v3;
         }
-      } else if (vec4 && gn + 3 < p.N) {
-        *reinterpret_cast<float4*>(crow + gn - cshift) = make_float4(v0, v1, v2, v3);
-      } else {
-        if (gn + 0 < p.N) crow[gn + 0 - cshift] = v0;
-        if (gn + 1 < p.N) crow[gn + 1 - cshift] = v1;
-        if (gn + 2 < p.N) crow[gn + 2 - cshift] = v2;
-        if (gn + 3 < p.N) crow[gn + 3 - cshift] = v3;
       }
     }
+    g0 += nk;
   }
 }
 
-// Writes C := alpha * (piece 0 + piece 1) + beta * C on the split tiles
-// [full_tiles, tiles_m * tiles_n) from their two partial sums in tail_ws.
-// Block (j, y) takes 2048 consecutive elements (2048 / bn rows) of split tile
-// j, 8 per thread at a stride of 256; every thread issues all its loads
-// before its first store, so the loads overlap.
+// Boundary c (0 < c < G) of the stream-K split is the first k-tile of CTA c,
+// c * total / G.  When it is not a multiple of nk it cuts tile
+// boundary / nk into two pieces: CTA c-1's last unit and CTA c's first.
+// Returns that tile, or -1.  The host counts the same boundaries.
+__device__ __forceinline__ int cut_tile(const SgemmParams& p, int c, int G) {
+  const int nk = (p.K + BK - 1) / BK;
+  const long long total = (long long)p.tiles_m * p.tiles_n * nk;
+  const long long bnd = (long long)c * total / G;
+  return bnd % nk != 0 ? (int)(bnd / nk) : -1;
+}
+
+// Writes C := alpha * (piece 0 + piece 1) + beta * C on the tile cut by
+// boundary c = blockIdx.x + 1 from its two partial sums in tail_ws (slots
+// 2 (c - 1) and 2 (c - 1) + 1).  Block (c - 1, y) takes 2048 consecutive
+// elements (2048 / bn rows) of that tile, 8 per thread at a stride of 256;
+// every thread issues all its loads before its first store, so the loads
+// overlap.
 constexpr int kFixupElems = 2048;
-__global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int bn) {
-  const int j = (int)blockIdx.x;
+__global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int bn, int G) {
+  const int c = (int)blockIdx.x + 1;
+  const int tile = cut_tile(p, c, G);
+  if (tile < 0) return;
   int tm, tn;
-  grouped_tile(p.full_tiles + j, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
+  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
   const int rows = min(BM, p.M - tm * BM);
   const int cols = min(bn, p.N - tn * bn);
-  const float* __restrict__ p0 = p.tail_ws + (long long)(2 * j) * (BM * bn);
+  const float* __restrict__ p0 = p.tail_ws + (long long)(2 * (c - 1)) * (BM * bn);
   const float* __restrict__ p1 = p0 + BM * bn;
   float* __restrict__ c0 = p.C + (long long)(tm * BM) * p.ldc + tn * bn;
   const int first = (int)blockIdx.y * kFixupElems;
@@ -475,31 +503,34 @@ __global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int
   for (int q = 0; q < kPer; ++q) {
     const int idx = first + (int)threadIdx.x + 256 * q;
     const int r = idx / bn;
-    const int c = idx - r * bn;
+    const int cc = idx - r * bn;
     v[q] = 0.f;
     old[q] = 0.f;
-    if (r < rows && c < cols) {
+    if (r < rows && cc < cols) {
       v[q] = p0[idx] + p1[idx];
-      if (p.beta != 0.f) old[q] = c0[(long long)r * p.ldc + c];
+      if (p.beta != 0.f) old[q] = c0[(long long)r * p.ldc + cc];
     }
   }
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int idx = first + (int)threadIdx.x + 256 * q;
     const int r = idx / bn;
-    const int c = idx - r * bn;
-    if (r < rows && c < cols) {
+    const int cc = idx - r * bn;
+    if (r < rows && cc < cols) {
       const float a = p.alpha * v[q];
-      c0[(long long)r * p.ldc + c] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
+      c0[(long long)r * p.ldc + cc] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
     }
   }
 }
 
-// Zeroes C on the split tiles [full_tiles, tiles_m * tiles_n), one CTA per
-// tile, before their two k-pieces add into it.
-__global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn) {
+// Zeroes C on the tile cut by boundary blockIdx.x + 1 (if any) before its
+// two pieces add into it.
+__global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn,
+                                                              int G) {
+  const int tile = cut_tile(p, (int)blockIdx.x + 1, G);
+  if (tile < 0) return;
   int tm, tn;
-  grouped_tile(p.full_tiles + (int)blockIdx.x, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
+  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
   const int rows = min(BM, p.M - tm * BM);
   const int cols = min(bn, p.N - tn * bn);
   for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
@@ -519,19 +550,20 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
                                        sgemm_smem_bytes(TN));
   if (e != cudaSuccess) return e;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int split = p.slices > 1 ? 0 : tiles - p.full_tiles;
-  if (split > 0 && p.tail_ws == nullptr) {
-    sgemm_zero_split_tiles<<<split, 256, 0, stream>>>(p, sgemm_bn(TN));
+  // Stream-K: G = p.grid CTAs (<= tiles); p.split_tiles tiles are cut in two.
+  const int G = p.slices > 1 ? tiles * p.slices : p.grid;
+  const bool cuts = p.slices == 1 && p.split_tiles > 0;
+  if (cuts && p.tail_ws == nullptr) {
+    sgemm_zero_split_tiles<<<G - 1, 256, 0, stream>>>(p, sgemm_bn(TN), G);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)(p.slices > 1 ? tiles * p.slices : tiles + split));
   sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB>
-      <<<grid, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
+      <<<G, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
   e = cudaGetLastError();
-  if (e != cudaSuccess || split == 0 || p.tail_ws == nullptr) return e;
-  const dim3 fixup_grid((unsigned)split, (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
-  sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN));
+  if (e != cudaSuccess || !cuts || p.tail_ws == nullptr) return e;
+  const dim3 fixup_grid((unsigned)(G - 1), (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
+  sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN), G);
   return cudaGetLastError();
 }
 

@@ -82,22 +82,78 @@ def test_valid_call_without_a_gpu_fails_loudly():
     assert st == dg.GEMM_ERR_UNSUPPORTED_DEVICE
 
 
+def _streamk_cuts(tiles, nk, grid):
+    """Tiles that a boundary c * tiles * nk // grid (0 < c < grid) cuts."""
+    total = tiles * nk
+    return sum(1 for c in range(1, grid) if (c * total // grid) % nk)
+
+
+def _streamk_units(tiles, nk, grid):
+    """The SGEMM kernel's unit loop, per CTA: (tile, k_begin, k_end)."""
+    total = tiles * nk
+    out = []
+    for b in range(grid):
+        it, end = b * total // grid, (b + 1) * total // grid
+        units = []
+        while it < end:
+            t = it // nk
+            kb = it - t * nk
+            ke = min(nk, kb + (end - it))
+            units.append((t, kb, ke))
+            it += ke - kb
+        out.append(units)
+    return out
+
+
+@pytest.mark.parametrize("tiles,nk,slots", [(512, 128, 152), (2048, 256, 152), (252, 8, 152),
+                                            (153, 3, 152), (60, 5, 152), (1000, 1, 304),
+                                            (305, 17, 304), (7, 2, 152)])
+def test_streamk_schedule_covers_every_k_tile_once(tiles, nk, slots):
+    # The plan's grid rule, then the kernel's unit loop: every (tile, k-tile)
+    # is computed exactly once, no tile has more than two pieces, the cut
+    # count is what the plan reports, and the two pieces of a cut tile map
+    # to the two workspace slots of its boundary.
+    grid = slots if tiles > slots else (2 * tiles if (2 * tiles <= slots and nk >= 2) else tiles)
+    units = _streamk_units(tiles, nk, grid)
+    seen = {}
+    slots_used = {}
+    for b, us in enumerate(units):
+        for (t, kb, ke) in us:
+            for k in range(kb, ke):
+                assert (t, k) not in seen
+                seen[(t, k)] = b
+            if (kb, ke) != (0, nk):
+                piece = 0 if kb == 0 else 1
+                cb = b + 1 if piece == 0 else b
+                assert 1 <= cb < grid
+                slots_used.setdefault((t, cb), set()).add(piece)
+    assert len(seen) == tiles * nk
+    pieces = {}
+    for (t, k), b in seen.items():
+        pieces.setdefault(t, set()).add(b)
+    assert max(len(v) for v in pieces.values()) <= 2
+    assert all(v == {0, 1} for v in slots_used.values())
+    assert len(slots_used) == _streamk_cuts(tiles, nk, grid)
+    assert len({cb for (_, cb) in slots_used}) == len(slots_used)   # one tile per boundary
+
+
 def test_plan_paths():
     ok, p = dg.gemm_plan("f32", 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
                          FAKE + (2 << 30), 4096)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_TMA
-    # many tiles: the wide 128 x 256 configuration, one CTA per SM; the last
-    # partial wave (512 - 3 x 152 = 56 tiles) runs as 112 k-halves
+    # many tiles: the wide 128 x 256 configuration, one CTA per SM, 512
+    # tiles shared out stream-K over 152 CTAs (3.37 tiles each); the range
+    # boundaries that fall inside a tile cut it in two
     assert (p.block_m, p.block_n, p.block_k, p.stages) == (128, 256, 32, 4)
-    assert p.tiles == 32 * 16 and p.split_tiles == 56 and p.ctas == 512 + 56
-    # 8192^3: 2048 tiles = 13 x 152 + 72, 2 x 72 <= 152 -> split
+    assert p.tiles == 32 * 16 and p.ctas == 152
+    assert p.split_tiles == _streamk_cuts(512, 128, 152) == 144
     ok, p = dg.gemm_plan("f32", 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
                          FAKE + (2 << 30), 8192, num_sms=152)
-    assert p.split_tiles == 72
-    # a remainder larger than half a wave is not split (252 = 152 + 100)
+    assert p.ctas == 152 and p.split_tiles == _streamk_cuts(2048, 256, 152)
+    # 252 = 152 + 100 tiles: balanced the same way
     ok, p = dg.gemm_plan("f32", 128 * 21, 256 * 12, 256, FAKE, 256, FAKE + (1 << 30), 3072,
                          FAKE + (2 << 30), 3072, num_sms=152)
-    assert p.tiles == 252 and p.split_tiles == 0 and p.ctas == 252
+    assert p.tiles == 252 and p.ctas == 152 and p.split_tiles == _streamk_cuts(252, 8, 152)
     # a single k-tile cannot be split
     ok, p = dg.gemm_plan("f32", 1000, 1030, 32, FAKE, 32, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030, num_sms=152)
@@ -301,14 +357,14 @@ def test_scaled_plans():
     assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
     ok, p = dg.gemm_plan_ex("bf16", 64, 64, 0, 1.0, 0, 0, 0, 64, 0.5, FAKE, 64, 152)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
-    # The SGEMM's last partial wave is split into k-halves either way; with
-    # beta != 0 the halves go through a workspace of two FP32 tiles each
-    # (56 tiles x 2 x 128 x 256 x 4 bytes), with beta == 0 they add into C.
+    # The SGEMM's stream-K pieces either way; with beta != 0 they go through
+    # a workspace of two FP32 tiles per range boundary (151 x 2 x 128 x 256
+    # x 4 bytes), with beta == 0 they add into C.
     args = (4096, 4096, 4096, 1.0, FAKE, 4096, FAKE + (1 << 30), 4096)
     ok, p0 = dg.gemm_plan_ex("f32", *args, 0.0, FAKE + (2 << 30), 4096, 152)
     ok, p1 = dg.gemm_plan_ex("f32", *args, 0.5, FAKE + (2 << 30), 4096, 152)
-    assert p0.split_tiles == 56 and p1.split_tiles == 56 and p1.ctas == 512 + 56
-    assert p0.workspace_bytes == 0 and p1.workspace_bytes == 56 * 2 * 128 * 256 * 4
+    assert p0.split_tiles == 144 and p1.split_tiles == 144 and p1.ctas == 152
+    assert p0.workspace_bytes == 0 and p1.workspace_bytes == 151 * 2 * 128 * 256 * 4
     # FP16/BF16 plans do not depend on alpha and beta
     for dt in ("f16", "bf16"):
         ok, q0 = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
