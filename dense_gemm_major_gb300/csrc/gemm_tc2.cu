@@ -122,8 +122,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   extern __shared__ unsigned char smem_raw[];
-  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
-  unsigned char* sA = reinterpret_cast<unsigned char*>(base);
+  unsigned char* const base = align_smem_1024(smem_raw);
+  unsigned char* sA = base;
   unsigned char* sB = sA + S * kABytes;
   unsigned char* sEpi = sB + S * kBBytes;
   Barriers* bars = reinterpret_cast<Barriers*>(sEpi + kEpiWarps * 2 * kEpiBufBytes);

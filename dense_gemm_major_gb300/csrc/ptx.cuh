@@ -16,6 +16,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// `raw` (a __shared__ array) advanced to the next 1024-byte boundary of the
+// shared window.  The pointer is formed by indexing the array itself, so the
+// compiler keeps it in the shared address space and emits shared loads and
+// stores through it (a pointer rounded through an integer becomes generic:
+// on sm_103a a generic 16-byte load from shared memory was measured at 4
+// wavefronts where the same ld.shared takes 2).
+__device__ __forceinline__ unsigned char* align_smem_1024(unsigned char* raw) {
+  const uint32_t pad = (1024u - (smem_u32(raw) & 1023u)) & 1023u;
+  return raw + pad;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

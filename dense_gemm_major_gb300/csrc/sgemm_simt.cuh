@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ int s_abort;
-  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+  unsigned char* const base = align_smem_1024(smem_raw);
   float* sA = reinterpret_cast<float*>(base);
   float* sB = sA + S * kAStageFloats;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * kBStageFloats);
