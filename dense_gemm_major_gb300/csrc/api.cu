@@ -225,6 +225,43 @@ int forced_sgemm_tn() {
   return v;
 }
 
+// FP32 tile configuration of a grid that is not split-K: 16 = wide (8 x 16
+// per thread, one CTA per SM), 9 = narrow with one CTA per SM, 8 = narrow
+// with two.  Picks the largest (speed relative to wide) x (share of the CTA
+// slots busy): a grid of more tiles than slots is balanced by stream-K
+// (share 1), a smaller one fills tiles / slots (twice that when it runs as
+// two k-halves per tile).  Relative speeds measured on GB300 at 4096^3 and
+// 8192 x 8192 x 4096: wide 1.00, narrow/1 0.96, narrow/2 0.95.
+int sgemm_pick_tn(int M, int N, int K, int sms) {
+  if (const int forced = forced_sgemm_tn()) return forced;
+  const int nk = ceil_div(K, dgemm::kSgemmBK);
+  struct Cfg {
+    int tn, per_sm;
+    double speed;
+  };
+  const Cfg cfgs[3] = {{16, 1, 1.00}, {9, 1, 0.96}, {8, 2, 0.95}};
+  int best = 16;
+  double best_score = -1.0;
+  for (const Cfg& c : cfgs) {
+    const int bn = dgemm::sgemm_bn(c.tn == 9 ? 8 : c.tn);
+    const long long tiles = (long long)ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, bn);
+    const long long slots = (long long)c.per_sm * sms;
+    double share;
+    if (tiles > slots)
+      share = 1.0;
+    else if (2 * tiles <= slots && nk >= 2)
+      share = 2.0 * (double)tiles / (double)slots;
+    else
+      share = (double)tiles / (double)slots;
+    const double score = c.speed * share;
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = c.tn;
+    }
+  }
+  return best;
+}
+
 gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
                         const void* A, int lda, const void* B, int ldb, float beta, const void* C,
                         int ldc, int num_sms, gemm_plan_t* plan) {
@@ -271,11 +308,6 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
       plan->path = GEMM_PATH_SIMT_MIXED;
     else
       plan->path = GEMM_PATH_SIMT_CPASYNC;
-    // With the last partial wave split into k-halves, the wide tile (8 x 16
-    // per thread, one CTA per SM) is at least as fast as the narrow one (8 x 8,
-    // two CTAs per SM) once the narrow grid has more tiles than SMs (measured
-    // on GB300: 4096^3 53.9 vs 53.8, 8192^3 56.5 vs 56.0, 2048^3 46.0 vs 43.9
-    // TFLOP/s); smaller grids keep the narrow tile for parallelism.
     const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
     const int nk_all = ceil_div(K, dgemm::kSgemmBK);
     // A grid of narrow tiles that fills at most half of the CTA slots runs
@@ -296,29 +328,31 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
       plan->ctas = narrow_tiles * slices;
       return GEMM_OK;
     }
-    int tn = narrow_tiles > sms ? 16 : 8;
-    if (const int forced = forced_sgemm_tn()) tn = forced == 16 ? 16 : 8;
+    const int tn = sgemm_pick_tn(M, N, K, sms);
+    const int tcfg = tn == 9 ? 8 : tn;   // the tile shape of narrow/1 is narrow's
     plan->block_m = dgemm::kSgemmBM;
-    plan->block_n = dgemm::sgemm_bn(tn);
+    plan->block_n = dgemm::sgemm_bn(tcfg);
     plan->block_k = dgemm::kSgemmBK;
-    plan->stages = dgemm::sgemm_stages(tn);
+    plan->stages = dgemm::sgemm_stages(tcfg);
     plan->threads = dgemm::kSgemmThreads;
     plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
-    plan->smem_bytes = dgemm::sgemm_smem_bytes(tn);
+    plan->smem_bytes = dgemm::sgemm_smem_bytes(tcfg);
     // Wave quantisation: with more tiles than resident CTAs the grid is
-    // one CTA per slot and each takes an equal share of the (tile, k-tile)
-    // iteration space (stream-K); a range boundary inside a tile cuts it
-    // into two pieces.  With beta == 0 the pieces add into zeroed C; with
+    // one CTA per slot; all full waves but the last one or two run as whole
+    // tiles, and each CTA takes an equal share of the remaining tiles'
+    // (tile, k-tile) iteration space (hybrid stream-K); a range boundary
+    // inside a tile cuts it into two pieces.  With beta == 0 the pieces add into zeroed C; with
     // beta != 0 they store FP32 partials to a workspace (two tiles per
     // boundary) that a fixup kernel combines.
-    const int slots = (tn == 8 && forced_sgemm_tn() != 9 ? 2 : 1) * sms;
+    const int slots = (tn == 8 ? 2 : 1) * sms;
     const int nk = ceil_div(K, dgemm::kSgemmBK);
     // (A single wave of at most half the slots runs as two CTAs per tile:
     // grid = 2 tiles puts every boundary in the middle of a tile.)
     const int grid = plan->tiles > slots        ? slots
                      : (2 * plan->tiles <= slots && nk >= 2) ? 2 * plan->tiles
                                                              : plan->tiles;
-    plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles, nk, grid);
+    const int dp_tiles = dgemm::sgemm_dp_tiles(plan->tiles, grid);
+    plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles - dp_tiles, nk, grid);
     plan->split_pieces = plan->split_tiles ? 2 : 1;
     plan->splitk_slices = 1;
     if (plan->split_tiles && beta != 0.f)
@@ -416,10 +450,11 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.ldb = ldb;
     p.C = static_cast<float*>(C);
     p.ldc = ldc;
-    const int tn = plan.block_n == dgemm::sgemm_bn(16) ? 16 : (forced_sgemm_tn() == 9 ? 9 : 8);
+    const int tn = plan.splitk_slices > 1 ? 8 : sgemm_pick_tn(M, N, K, dev->sms);
     p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
     p.tiles_n = ceil_div(N, plan.block_n);
     p.grid = plan.ctas;
+    p.dp_tiles = plan.splitk_slices > 1 ? 0 : dgemm::sgemm_dp_tiles(plan.tiles, plan.ctas);
     p.split_tiles = plan.split_tiles;
     p.slices = plan.splitk_slices;
     p.ws = nullptr;

@@ -37,10 +37,11 @@ struct SgemmParams {
   float* C;
   long long ldc;
   int tiles_m, tiles_n;
-  // Stream-K schedule (slices == 1): CTA c of grid G (G <= tiles or
-  // G = 2 tiles) computes
-  // the k-tiles [c * total / G, (c + 1) * total / G) of the (tile, k-tile)
-  // iteration space, total = tiles * nk, as one unit per tile it touches.
+  // Hybrid stream-K schedule (slices == 1), grid G: CTA c computes the
+  // whole tiles c, c + G, ... below dp_tiles, then the k-tiles
+  // [c * total / G, (c + 1) * total / G) of the iteration space of the
+  // remaining tiles, total = (tiles - dp_tiles) * nk (G <= tiles - dp_tiles,
+  // or G = 2 tiles with dp_tiles = 0), one unit per tile it touches.
   // split_tiles tiles are cut by a range boundary into two pieces.  With
   // tail_ws == nullptr (only when beta = 0) both pieces add alpha times
   // their FP32 partial sums into C, which is zeroed first; with exactly two
@@ -50,6 +51,7 @@ struct SgemmParams {
   // BN) and a fixup kernel writes alpha * (piece 0 + piece 1) + beta * C, in
   // that order, so the result is again independent of scheduling.
   int grid;
+  int dp_tiles = 0;
   int split_tiles;
   float* tail_ws = nullptr;
   // Split-K mode (slices > 1): CTA u computes k-slice u % slices of tile
@@ -102,9 +104,16 @@ cudaError_t launch_sgemm_op(const SgemmParams& p, int tn, bool use_tma, const CU
 // tile of a transposed B (which = 2); host copy of the device layout.
 int sgemm_smem_offset(int which, int bn, int r, int c);
 
-// Stream-K schedule of `tiles` tiles of nk k-tiles each on `grid` CTAs
-// (grid <= tiles, or grid = 2 tiles): returns the number of tiles a range
-// boundary c * tiles * nk / grid cuts (the kernel's rule).
+// Whole tiles a hybrid stream-K schedule of `tiles` tiles on `grid` CTAs
+// computes in full waves before sharing out the rest: all waves but the
+// last one or two, so that at least `grid` tiles are left.
+inline int sgemm_dp_tiles(int tiles, int grid) {
+  return tiles / grid >= 2 ? (tiles / grid - 1) * grid : 0;
+}
+
+// Stream-K share of `tiles` tiles of nk k-tiles each on `grid` CTAs (grid <=
+// tiles, or grid = 2 tiles): returns the number of tiles a range boundary
+// c * tiles * nk / grid cuts (the kernel's rule).
 inline int sgemm_streamk_cuts(int tiles, int nk, int grid) {
   if (grid <= 1 || nk <= 0) return 0;
   const long long total = (long long)tiles * nk;

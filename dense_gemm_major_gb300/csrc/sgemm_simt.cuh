@@ -161,27 +161,31 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   const int b_col0 = warp_n * (BN / 2) + tc * 4;
 
   // Work of this CTA.  Split-K mode (slices > 1): one unit, k-slice
-  // b % slices of tile b / slices.  Otherwise the k-tiles
-  // [b * total / G, (b + 1) * total / G) of the (tile, k-tile) iteration
-  // space in tile-major order (total = tiles * nk_all, G = gridDim.x),
-  // as one unit per tile they touch (stream-K).  The host keeps
-  // G <= tiles, so each range covers at least one tile's worth of k-tiles,
-  // or G = 2 tiles, so each range is half a tile: either way a tile is cut
-  // into at most two pieces.  The ring's slot and phase
+  // b % slices of tile b / slices.  Otherwise (hybrid stream-K, G =
+  // gridDim.x): first whole tiles b, b + G, ... below dp_tiles (full waves in
+  // tile order, so the tiles in flight together are neighbours and share
+  // A and B in L2), then the k-tiles [b * total / G, (b + 1) * total / G) of
+  // the remaining tiles' (tile, k-tile) iteration space, total =
+  // (tiles - dp_tiles) * nk_all, as one unit per tile they touch.  The host
+  // keeps G <= tiles - dp_tiles, so each range covers at least one tile's
+  // worth of k-tiles, or G = 2 tiles, so each range is half a tile: either
+  // way a tile is cut into at most two pieces.  The ring's slot and phase
   // follow the k-tiles this CTA has consumed over all its units (g0 + kt).
   const int nk_all = (p.K + BK - 1) / BK;
   const int b = blockIdx.x;
+  int dp_next = b;
   long long it, it_end;
   if (p.slices > 1) {
+    dp_next = 0x7fffffff;
     it = 0;
     it_end = 1;
   } else {
-    const long long total = (long long)p.tiles_m * p.tiles_n * nk_all;
+    const long long total = (long long)(p.tiles_m * p.tiles_n - p.dp_tiles) * nk_all;
     it = (long long)b * total / gridDim.x;
     it_end = (long long)(b + 1) * total / gridDim.x;
   }
   int g0 = 0;
-  while (it < it_end) {
+  while (dp_next < p.dp_tiles || it < it_end) {
     int tile, k_begin, k_end;
     if (p.slices > 1) {
       tile = b / p.slices;
@@ -189,9 +193,15 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       k_begin = sl * nk_all / p.slices;
       k_end = (sl + 1) * nk_all / p.slices;
       it = it_end;
+    } else if (dp_next < p.dp_tiles) {
+      tile = dp_next;
+      k_begin = 0;
+      k_end = nk_all;
+      dp_next += gridDim.x;
     } else {
-      tile = (int)(it / nk_all);
-      k_begin = (int)(it - (long long)tile * nk_all);
+      const int t = (int)(it / nk_all);
+      tile = p.dp_tiles + t;
+      k_begin = (int)(it - (long long)t * nk_all);
       const long long left = it_end - it;
       k_end = left < nk_all - k_begin ? k_begin + (int)left : nk_all;
       it += k_end - k_begin;
@@ -467,15 +477,16 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   }
 }
 
-// Boundary c (0 < c < G) of the stream-K split is the first k-tile of CTA c,
-// c * total / G.  When it is not a multiple of nk it cuts tile
-// boundary / nk into two pieces: CTA c-1's last unit and CTA c's first.
-// Returns that tile, or -1.  The host counts the same boundaries.
+// Boundary c (0 < c < G) of the stream-K split is the first k-tile of CTA c
+// in the stream-K tiles' iteration space, c * total / G.  When it is not a
+// multiple of nk it cuts tile dp_tiles + boundary / nk into two pieces: CTA
+// c-1's last unit and CTA c's first.  Returns that tile, or -1.  The host
+// counts the same boundaries.
 __device__ __forceinline__ int cut_tile(const SgemmParams& p, int c, int G) {
   const int nk = (p.K + BK - 1) / BK;
-  const long long total = (long long)p.tiles_m * p.tiles_n * nk;
+  const long long total = (long long)(p.tiles_m * p.tiles_n - p.dp_tiles) * nk;
   const long long bnd = (long long)c * total / G;
-  return bnd % nk != 0 ? (int)(bnd / nk) : -1;
+  return bnd % nk != 0 ? p.dp_tiles + (int)(bnd / nk) : -1;
 }
 
 // Writes C := alpha * (piece 0 + piece 1) + beta * C on the tile cut by
