@@ -66,16 +66,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is
+// suspended in hardware until it completes or about `hint_ns` pass, instead
+// of returning at once: a waiting warp issues almost nothing while it waits.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if
 // `timeout_ns` elapses first, or if `*abort` becomes non-zero (another role
-// of the same CTA gave up).
+// of the same CTA gave up).  Each try suspends the thread for up to 10 us, so
+// the timeout and the abort flag are checked at least every few ms.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t timeout_ns,
                                                   const volatile int* abort) {
+  constexpr uint32_t kSuspendNs = 10000;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
     if ((it & 255u) == 0) {
       if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > timeout_ns) return false;
