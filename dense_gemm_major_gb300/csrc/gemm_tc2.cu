@@ -45,15 +45,25 @@ constexpr int BN = kTc2BN;            // columns per pair tile
 constexpr int BK = kTc2BK;
 constexpr int S = kTc2Stages;
 constexpr int UMMA_K = 16;
-constexpr uint32_t kABytes = BM * BK * 2;          // 16 KB
-constexpr uint32_t kBBoxBytes = 64 * BK * 2;       // one 64-column box: 8 KB
-constexpr uint32_t kBBytes = (BN / 2) * BK * 2;    // this CTA's half of B: 16 KB
+constexpr uint32_t kABytes = BM * BK * 2;          // 32 KB
+constexpr uint32_t kBBoxBytes = 64 * BK * 2;       // one 64-column block of B: 16 KB
+constexpr uint32_t kBBytes = (BN / 2) * BK * 2;    // this CTA's half of B: 32 KB
+// A stage holds BK / 64 k-blocks of 64: a K-major operand keeps each as its
+// own 128-byte-swizzled tile (rows x 128 bytes), kAKBlock / kBKBlock bytes
+// apart; an MN-major operand keeps BK rows of 128 bytes per 64-wide block,
+// kMNBlock bytes apart.  Every TMA box is 64 k deep (the tensor maps are the
+// single-CTA kernel's), so a stage takes BK / 64 boxes per block.
+constexpr int kKBlocks = BK / 64;
+constexpr uint32_t kAKBlock = BM * 128;            // 16 KB
+constexpr uint32_t kBKBlock = (BN / 2) * 128;      // 16 KB
+constexpr uint32_t kMNBlock = BK * 128;            // 16 KB
+constexpr uint32_t kBox64 = 64 * 128;              // one 64 x 64 box: 8 KB
 constexpr uint32_t kEpiBufBytes = 32 * kTcEpiCols * 2;
 constexpr int kAccBufs = kTc2AccBufs;              // accumulator buffers in TMEM
 constexpr uint32_t kTmemCols = kAccBufs * BN;
 constexpr int kEpiWarps = 4;
 
-static_assert(BK * 2 == 128, "A rows of a stage are one 128-byte swizzle row");
+static_assert(BK % 64 == 0, "a stage is whole 64-deep swizzle blocks");
 static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
 
 struct alignas(8) Barriers {
@@ -190,19 +200,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * (kABytes + boxes * kBBoxBytes));
           const uint32_t adst = smem_u32(sA + s * kABytes);
           const int m = w.tm * (2 * BM) + (int)rank * BM;
-          if constexpr (!kAT) {
-            tma_load_2d_pair(adst, &tmA, fb, kt * BK, m);
-          } else {   // A stored K x M: two 64-row (m) blocks, MN-major
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d_pair(adst + j * kBBoxBytes, &tmA, fb, m + j * 64, kt * BK);
+          for (int kb = 0; kb < kKBlocks; ++kb) {
+            const int k = kt * BK + kb * 64;
+            if constexpr (!kAT) {   // K-major: one 128-row box per k-block
+              tma_load_2d_pair(adst + kb * kAKBlock, &tmA, fb, k, m);
+            } else {   // A stored K x M: two 64-row (m) blocks, MN-major
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d_pair(adst + j * kMNBlock + kb * kBox64, &tmA, fb, m + j * 64, k);
+            }
           }
           const uint32_t bdst = smem_u32(sB + s * kBBytes);
           for (int j = 0; j < boxes; ++j) {
             const int n = w.tn * BN + w.n_off + (int)rank * half + j * 64;
-            if constexpr (!kBT)
-              tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb, n, kt * BK);
-            else   // B stored N x K: 64 rows (n) of 64 k each, K-major
-              tma_load_2d_pair(bdst + j * kBBoxBytes, &tmB, fb, kt * BK, n);
+            for (int kb = 0; kb < kKBlocks; ++kb) {
+              const int k = kt * BK + kb * 64;
+              if constexpr (!kBT)   // MN-major: 64-column blocks of BK rows
+                tma_load_2d_pair(bdst + j * kMNBlock + kb * kBox64, &tmB, fb, n, k);
+              else   // B stored N x K: 64 rows (n) of 64 k per box, K-major
+                tma_load_2d_pair(bdst + kb * kBKBlock + j * kBox64, &tmB, fb, k, n);
+            }
           }
           issued = it + 1;
         }
@@ -236,8 +252,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             const uint32_t b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint64_t ad = kAT ? mnmajor_desc(a0, k) : kmajor_desc(a0, k);
-              const uint64_t bd = kBT ? kmajor_desc(b0, k) : mnmajor_desc(b0, k);
+              const uint64_t ad = kAT ? mnmajor_desc(a0, k, kMNBlock)
+                                      : kmajor_desc(a0 + (k >> 2) * kAKBlock, k & 3);
+              const uint64_t bd = kBT ? kmajor_desc(b0 + (k >> 2) * kBKBlock, k & 3)
+                                      : mnmajor_desc(b0, k, kMNBlock);
               mma_f16_pair(d_tmem, ad, bd, idesc, (kt > 0 || k > 0) ? 1u : 0u);
             }
             // Both CTAs' stage s is free once these MMAs finish.

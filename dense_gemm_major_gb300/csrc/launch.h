@@ -199,12 +199,13 @@ cudaError_t launch_gemm_tc(int dtype, const TcParams& p, const CUtensorMap* tmA,
 // ---------------------------------------------------------------- FP16/BF16 CTA pairs
 
 // A cluster of two CTAs computes a 256 x 256 tile with tcgen05.mma.cta_group::2;
-// each CTA stages 128 rows of A and 128 columns of B per 64-deep k-tile in a
-// 6-stage ring.  Same 192-thread role layout as the single-CTA kernel.
+// each CTA stages 128 rows of A and 128 columns of B per 128-deep k-tile in a
+// 3-stage ring (eight MMAs per barrier round trip).  Same 192-thread role
+// layout as the single-CTA kernel.
 constexpr int kTc2BM = 128;              // rows per CTA
 constexpr int kTc2BN = 256;              // columns per pair tile
-constexpr int kTc2BK = 64;
-constexpr int kTc2Stages = 6;
+constexpr int kTc2BK = 128;
+constexpr int kTc2Stages = 3;
 constexpr int kTc2AccBufs = 2;           // accumulator buffers (256 TMEM columns each)
 constexpr int kTc2SmemBytes =
     kTc2Stages * (kTc2BM * kTc2BK + kTc2BK * (kTc2BN / 2)) * 2   // A and B-half ring

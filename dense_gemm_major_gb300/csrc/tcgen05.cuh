@@ -43,12 +43,14 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, uint32_t m, 
 // stage, 128-byte swizzled, 8-row groups 1024 bytes apart:
 //  * K-major (rows of 64 k, 128 bytes): +32 bytes per k-step;
 //  * MN-major (rows of 64 m or n, 128 bytes, one row per k; 64-wide blocks
-//    8 KB apart): +16 rows = 2048 bytes per k-step, leading offset 8 KB.
+//    block_bytes apart, 8 KB for a 64-deep stage): +16 rows = 2048 bytes per
+//    k-step, leading offset block_bytes.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k16) {
   return smem_desc(base + k16 * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k16) {
-  return smem_desc(base + k16 * 2048, 8192, 1024);
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k16,
+                                                 uint32_t block_bytes = 8192) {
+  return smem_desc(base + k16 * 2048, block_bytes, 1024);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

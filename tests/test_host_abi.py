@@ -206,7 +206,7 @@ def test_plan_paths():
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA
         # CTA pairs: 256 tiles of 256 x 256 = 3 x 76 + 28; the last 28 tiles
         # run as 2 column parts
-        assert (p.cluster_ctas, p.block_m, p.block_n, p.stages) == (2, 256, 256, 6)
+        assert (p.cluster_ctas, p.block_m, p.block_n, p.block_k, p.stages) == (2, 256, 256, 128, 3)
         assert p.tiles == 16 * 16 and p.ctas == 152
         assert (p.split_tiles, p.split_pieces) == (28, 2)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
