@@ -335,7 +335,7 @@ def run_e2e(dg, cases, dev, stream, args):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-KERNEL_SOURCES = {"f32": ("sgemm_simt.cu",),
+KERNEL_SOURCES = {"f32": ("sgemm_simt.cuh", "sgemm_simt.cu"),
                   "f16": ("gemm_tc.cu", "gemm_tc2.cu", "tcgen05.cuh"),
                   "bf16": ("gemm_tc.cu", "gemm_tc2.cu", "tcgen05.cuh")}
 
