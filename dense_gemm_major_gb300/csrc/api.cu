@@ -395,10 +395,16 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   plan->stages = dgemm::kTcStages;
   plan->tiles = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
   plan->smem_bytes = dgemm::kTcSmemBytes;
-  // A grid filling at most half of the SMs with a long K runs as split-K.
-  const int slices = tc_split_disabled() ? 1
-                                         : splitk_slices_capped(plan->tiles, sms,
-                                                                ceil_div(K, dgemm::kTcBK), M, N);
+  // A grid filling at most half of the SMs with a long K runs as split-K,
+  // unless splitting every tile into column parts (full K each) already
+  // fills three quarters of the SMs: that needs no workspace and no second
+  // launch (1024^3 FP16: 22.5 us with split-K; a launch alone costs ~4.5 us).
+  const dgemm::TcSplit parts_only = dgemm::tc_split(plan->tiles, sms);
+  const bool parts_fill = parts_only.split_tiles == plan->tiles &&
+                          4 * parts_only.parts * plan->tiles >= 3 * sms;
+  const int slices = (tc_split_disabled() || parts_fill)
+                         ? 1
+                         : splitk_slices_capped(plan->tiles, sms, ceil_div(K, dgemm::kTcBK), M, N);
   if (slices > 1) {
     plan->split_pieces = 1;
     plan->splitk_slices = slices;

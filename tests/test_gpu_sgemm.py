@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from parity import TOL, check_device, compare, gpu_lib, padded, run_gemm
 
@@ -134,31 +135,61 @@ def test_bounded_wait_self_test_reports_timeout(dg):
     _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)
 
 
-@pytest.mark.parametrize("shape", [(4096, 4096, 64), (2688, 3072, 96), (1000, 1030, 65),
-                                   (300, 260, 999)])
-def test_f32_split_tail_tiles(dg, shape):
-    # Grids whose last partial wave (or whole grid) is split into k-halves
-    # that add into C; C starts as NaN, so a tile the zeroing kernel or a
-    # piece misses shows up.
+# Hybrid stream-K schedules: whole-tile waves, then equal k-tile ranges per
+# CTA; a range boundary inside a tile cuts it into two pieces that add into
+# zeroed C (beta = 0) or meet in the tail workspace (beta != 0).  C starts as
+# NaN, so a tile the zeroing kernel or a piece misses shows up; integer
+# entries make every sum exact, so a k-range counted twice or skipped
+# breaks bit-exactness.
+STREAMK_SHAPES = [
+    (2176, 2304, 96),    # 153 wide tiles on 152 CTAs, 3 k-tiles each: a cut almost everywhere
+    (4096, 4096, 64),    # 512 tiles, 2 k-tiles: whole-tile waves + cuts at half tiles
+    (4096, 4096, 32),    # 1 k-tile per tile: uneven whole-tile counts, no cuts
+    (5000, 3000, 300),   # ragged in M, N and K
+    (1000, 1030, 65),    # 72 narrow tiles as 144 half-tile CTAs (grid = 2 tiles)
+]
+
+
+def _plan32_ex(dg, M, N, K, beta):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return dg.gemm_plan_ex("f32", M, N, K, 1.0, 1 << 40, K, 2 << 40, N, beta, 3 << 40, N, sms)[1]
+
+
+@pytest.mark.parametrize("shape", STREAMK_SHAPES)
+def test_f32_streamk(dg, shape):
     M, N, K = shape
-    w = workloads.Workload(f"split{M}x{N}x{K}", "f32", M, N, K, "uniform", 61)
+    w = workloads.Workload(f"sk{M}x{N}x{K}", "f32", M, N, K, "uniform", 61)
     A, B = workloads.make(w)
-    st, plan = dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N,
-                            torch.cuda.get_device_properties(0).multi_processor_count)
+    plan = _plan32_ex(dg, M, N, K, 0.0)
+    assert plan.splitk_slices == 1
+    if K > 32:
+        assert plan.split_tiles > 0
     C = run_gemm(dg, A.cuda(), B.cuda())
     rows = None if M * N * K < 3e9 else workloads.sample_rows(M, 64, seed=61)
     compare("f32", A, B, C, rows=rows)
-    return plan.split_tiles
 
 
-def test_f32_split_tail_integer_exact(dg):
-    # 1024 tiles -> 112 split tiles at 4096 x 4096; integer entries make the
-    # two-piece sums exact, so the split result is bit-exact.
-    w = workloads.Workload("split_int", "f32", 4096, 4096, 256, "int", 62, -2, 2)
+@pytest.mark.parametrize("shape", STREAMK_SHAPES)
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (2.0, -1.0)])
+def test_f32_streamk_integer_exact(dg, shape, alpha, beta):
+    M, N, K = shape
+    w = workloads.Workload(f"ski{M}x{N}x{K}", "f32", M, N, K, "int", 62, -2, 2)
     A, B = workloads.make(w)
-    C = run_gemm(dg, A.cuda(), B.cuda())
-    compare("f32", A, B, C, rows=workloads.sample_rows(w.M, 96, seed=62), exact=True)
-
+    C_in = torch.randint(-3, 4, (M, N), generator=torch.Generator().manual_seed(63)).float()
+    C = C_in.cuda()
+    Ad, Bd = A.cuda(), B.cuda()
+    st = dg.gemm_ex("f32", M, N, K, alpha, Ad.data_ptr(), K, Bd.data_ptr(), N, beta,
+                    C.data_ptr(), N, torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK, dg.status_string(st)
+    check_device(dg)
+    rows = workloads.sample_rows(M, 64, seed=64) if M * N * K >= 3e9 else None
+    a, b = workloads.to_numpy_bits(A), workloads.to_numpy_bits(B)
+    cin = workloads.to_numpy_bits(C_in) if beta != 0 else None
+    ref, _ = oracle.gemm_scaled("f32", alpha, a, b, beta, cin, rows=rows)
+    got = C.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[np.asarray(rows)]
+    assert np.array_equal(got, ref)
 
 
 def _plan32(dg, M, N, K):
