@@ -367,12 +367,33 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   plan->path = GEMM_PATH_TC_TMA;
   plan->threads = dgemm::kTcThreads;
   plan->cluster_ctas = 1;
-  // CTA pairs (256 x 256 tiles, half of B staged per SM) once there are at
-  // least as many pair tiles as SM pairs; single CTAs for smaller grids.
+  // CTA pairs (256 x 256 tiles, half of B staged per SM, 128-deep stages)
+  // unless single CTAs keep clearly more SMs busy in their first round
+  // (column parts or split-K on a small grid): with the same SMs busy the
+  // pair kernel was measured 1.06-1.17x faster (2048^3: 21.2 vs 22.6 us;
+  // 2048 x 2048 x 8192: 54.3 vs 63.5 us), so it wins unless
+  // 1.15 x its busy SMs < the single kernel's.
   const int pairs = sms / 2;
   const int pair_tiles = ceil_div(M, 2 * dgemm::kTc2BM) * ceil_div(N, dgemm::kTc2BN);
   const int forced = forced_tc_kernel();
-  if (pairs >= 1 && (forced == 2 || (forced == 0 && pair_tiles >= pairs))) {
+  const auto single_busy = [&]() {
+    const int tiles1 = ceil_div(M, dgemm::kTcBM) * ceil_div(N, dgemm::kTcBN);
+    const dgemm::TcSplit parts = dgemm::tc_split(tiles1, sms);
+    const bool fill = parts.split_tiles == tiles1 && 4 * parts.parts * tiles1 >= 3 * sms;
+    const int slices =
+        fill ? 1 : splitk_slices_capped(tiles1, sms, ceil_div(K, dgemm::kTcBK), M, N);
+    const long long units = slices > 1 ? (long long)tiles1 * slices
+                                       : tiles1 + (long long)parts.split_tiles * (parts.parts - 1);
+    return units < sms ? (int)units : sms;
+  };
+  const auto pair_busy = [&]() {
+    const dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
+    const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
+    return 2 * (units < pairs ? units : pairs);
+  };
+  const bool use_pairs =
+      forced == 2 || (forced == 0 && 115LL * pair_busy() >= 100LL * single_busy());
+  if (pairs >= 1 && use_pairs) {
     plan->cluster_ctas = 2;
     plan->block_m = 2 * dgemm::kTc2BM;
     plan->block_n = dgemm::kTc2BN;

@@ -213,9 +213,17 @@ def test_plan_paths():
                              FAKE + (2 << 30), 3000, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA and p.tiles == 17 * 12
         assert p.cluster_ctas == 2
+        # one tile: a CTA pair with two 128-column parts (4 SMs), the same
+        # number of busy SMs as four single-CTA parts, and the pair kernel
+        # is the faster one per SM
         ok, p = dg.gemm_plan(dt, 2, 3, 4, FAKE, 8, FAKE + 4096, 8, FAKE + 8192, 8, num_sms=152)
-        assert ok == dg.GEMM_OK and (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 1, 4, 4)
-        assert p.cluster_ctas == 1 and (p.block_m, p.block_n) == (128, 256) and p.splitk_slices == 1
+        assert ok == dg.GEMM_OK and (p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 1, 2, 4)
+        assert p.cluster_ctas == 2 and (p.block_m, p.block_n) == (256, 256) and p.splitk_slices == 1
+        # a 129 x 264 grid: four single-CTA tiles in four column parts (16
+        # SMs) beat two pair tiles in two parts (8 SMs)
+        ok, p = dg.gemm_plan(dt, 129, 264, 72, FAKE, 72, FAKE + 4096, 264, FAKE + (1 << 20), 264,
+                             num_sms=152)
+        assert (p.cluster_ctas, p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (1, 4, 4, 4, 16)
         # 4 tiles, 16 k-tiles: split-K, 4 slices of 4 k-tiles on 16 CTAs
         ok, p = dg.gemm_plan(dt, 256, 512, 1024, FAKE, 1024, FAKE + (1 << 30), 512,
                              FAKE + (2 << 30), 512, num_sms=152)
@@ -237,10 +245,16 @@ def test_plan_paths():
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
         assert (p.split_tiles, p.split_pieces) == (0, 1)
-        # fewer pair tiles than SM pairs: single CTAs (2048 x 1024: 32 tiles)
+        # fewer pair tiles than SM pairs (2048 x 1024: 32 tiles): still pairs,
+        # as two column parts each, 128 SMs busy like 64 single-CTA tiles in
+        # two parts would keep
         ok, p = dg.gemm_plan(dt, 2048, 1024, 512, FAKE, 512, FAKE + (1 << 30), 1024,
                              FAKE + (2 << 30), 1024, num_sms=152)
-        assert p.cluster_ctas == 1 and p.tiles == 16 * 4
+        assert (p.cluster_ctas, p.tiles, p.split_tiles, p.split_pieces, p.ctas) == (2, 32, 32, 2, 128)
+        # long K on a small grid: single-CTA split-K (2 x 1 tiles, 32 slices)
+        ok, p = dg.gemm_plan(dt, 256, 256, 65536, FAKE, 65536, FAKE + (1 << 30), 256,
+                             FAKE + (2 << 30), 256, num_sms=152)
+        assert (p.cluster_ctas, p.tiles, p.splitk_slices) == (1, 2, 32)
         # lda not a multiple of 8 elements, or a 2-byte aligned base: refused
         ok, _ = dg.gemm_plan(dt, 64, 64, 60, FAKE, 60, FAKE + 4096, 64, FAKE + 65536, 64)
         assert ok == dg.GEMM_ERR_MISALIGNED
