@@ -126,6 +126,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest `value` over all ranks (every rank gets it); the value
+    itself with one rank.  The replicas' step time is the slowest rank's."""
+    if ws <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(step_flops: float, step_ms: float, ws: int) -> float:
+    """Whole-job throughput: every one of the ws replicas does step_flops per
+    step, and a step of the job takes the slowest rank's step_ms."""
+    return ws * step_flops / (step_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ our arm
 
 def run_ours(args, ws, rank, local):
@@ -211,13 +229,9 @@ def run_ours(args, ws, rank, local):
 
     per_ms = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)]
               for i in range(len(cases))]
-    step_ms = sum(sum(x) for x in per_ms) / args.steps
-    if ws > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(sum(x) for x in per_ms) / args.steps, ws, dev)
     step_flops = sum(c["w"].flops for c in cases)
-    value = ws * step_flops / (step_ms * 1e-3) / 1e12
+    value = job_tflops(step_flops, step_ms, ws)
 
     # Per-kernel figures and rooflines.
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
