@@ -332,14 +332,22 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
             ulonglong2 b[NH];
   #pragma unroll
             for (int h = 0; h < NH; ++h) b[h] = lds128_pairs(brow + 32 * h);
+            // All eight broadcast A pairs first, then the FFMA2s with the B
+            // column group outermost: the first group needs only b[0], so
+            // the FMA pipe starts before the other fragment loads land
+            // (measured 2184 -> 2100 us at 4096^3 against row-outermost).
+            unsigned long long aa[8];
   #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float av = (&a[i].x)[kk];
-              const unsigned long long aa = pack_pair(av, av);
+              aa[i] = pack_pair(av, av);
+            }
   #pragma unroll
-              for (int h = 0; h < NH; ++h) {
-                ffma2(acc[i][2 * h + 0], aa, b[h].x);
-                ffma2(acc[i][2 * h + 1], aa, b[h].y);
+            for (int h = 0; h < NH; ++h) {
+  #pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                ffma2(acc[i][2 * h + 0], aa[i], b[h].x);
+                ffma2(acc[i][2 * h + 1], aa[i], b[h].y);
               }
             }
           }
