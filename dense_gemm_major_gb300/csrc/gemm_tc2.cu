@@ -12,9 +12,11 @@
 // A cluster of two CTAs on two SMs computes a 256 x 256 output tile with
 // tcgen05.mma.cta_group::2 (M = 256): each CTA stages its own 128 rows of A
 // and its own half (128 columns) of B, and the MMA reads the peer's half
-// through the cluster.  Per SM that is 32 KB per 64-deep k-tile instead of
-// 48 KB, so six stages fit and each SM fetches a third fewer operand bytes
-// per FLOP.
+// through the cluster.  Per SM and 64 of K that is 32 KB instead of 48 KB,
+// so each SM fetches a third fewer operand bytes per FLOP.  A ring stage is
+// 128 deep (64 KB, three stages): one barrier wait, fence and commit covers
+// eight MMAs (a %globaltimer trace had put ~43 % of the MMA issuer's loop in
+// that per-stage bookkeeping with 64-deep stages).
 //
 // Roles per CTA (192 threads): warp 0 TMA producer, warp 1 TMEM allocator
 // (both CTAs) and MMA issuer (even CTA only, one thread), warps 2-5 epilogue

@@ -32,10 +32,14 @@
 //    every issue slot of an SM sub-partition to reach the FFMA peak.
 //  * A multi-stage pipeline (wingedge777 section 6 double buffer; m.lqnn.cn v4
 //    cp.async double buffer; m.nxbn.cn section 3.1-3.2 three or four stages and
-//    TMA).  Here: a 3-stage ring filled by TMA (one thread issues both tile
-//    copies, completion on an mbarrier) or, when a base or leading dimension
-//    is not 16-byte aligned, by 4-byte cp.async with zero fill completing on
-//    the same mbarrier.  One __syncthreads per 32-deep k-tile releases a slot.
+//    TMA).  Here: a 3- or 4-stage ring filled by TMA (one thread issues both
+//    tile copies, completion on an mbarrier) or, when a base or leading
+//    dimension is not 16-byte aligned, by 4-byte cp.async with zero fill
+//    completing on the same mbarrier.  One __syncthreads per 32-deep k-tile
+//    releases a slot.
+//  * Hybrid stream-K tile scheduling (see the unit loop below) instead of one
+//    tile per CTA: full waves of whole tiles, then an equal share of the
+//    remaining (tile, k-tile) iterations per CTA.
 //  * Operands stored transposed (A as K x M, B as N x K: the column-major B
 //    of the m.lqnn.cn article, section 3.1) are transposed while they are
 //    staged: 4-byte cp.async scatters each element to its place in the same

@@ -39,12 +39,13 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_type, uint32_t m, 
          | ((m >> 4) << 24);
 }
 
-// Shared-memory descriptors of one 16-deep k-step (k16 = 0..3) of a 64-deep
-// stage, 128-byte swizzled, 8-row groups 1024 bytes apart:
-//  * K-major (rows of 64 k, 128 bytes): +32 bytes per k-step;
+// Shared-memory descriptors of one 16-deep k-step, 128-byte swizzled, 8-row
+// groups 1024 bytes apart:
+//  * K-major (rows of 64 k, 128 bytes): +32 bytes per k-step within one
+//    64-deep block (k16 = 0..3; a deeper stage keeps further blocks apart);
 //  * MN-major (rows of 64 m or n, 128 bytes, one row per k; 64-wide blocks
-//    block_bytes apart, 8 KB for a 64-deep stage): +16 rows = 2048 bytes per
-//    k-step, leading offset block_bytes.
+//    block_bytes apart, i.e. 128 bytes x the stage depth): +16 rows = 2048
+//    bytes per k-step over the whole stage depth, leading offset block_bytes.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k16) {
   return smem_desc(base + k16 * 32, 16, 1024);
 }

@@ -146,9 +146,9 @@ gemm_status_t gemm_f32_noalloc(int M, int N, int K,
  *  - beta == 0: the old C is not read (NaN or Inf there is ignored).
  *  - alpha == 0 or K == 0: C := beta * C and A, B are not read (they may be
  *    NULL); beta == 0 as well gives zeros.
- *  - gemm_f32_ex with beta != 0 computes the k-halves of a last partial
- *    wave of tiles into the library's workspace (two FP32 tiles per split
- *    tile, gemm_plan_t.workspace_bytes) and combines them in a fixed order.
+ *  - gemm_f32_ex with beta != 0 computes the two pieces of each tile cut by
+ *    the stream-K schedule into the library's workspace (two FP32 tiles per
+ *    cut, gemm_plan_t.workspace_bytes) and combines them in a fixed order.
  * alpha = 1, beta = 0 is exactly the plain entry point.
  */
 gemm_status_t gemm_f32_ex(int M, int N, int K, float alpha,
@@ -243,13 +243,15 @@ typedef struct gemm_plan_t {
   int ctas;          /* grid size                         */
   int tiles;         /* output tiles                      */
   int smem_bytes;    /* dynamic shared memory per CTA     */
-  int split_tiles;   /* tiles of the last partial wave (or of a grid that
-                        fills at most half of the CTA slots) that run as
-                        split_pieces smaller work units                   */
-  int split_pieces;  /* 1 when nothing is split.  FP32: 2 k-halves whose
-                        FP32 partials are added into C after zeroing it.
-                        FP16/BF16: 2 or 4 column parts of the output
-                        tile, each over the full K range                  */
+  int split_tiles;   /* FP32: tiles the stream-K schedule cuts into two
+                        pieces (k-ranges of two CTAs); FP16/BF16: tiles
+                        of the last partial round (or of a small grid)
+                        run as split_pieces column parts                 */
+  int split_pieces;  /* 1 when nothing is split.  FP32: 2, the pieces'
+                        FP32 partials are added into zeroed C (or, with
+                        beta != 0, combined from a workspace).  FP16/BF16:
+                        2 or 4 column parts of the output tile, each over
+                        the full K range                                  */
   int cluster_ctas;  /* FP16/BF16: 2 when CTA pairs (tcgen05 cta_group::2)
                         compute 256 x 256 tiles, else 1                   */
   int splitk_slices; /* > 1: the grid is too small for the GPU, so each tile
