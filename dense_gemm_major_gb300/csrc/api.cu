@@ -262,6 +262,74 @@ int sgemm_pick_tn(int M, int N, int K, int sms) {
   return best;
 }
 
+// FP32 plan of the problem as the SGEMM kernel sees it (M x N output, A and
+// B with storage ops op_a / op_b, a16 / b16: base and leading dimension
+// 16-byte aligned).  The arguments are already validated.
+gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool b16, float beta,
+                         int sms, gemm_plan_t* plan) {
+  // TMA cannot transpose 4-byte elements: a transposed operand is staged
+  // by the transposing cp.async loaders; with exactly one transposed, the
+  // other comes by TMA when it is 16-byte aligned.
+  if (!op_a && !op_b)
+    plan->path = (a16 && b16) ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
+  else if (op_a != op_b && (op_a ? b16 : a16))
+    plan->path = GEMM_PATH_SIMT_MIXED;
+  else
+    plan->path = GEMM_PATH_SIMT_CPASYNC;
+  const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
+  const int nk_all = ceil_div(K, dgemm::kSgemmBK);
+  // A grid of narrow tiles that fills at most half of the CTA slots runs
+  // as split-K (k-slices into a workspace, then a reduction).
+  const int slices = forced_sgemm_tn() ? 1
+                                       : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
+  if (slices > 1) {
+    plan->block_m = dgemm::kSgemmBM;
+    plan->block_n = dgemm::sgemm_bn(8);
+    plan->block_k = dgemm::kSgemmBK;
+    plan->stages = dgemm::sgemm_stages(8);
+    plan->threads = dgemm::kSgemmThreads;
+    plan->tiles = narrow_tiles;
+    plan->smem_bytes = dgemm::sgemm_smem_bytes(8);
+    plan->split_pieces = 1;
+    plan->splitk_slices = slices;
+    plan->workspace_bytes = (long long)slices * M * (((long long)N + 3) / 4 * 4) * 4;
+    plan->ctas = narrow_tiles * slices;
+    return GEMM_OK;
+  }
+  const int tn = sgemm_pick_tn(M, N, K, sms);
+  const int tcfg = tn == 9 ? 8 : tn;   // the tile shape of narrow/1 is narrow's
+  plan->block_m = dgemm::kSgemmBM;
+  plan->block_n = dgemm::sgemm_bn(tcfg);
+  plan->block_k = dgemm::kSgemmBK;
+  plan->stages = dgemm::sgemm_stages(tcfg);
+  plan->threads = dgemm::kSgemmThreads;
+  plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
+  plan->smem_bytes = dgemm::sgemm_smem_bytes(tcfg);
+  // Wave quantisation: with more tiles than resident CTAs the grid is
+  // one CTA per slot; all full waves but the last one or two run as whole
+  // tiles, and each CTA takes an equal share of the remaining tiles'
+  // (tile, k-tile) iteration space (hybrid stream-K); a range boundary
+  // inside a tile cuts it into two pieces.  With beta == 0 the pieces add
+  // into zeroed C; with beta != 0 they store FP32 partials to a workspace
+  // (two tiles per boundary) that a fixup kernel combines.
+  const int slots = (tn == 8 ? 2 : 1) * sms;
+  const int nk = ceil_div(K, dgemm::kSgemmBK);
+  // (A single wave of at most half the slots runs as two CTAs per tile:
+  // grid = 2 tiles puts every boundary in the middle of a tile.)
+  const int grid = plan->tiles > slots        ? slots
+                   : (2 * plan->tiles <= slots && nk >= 2) ? 2 * plan->tiles
+                                                           : plan->tiles;
+  const int dp_tiles = dgemm::sgemm_dp_tiles(plan->tiles, grid);
+  plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles - dp_tiles, nk, grid);
+  plan->split_pieces = plan->split_tiles ? 2 : 1;
+  plan->splitk_slices = 1;
+  if (plan->split_tiles && beta != 0.f)
+    plan->workspace_bytes =
+        (long long)(grid - 1) * 2 * dgemm::kSgemmBM * plan->block_n * 4;
+  plan->ctas = grid;
+  return GEMM_OK;
+}
+
 gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
                         const void* A, int lda, const void* B, int ldb, float beta, const void* C,
                         int ldc, int num_sms, gemm_plan_t* plan) {
@@ -298,68 +366,12 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
 
   const int sms = num_sms > 0 ? num_sms : 1;
   if (dtype == 0) {
-    // TMA cannot transpose 4-byte elements: a transposed operand is staged
-    // by the transposing cp.async loaders; with exactly one transposed, the
-    // other comes by TMA when it is 16-byte aligned.
     const bool a16 = aligned16(A) && (lda % 4 == 0), b16 = aligned16(B) && (ldb % 4 == 0);
-    if (!op_a && !op_b)
-      plan->path = (a16 && b16) ? GEMM_PATH_SIMT_TMA : GEMM_PATH_SIMT_CPASYNC;
-    else if (op_a != op_b && (op_a ? b16 : a16))
-      plan->path = GEMM_PATH_SIMT_MIXED;
-    else
-      plan->path = GEMM_PATH_SIMT_CPASYNC;
-    const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
-    const int nk_all = ceil_div(K, dgemm::kSgemmBK);
-    // A grid of narrow tiles that fills at most half of the CTA slots runs
-    // as split-K (k-slices into a workspace, then a reduction).
-    const int slices = forced_sgemm_tn() ? 1
-                                         : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
-    if (slices > 1) {
-      plan->block_m = dgemm::kSgemmBM;
-      plan->block_n = dgemm::sgemm_bn(8);
-      plan->block_k = dgemm::kSgemmBK;
-      plan->stages = dgemm::sgemm_stages(8);
-      plan->threads = dgemm::kSgemmThreads;
-      plan->tiles = narrow_tiles;
-      plan->smem_bytes = dgemm::sgemm_smem_bytes(8);
-      plan->split_pieces = 1;
-      plan->splitk_slices = slices;
-      plan->workspace_bytes = (long long)slices * M * (((long long)N + 3) / 4 * 4) * 4;
-      plan->ctas = narrow_tiles * slices;
-      return GEMM_OK;
-    }
-    const int tn = sgemm_pick_tn(M, N, K, sms);
-    const int tcfg = tn == 9 ? 8 : tn;   // the tile shape of narrow/1 is narrow's
-    plan->block_m = dgemm::kSgemmBM;
-    plan->block_n = dgemm::sgemm_bn(tcfg);
-    plan->block_k = dgemm::kSgemmBK;
-    plan->stages = dgemm::sgemm_stages(tcfg);
-    plan->threads = dgemm::kSgemmThreads;
-    plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
-    plan->smem_bytes = dgemm::sgemm_smem_bytes(tcfg);
-    // Wave quantisation: with more tiles than resident CTAs the grid is
-    // one CTA per slot; all full waves but the last one or two run as whole
-    // tiles, and each CTA takes an equal share of the remaining tiles'
-    // (tile, k-tile) iteration space (hybrid stream-K); a range boundary
-    // inside a tile cuts it into two pieces.  With beta == 0 the pieces add into zeroed C; with
-    // beta != 0 they store FP32 partials to a workspace (two tiles per
-    // boundary) that a fixup kernel combines.
-    const int slots = (tn == 8 ? 2 : 1) * sms;
-    const int nk = ceil_div(K, dgemm::kSgemmBK);
-    // (A single wave of at most half the slots runs as two CTAs per tile:
-    // grid = 2 tiles puts every boundary in the middle of a tile.)
-    const int grid = plan->tiles > slots        ? slots
-                     : (2 * plan->tiles <= slots && nk >= 2) ? 2 * plan->tiles
-                                                             : plan->tiles;
-    const int dp_tiles = dgemm::sgemm_dp_tiles(plan->tiles, grid);
-    plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles - dp_tiles, nk, grid);
-    plan->split_pieces = plan->split_tiles ? 2 : 1;
-    plan->splitk_slices = 1;
-    if (plan->split_tiles && beta != 0.f)
-      plan->workspace_bytes =
-          (long long)(grid - 1) * 2 * dgemm::kSgemmBM * plan->block_n * 4;
-    plan->ctas = grid;
-    return GEMM_OK;
+    // Both operands stored transposed: C^T = B_st . A_st is a product of two
+    // row-major arrays, which the kernel computes with TMA staging and
+    // stores transposed (SgemmParams::c_trans).
+    if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan);
+    return plan_sgemm(M, N, K, op_a, op_b, a16, b16, beta, sms, plan);
   }
   // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda % 8) || (ldb % 8) || (ldc % 8))
@@ -465,27 +477,36 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
   if (plan.path == GEMM_PATH_ZERO_FILL) {
     e = dgemm::launch_scale_c(C, M, N, ldc, dtype, beta, stream);
   } else if (dtype == 0) {
+    // The kernel's view: with both operands stored transposed it computes
+    // C^T = B_st . A_st (N x M, row-major operands) and stores C transposed.
+    const bool swap = op_a && op_b;
+    const int kM = swap ? N : M, kN = swap ? M : N;
+    const void* kA = swap ? B : A;
+    const void* kB = swap ? A : B;
+    const int klda = swap ? ldb : lda, kldb = swap ? lda : ldb;
+    const int kop_a = swap ? 0 : op_a, kop_b = swap ? 0 : op_b;
     dgemm::SgemmParams p;
-    p.M = M;
-    p.N = N;
+    p.M = kM;
+    p.N = kN;
     p.K = K;
-    p.op_a = op_a;
-    p.op_b = op_b;
-    p.A = static_cast<const float*>(A);
-    p.lda = lda;
-    p.B = static_cast<const float*>(B);
-    p.ldb = ldb;
+    p.op_a = kop_a;
+    p.op_b = kop_b;
+    p.c_trans = swap ? 1 : 0;
+    p.A = static_cast<const float*>(kA);
+    p.lda = klda;
+    p.B = static_cast<const float*>(kB);
+    p.ldb = kldb;
     p.C = static_cast<float*>(C);
     p.ldc = ldc;
-    const int tn = plan.splitk_slices > 1 ? 8 : sgemm_pick_tn(M, N, K, dev->sms);
-    p.tiles_m = ceil_div(M, dgemm::kSgemmBM);
-    p.tiles_n = ceil_div(N, plan.block_n);
+    const int tn = plan.splitk_slices > 1 ? 8 : sgemm_pick_tn(kM, kN, K, dev->sms);
+    p.tiles_m = ceil_div(kM, dgemm::kSgemmBM);
+    p.tiles_n = ceil_div(kN, plan.block_n);
     p.grid = plan.ctas;
     p.dp_tiles = plan.splitk_slices > 1 ? 0 : dgemm::sgemm_dp_tiles(plan.tiles, plan.ctas);
     p.split_tiles = plan.split_tiles;
     p.slices = plan.splitk_slices;
     p.ws = nullptr;
-    p.ldw = ((long long)N + 3) / 4 * 4;
+    p.ldw = ((long long)kN + 3) / 4 * 4;
     if (p.slices > 1) {
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
       if (st != GEMM_OK) return st;
@@ -502,19 +523,20 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     const bool tma = plan.path == GEMM_PATH_SIMT_TMA || plan.path == GEMM_PATH_SIMT_MIXED;
     alignas(64) CUtensorMap tmA{}, tmB{};
     // (Mixed staging: only the operand that is not transposed has a map.)
-    if (tma && !op_a &&
-        !encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
-                   (uint64_t)lda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
+    if (tma && !kop_a &&
+        !encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kA, (uint64_t)K, (uint64_t)kM,
+                   (uint64_t)klda * 4, dgemm::kSgemmBK, dgemm::kSgemmBM,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return GEMM_ERR_LAUNCH;
-    if (tma && !op_b &&
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
-                   (uint64_t)ldb * 4, (uint32_t)plan.block_n, dgemm::kSgemmBK,
+    if (tma && !kop_b &&
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kB, (uint64_t)kN, (uint64_t)K,
+                   (uint64_t)kldb * 4, (uint32_t)plan.block_n, dgemm::kSgemmBK,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return GEMM_ERR_LAUNCH;
     e = dgemm::launch_sgemm(p, tn, tma, &tmA, &tmB, stream);
     if (e == cudaSuccess && p.slices > 1)
-      e = dgemm::launch_splitk_reduce(p.ws, p.slices, M, N, p.ldw, C, ldc, 0, alpha, beta, stream);
+      e = dgemm::launch_splitk_reduce(p.ws, p.slices, kM, kN, p.ldw, C, ldc, 0, alpha, beta,
+                                      stream, p.c_trans);
   } else {
     const CUtensorMapDataType dt =
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -50,7 +50,7 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
 template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int slices, int M, int N,
                                      long long ldw, T* __restrict__ C, long long ldc, float alpha,
-                                     float beta) {
+                                     float beta, int c_trans) {
   const long long total = (long long)M * N;
   const long long slice_stride = (long long)M * ldw;
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -61,8 +61,9 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int slices, i
     float acc = __ldg(src);
     for (int s = 1; s < slices; ++s) acc += __ldg(src + s * slice_stride);
     float v = alpha * acc;
-    if (beta != 0.f) v = fmaf(beta, to_f32<T>(C[i * ldc + j]), v);
-    C[i * ldc + j] = from_f32<T>(v);
+    T* c = C + (c_trans ? j * ldc + i : i * ldc + j);
+    if (beta != 0.f) v = fmaf(beta, to_f32<T>(*c), v);
+    *c = from_f32<T>(v);
   }
 }
 
@@ -82,20 +83,20 @@ __global__ void scale_c_kernel(T* C, int M, int N, long long ldc, float beta) {
 
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
                                  void* C, long long ldc, int elem, float alpha, float beta,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int c_trans) {
   const long long total = (long long)M * N;
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   if (elem == 0)
     splitk_reduce_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<float*>(C), ldc, alpha, beta);
+        ws, slices, M, N, ldw, static_cast<float*>(C), ldc, alpha, beta, c_trans);
   else if (elem == 1)
     splitk_reduce_kernel<__half><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<__half*>(C), ldc, alpha, beta);
+        ws, slices, M, N, ldw, static_cast<__half*>(C), ldc, alpha, beta, c_trans);
   else
     splitk_reduce_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
-        ws, slices, M, N, ldw, static_cast<__nv_bfloat16*>(C), ldc, alpha, beta);
+        ws, slices, M, N, ldw, static_cast<__nv_bfloat16*>(C), ldc, alpha, beta, c_trans);
   return cudaGetLastError();
 }
 

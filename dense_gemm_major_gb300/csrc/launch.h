@@ -67,6 +67,10 @@ struct SgemmParams {
   // with tail_ws the fixup kernel does).
   float alpha = 1.f, beta = 0.f;
   int c_vec4;        // C rows may be written with 16-byte stores
+  // c_trans = 1: the kernel's output element (r, c) lives at C[c * ldc + r]
+  // (the product is computed as C^T = B_st . A_st for operands both stored
+  // transposed); C is then read and written element by element.
+  int c_trans = 0;
   unsigned* fault;   // device fault word
   unsigned long long timeout_ns;
 };
@@ -232,10 +236,11 @@ cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap*
 
 // C[i][j] = alpha * (sum over s of ws[s * M * ldw + i * ldw + j], in slice
 // order) + beta * C[i][j], rounded once to the element type of C (elem:
-// 0 = FP32, 1 = FP16, 2 = BF16); C is read only when beta != 0.
+// 0 = FP32, 1 = FP16, 2 = BF16); C is read only when beta != 0.  With
+// c_trans, element (i, j) of C is C[j * ldc + i].
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
                                  void* C, long long ldc, int elem, float alpha, float beta,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int c_trans = 0);
 
 // C := beta * C on an M x N block (C is not read when beta == 0): the
 // product when K == 0 or alpha == 0.

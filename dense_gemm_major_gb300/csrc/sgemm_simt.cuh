@@ -112,6 +112,12 @@ __device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long 
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
 
+// Offset of the kernel's output element (r, c) in C: row-major, or
+// transposed when the product is computed as C^T (p.c_trans).
+__host__ __device__ __forceinline__ long long c_index(const SgemmParams& p, int r, int c) {
+  return p.c_trans ? (long long)c * p.ldc + r : (long long)r * p.ldc + c;
+}
+
 // kTA / kTB: A stored K x M / B stored N x K, staged by the transposing
 // cp.async copies.  kTma: the operands that are not transposed come by TMA
 // (all others by cp.async); with one operand transposed the two kinds of
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     // stay unscaled).  The old C of one row (TN values) is loaded at once so
     // that those loads overlap instead of each waiting behind a store.
     if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
-      const bool vec4c = p.c_vec4 != 0;
+      const bool vec4c = p.c_vec4 != 0 && !p.c_trans;
   #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int gm = m0 + a_row0 + 4 * i;
@@ -427,10 +433,10 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
             if (vec4c && gn + 3 < p.N) {
               c = *reinterpret_cast<const float4*>(crow + gn);
             } else {
-              if (gn + 0 < p.N) c.x = crow[gn + 0];
-              if (gn + 1 < p.N) c.y = crow[gn + 1];
-              if (gn + 2 < p.N) c.z = crow[gn + 2];
-              if (gn + 3 < p.N) c.w = crow[gn + 3];
+              if (gn + 0 < p.N) c.x = p.C[c_index(p, gm, gn + 0)];
+              if (gn + 1 < p.N) c.y = p.C[c_index(p, gm, gn + 1)];
+              if (gn + 2 < p.N) c.z = p.C[c_index(p, gm, gn + 2)];
+              if (gn + 3 < p.N) c.w = p.C[c_index(p, gm, gn + 3)];
             }
           }
           old[h] = c;
@@ -455,11 +461,15 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     for (int i = 0; i < 8; ++i) {
       const int gm = m0 + a_row0 + 4 * i;
       if (gm >= p.M) continue;
-      // Column gn of this row is crow[gn - cshift].
+      // Column gn of this row is crow[gn - cshift] (element by element at
+      // c_index for a transposed C).
       float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
                                     : p.C + (long long)gm * p.ldc;
       const int cshift = part_n0;
-      const bool vec4 = part != nullptr ? true : p.c_vec4 != 0;
+      const bool vec4 = part != nullptr ? true : (p.c_vec4 != 0 && !p.c_trans);
+      const auto elem = [&](int col) {
+        return part != nullptr ? crow + col - cshift : p.C + c_index(p, gm, col);
+      };
   #pragma unroll
       for (int h = 0; h < NH; ++h) {
         const int gn = n0 + b_col0 + 32 * h;
@@ -470,18 +480,18 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           if (vec4 && gn + 3 < p.N) {
             atomicAdd(reinterpret_cast<float4*>(crow + gn), make_float4(v0, v1, v2, v3));
           } else {
-            if (gn + 0 < p.N) atomicAdd(crow + gn + 0, v0);
-            if (gn + 1 < p.N) atomicAdd(crow + gn + 1, v1);
-            if (gn + 2 < p.N) atomicAdd(crow + gn + 2, v2);
-            if (gn + 3 < p.N) atomicAdd(crow + gn + 3, v3);
+            if (gn + 0 < p.N) atomicAdd(elem(gn + 0), v0);
+            if (gn + 1 < p.N) atomicAdd(elem(gn + 1), v1);
+            if (gn + 2 < p.N) atomicAdd(elem(gn + 2), v2);
+            if (gn + 3 < p.N) atomicAdd(elem(gn + 3), v3);
           }
         } else if (vec4 && gn + 3 < p.N) {
           *reinterpret_cast<float4*>(crow + gn - cshift) = make_float4(v0, v1, v2, v3);
         } else {
-          if (gn + 0 < p.N) crow[gn + 0 - cshift] = v0;
-          if (gn + 1 < p.N) crow[gn + 1 - cshift] = v1;
-          if (gn + 2 < p.N) crow[gn + 2 - cshift] = v2;
-          if (gn + 3 < p.N) crow[gn + 3 - cshift] = v3;
+          if (gn + 0 < p.N) *elem(gn + 0) = v0;
+          if (gn + 1 < p.N) *elem(gn + 1) = v1;
+          if (gn + 2 < p.N) *elem(gn + 2) = v2;
+          if (gn + 3 < p.N) *elem(gn + 3) = v3;
         }
       }
     }
@@ -518,7 +528,7 @@ __global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int
   const int cols = min(bn, p.N - tn * bn);
   const float* __restrict__ p0 = p.tail_ws + (long long)(2 * (c - 1)) * (BM * bn);
   const float* __restrict__ p1 = p0 + BM * bn;
-  float* __restrict__ c0 = p.C + (long long)(tm * BM) * p.ldc + tn * bn;
+  const int r0 = tm * BM, cl0 = tn * bn;
   const int first = (int)blockIdx.y * kFixupElems;
   constexpr int kPer = kFixupElems / 256;
   float v[kPer], old[kPer];
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int
     old[q] = 0.f;
     if (r < rows && cc < cols) {
       v[q] = p0[idx] + p1[idx];
-      if (p.beta != 0.f) old[q] = c0[(long long)r * p.ldc + cc];
+      if (p.beta != 0.f) old[q] = p.C[c_index(p, r0 + r, cl0 + cc)];
     }
   }
 #pragma unroll
@@ -541,7 +551,7 @@ __global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int
     const int cc = idx - r * bn;
     if (r < rows && cc < cols) {
       const float a = p.alpha * v[q];
-      c0[(long long)r * p.ldc + cc] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
+      p.C[c_index(p, r0 + r, cl0 + cc)] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
     }
   }
 }
@@ -559,7 +569,7 @@ __global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams 
   for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
     const int r = idx / cols;
     const int c = idx - r * cols;
-    p.C[(long long)(tm * BM + r) * p.ldc + tn * bn + c] = 0.f;
+    p.C[c_index(p, tm * BM + r, tn * bn + c)] = 0.f;
   }
 }
 

@@ -194,3 +194,24 @@ def test_matmul_reads_transposed_views(dg):
         assert err <= TOL[dtype], (dtype, err)
         if dtype == "f32":
             assert torch.equal(out_t, out_r)
+
+
+@pytest.mark.parametrize("op_a,op_b", OPS)
+@pytest.mark.parametrize("dtype,shape", [("f32", (256, 256, 16384)), ("f16", (256, 256, 16384)),
+                                         ("bf16", (300, 264, 8192))])
+def test_op_splitk_scaled(dg, dtype, shape, op_a, op_b):
+    # Skinny long-K shapes run as split-K (FP32 workspace, slice-order
+    # reduction that applies alpha and beta) with the operands stored
+    # transposed.
+    M, N, K = shape
+    st, plan = dg.gemm_plan_op(dtype, op_a, op_b, M, N, K, 0.5, 1 << 40,
+                               K if op_a == "N" else (M + 7) // 8 * 8, 1 << 41,
+                               N if op_b == "N" else K, 2.0, 1 << 42, N,
+                               torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == dg.GEMM_OK and plan.splitk_slices > 1
+    A, B = _inputs(dtype, M, N, K, 111)
+    C_in = (torch.rand((M, N), generator=torch.Generator().manual_seed(112)) * 2 - 1).to(A.dtype)
+    C = C_in.cuda()
+    A_st, B_st = _stored(A, op_a), _stored(B, op_b)
+    _call(dg, dtype, op_a, op_b, A_st, B_st, C, M, N, K, alpha=0.5, beta=2.0)
+    _check(dtype, op_a, op_b, A_st, B_st, C, alpha=0.5, beta=2.0, C_in=C_in)

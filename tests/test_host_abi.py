@@ -500,7 +500,12 @@ def test_op_plans_and_validation():
     assert plan("f32", "N", "T", 104, 104)[1].path == dg.PATH_SIMT_MIXED
     assert plan("f32", "T", "N", 304, 201)[1].path == dg.PATH_SIMT_CPASYNC
     assert plan("f32", "N", "T", 101, 104)[1].path == dg.PATH_SIMT_CPASYNC
-    assert plan("f32", "T", "T", 304, 104)[1].path == dg.PATH_SIMT_CPASYNC
+    # both transposed: computed as C^T = B_st . A_st, two row-major arrays
+    # (TMA when aligned), stored transposed; the plan describes that product
+    st, p = plan("f32", "T", "T", 304, 104)
+    assert p.path == dg.PATH_SIMT_TMA
+    assert p.tiles == ((N + 127) // 128) * ((M + 127) // 128)     # N x M output, narrow tiles
+    assert plan("f32", "T", "T", 301, 104)[1].path == dg.PATH_SIMT_CPASYNC
     # FP16/BF16: TMA either way; the stored row must be 16-byte aligned
     for dt in ("f16", "bf16"):
         st, p = plan(dt, "T", "T", 304, 104)
