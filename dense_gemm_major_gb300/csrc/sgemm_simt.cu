@@ -8,7 +8,7 @@ cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUten
                          const CUtensorMap* tmB, cudaStream_t stream) {
   CUtensorMap none{};
   if (!use_tma) tmA = tmB = &none;
-  if (p.op_a || p.op_b) return launch_sgemm_op(p, tn, use_tma, tmA, tmB, stream);
+  if (p.op_a || p.op_b || p.c_trans) return launch_sgemm_op(p, tn, use_tma, tmA, tmB, stream);
   if (tn == 16)
     return use_tma ? launch_cfg<true, 16, 1>(p, tmA, tmB, stream)
                    : launch_cfg<false, 16, 1>(p, tmA, tmB, stream);

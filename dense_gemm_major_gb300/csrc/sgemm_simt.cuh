@@ -117,12 +117,18 @@ __device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long 
 __host__ __device__ __forceinline__ long long c_index(const SgemmParams& p, int r, int c) {
   return p.c_trans ? (long long)c * p.ldc + r : (long long)r * p.ldc + c;
 }
+template <bool kCT>
+__device__ __forceinline__ long long kc_index(const SgemmParams& p, int r, int c) {
+  return kCT ? (long long)c * p.ldc + r : (long long)r * p.ldc + c;
+}
 
 // kTA / kTB: A stored K x M / B stored N x K, staged by the transposing
 // cp.async copies.  kTma: the operands that are not transposed come by TMA
 // (all others by cp.async); with one operand transposed the two kinds of
 // copy complete on the same mbarrier (1 TMA arrival + 256 cp.async ones).
-template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false>
+// kCT: C is stored transposed (p.c_trans), a compile-time choice so that the
+// row-major instances carry no trace of it.
+template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false>
 __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const SgemmParams p) {
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     // stay unscaled).  The old C of one row (TN values) is loaded at once so
     // that those loads overlap instead of each waiting behind a store.
     if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
-      const bool vec4c = p.c_vec4 != 0 && !p.c_trans;
+      const bool vec4c = p.c_vec4 != 0 && !kCT;
   #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int gm = m0 + a_row0 + 4 * i;
@@ -433,10 +439,10 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
             if (vec4c && gn + 3 < p.N) {
               c = *reinterpret_cast<const float4*>(crow + gn);
             } else {
-              if (gn + 0 < p.N) c.x = p.C[c_index(p, gm, gn + 0)];
-              if (gn + 1 < p.N) c.y = p.C[c_index(p, gm, gn + 1)];
-              if (gn + 2 < p.N) c.z = p.C[c_index(p, gm, gn + 2)];
-              if (gn + 3 < p.N) c.w = p.C[c_index(p, gm, gn + 3)];
+              if (gn + 0 < p.N) c.x = kCT ? p.C[kc_index<kCT>(p, gm, gn + 0)] : crow[gn + 0];
+              if (gn + 1 < p.N) c.y = kCT ? p.C[kc_index<kCT>(p, gm, gn + 1)] : crow[gn + 1];
+              if (gn + 2 < p.N) c.z = kCT ? p.C[kc_index<kCT>(p, gm, gn + 2)] : crow[gn + 2];
+              if (gn + 3 < p.N) c.w = kCT ? p.C[kc_index<kCT>(p, gm, gn + 3)] : crow[gn + 3];
             }
           }
           old[h] = c;
@@ -466,9 +472,12 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       float* crow = part != nullptr ? part + (long long)(gm - part_m0) * part_ld
                                     : p.C + (long long)gm * p.ldc;
       const int cshift = part_n0;
-      const bool vec4 = part != nullptr ? true : (p.c_vec4 != 0 && !p.c_trans);
+      const bool vec4 = part != nullptr ? true : (p.c_vec4 != 0 && !kCT);
       const auto elem = [&](int col) {
-        return part != nullptr ? crow + col - cshift : p.C + c_index(p, gm, col);
+        if constexpr (kCT)
+          return part != nullptr ? crow + col - cshift : p.C + kc_index<kCT>(p, gm, col);
+        else
+          return crow + col - cshift;
       };
   #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -573,12 +582,12 @@ __global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams 
   }
 }
 
-template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false>
+template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false>
 cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                        cudaStream_t stream) {
   // The attribute is per function; setting it on every call is cheap and
   // keeps this correct for every device of the process.
-  cudaError_t e = cudaFuncSetAttribute(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB>,
+  cudaError_t e = cudaFuncSetAttribute(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        sgemm_smem_bytes(TN));
   if (e != cudaSuccess) return e;
@@ -591,7 +600,7 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB>
+  sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>
       <<<G, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || !cuts || p.tail_ws == nullptr) return e;

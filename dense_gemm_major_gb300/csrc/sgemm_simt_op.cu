@@ -1,6 +1,8 @@
 // FP32 SIMT SGEMM with an operand stored transposed (A as K x M and/or B as
 // N x K): the kernel of sgemm_simt.cuh with its transposing cp.async
-// loaders, the other operand by TMA where it is 16-byte aligned.  A separate translation unit so that these instances compile in
+// loaders, the other operand by TMA where it is 16-byte aligned; and the
+// row-major kernel that stores C transposed (the product of two operands
+// both stored transposed is computed as C^T).  A separate translation unit so that these instances compile in
 // parallel with the row-major ones.
 #include "sgemm_simt.cuh"
 
@@ -11,6 +13,9 @@ namespace {
 template <int TN, int kMinBlocks>
 cudaError_t launch_ops(const SgemmParams& p, bool use_tma, const CUtensorMap* tmA,
                        const CUtensorMap* tmB, cudaStream_t stream) {
+  if (p.c_trans)   // row-major operands, C stored transposed
+    return use_tma ? launch_cfg<true, TN, kMinBlocks, false, false, true>(p, tmA, tmB, stream)
+                   : launch_cfg<false, TN, kMinBlocks, false, false, true>(p, tmA, tmB, stream);
   if (p.op_a && p.op_b) return launch_cfg<false, TN, kMinBlocks, true, true>(p, tmA, tmB, stream);
   if (p.op_a)
     return use_tma ? launch_cfg<true, TN, kMinBlocks, true, false>(p, tmA, tmB, stream)
