@@ -52,7 +52,8 @@ class Plan(ctypes.Structure):
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int),
                 ("cluster_ctas", ctypes.c_int), ("splitk_slices", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_longlong)]
+                ("workspace_bytes", ctypes.c_longlong), ("pack", ctypes.c_int),
+                ("pack_bytes", ctypes.c_longlong)]
 
 
 _lib = None

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include <cuda.h>
@@ -40,22 +41,26 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_devices[kMaxDevices];
 
-// Split-K workspaces: one per (device, stream), grown on demand, never
-// shrunk, freed at process exit by the driver.
+// Device workspaces: one per (device, stream, use), grown on demand, never
+// shrunk, freed at process exit by the driver.  Use kWsPartials holds
+// split-K slices or stream-K partial tiles, kWsPack a packed operand; one
+// call can need both.
 struct Workspace {
   float* ptr = nullptr;
   size_t bytes = 0;
 };
-std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;   // guarded by g_mu
+constexpr int kWsPartials = 0, kWsPack = 1;
+std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_workspaces;   // guarded by g_mu
 
-gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out) {
+gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out,
+                            int use = kWsPartials) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_UNSUPPORTED_DEVICE;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+  Workspace& w = g_workspaces[std::make_tuple(dev, stream, use)];
   if (w.bytes < bytes) {
     // Earlier work queued on this stream may still use the old buffer.
     if (w.ptr != nullptr) {
@@ -79,6 +84,12 @@ gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out) {
 }
 
 constexpr long long kSplitkWorkspaceCap = 64ll << 20;   // bytes
+
+// Packing a transposed FP32 operand (see plan_impl): minimum reuse of each
+// packed element, minimum M * N * K, and the largest scratch copy.
+constexpr int kPackMinReuse = 256;
+constexpr long long kPackMinWork = 1ll << 30;
+constexpr long long kPackCapBytes = 1ll << 30;
 
 // Slices for a split-K problem, bounded so the workspace stays under the cap.
 int splitk_slices_capped(int tiles, int slots, int nk, int M, int N) {
@@ -177,6 +188,19 @@ inline bool overlap(const void* a, uint64_t an, const void* b, uint64_t bn) {
 }
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Measurement override: DENSE_GEMM_SGEMM_PACK=0 never packs a transposed
+// FP32 operand, =1 packs one whatever the reuse (-1 = no override).
+int forced_sgemm_pack() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_SGEMM_PACK");
+    if (s == nullptr) return -1;
+    if (std::strcmp(s, "0") == 0) return 0;
+    if (std::strcmp(s, "1") == 0) return 1;
+    return -1;
+  }();
+  return v;
+}
 
 // Measurement override: DENSE_GEMM_TC_SPLIT=0 turns off the column split of
 // the last partial round of FP16/BF16 tiles.
@@ -371,6 +395,31 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     // row-major arrays, which the kernel computes with TMA staging and
     // stores transposed (SgemmParams::c_trans).
     if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan);
+    // Exactly one stored transposed: pack it (A into M x K, B into K x N,
+    // rows padded to 16 bytes) and run the row-major product, when each
+    // packed element is used by at least kPackMinReuse output columns
+    // (rows) and the product is large enough to hide the copy's ~6 us of
+    // launch and latency.  The copy reads and writes the operand once;
+    // staging it transposed with 4-byte cp.async costs the product 13-37 %
+    // (measured on GB300: 4096^3 TN +15.6 % staged, +1.3 % packed; 2048^3
+    // +32 % / +3.5 %; 1024^3 +16 % / +10 %; 512^3 +17 % / +25 %;
+    // 4096 x 128 x 4096 TN +23 % / +30 %).
+    if (op_a || op_b) {
+      const long long rows = op_a ? M : K, cols = op_a ? K : N;
+      const long long bytes = rows * ((cols + 3) / 4 * 4) * 4;
+      const int reuse = op_a ? N : M;
+      const int forced = forced_sgemm_pack();
+      const bool pack = forced == 1 || (forced == -1 && reuse >= kPackMinReuse &&
+                                        (long long)M * N * K >= kPackMinWork &&
+                                        bytes <= kPackCapBytes);
+      if (pack) {
+        const gemm_status_t st =
+            plan_sgemm(M, N, K, 0, 0, op_a ? true : a16, op_b ? true : b16, beta, sms, plan);
+        plan->pack = op_a ? 1 : 2;
+        plan->pack_bytes = bytes;
+        return st;
+      }
+    }
     return plan_sgemm(M, N, K, op_a, op_b, a16, b16, beta, sms, plan);
   }
   // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
@@ -483,8 +532,32 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     const int kM = swap ? N : M, kN = swap ? M : N;
     const void* kA = swap ? B : A;
     const void* kB = swap ? A : B;
-    const int klda = swap ? ldb : lda, kldb = swap ? lda : ldb;
-    const int kop_a = swap ? 0 : op_a, kop_b = swap ? 0 : op_b;
+    int klda = swap ? ldb : lda, kldb = swap ? lda : ldb;
+    int kop_a = swap ? 0 : op_a, kop_b = swap ? 0 : op_b;
+    if (plan.pack) {
+      // A stored K x M becomes M x K; B stored N x K becomes K x N.
+      float* packed = nullptr;
+      st = get_workspace(stream, (size_t)plan.pack_bytes, &packed, kWsPack);
+      if (st != GEMM_OK) return st;
+      const bool pa = plan.pack == 1;
+      const long long rows = pa ? K : N, cols = pa ? M : K;
+      const long long ldp = (rows + 3) / 4 * 4;
+      e = dgemm::launch_transpose_f32(static_cast<const float*>(pa ? A : B), rows, cols,
+                                      pa ? lda : ldb, packed, ldp, dev->sms, stream);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+      }
+      if (pa) {
+        kA = packed;
+        klda = (int)ldp;
+        kop_a = 0;
+      } else {
+        kB = packed;
+        kldb = (int)ldp;
+        kop_b = 0;
+      }
+    }
     dgemm::SgemmParams p;
     p.M = kM;
     p.N = kN;
@@ -517,7 +590,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     }
     p.alpha = alpha;
     p.beta = beta;
-    p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (N % 4 == 0);
+    p.c_vec4 = aligned16(C) && (ldc % 4 == 0) && (swap || N % 4 == 0);
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
     const bool tma = plan.path == GEMM_PATH_SIMT_TMA || plan.path == GEMM_PATH_SIMT_MIXED;

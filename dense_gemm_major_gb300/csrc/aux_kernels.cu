@@ -1,6 +1,7 @@
 // Small kernels around the GEMM path: the K == 0 / alpha == 0 product
-// (C := beta * C), the split-K slice reduction, and the self-test of the
-// bounded mbarrier wait.
+// (C := beta * C), the split-K slice reduction, the FP32 operand transpose
+// that packs a transposed operand into row-major scratch, and the self-test
+// of the bounded mbarrier wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -79,6 +80,48 @@ __global__ void scale_c_kernel(T* C, int M, int N, long long ldc, float beta) {
   }
 }
 
+// D (cols x rows, row pitch ldd) := transpose of S (rows x cols, row pitch
+// lds), through 64 x 64 tiles in shared memory so that both the reads of S
+// and the writes of D are whole 128-byte row segments.  Each thread first
+// issues its 16 loads, then stores them; the tile's row pitch of 65 words
+// keeps both the row-wise writes and the column-wise reads of shared
+// memory free of bank conflicts.  HBM-bound: every element is read once
+// and written once.
+constexpr int kTrTile = 64;
+constexpr int kTrThreads = 256;
+
+__global__ void __launch_bounds__(kTrThreads)
+    transpose_f32_kernel(const float* __restrict__ S, long long rows, long long cols,
+                         long long lds, float* __restrict__ D, long long ldd) {
+  __shared__ float tile[kTrTile][kTrTile + 1];
+  constexpr int kPer = kTrTile * kTrTile / kTrThreads;   // 16
+  constexpr int kRowsPerPass = kTrThreads / kTrTile;     // 4
+  const int t = threadIdx.x;
+  const int tc = t % kTrTile, tr = t / kTrTile;
+  const long long tiles_c = (cols + kTrTile - 1) / kTrTile;
+  const long long tiles = (rows + kTrTile - 1) / kTrTile * tiles_c;
+  for (long long tile_id = blockIdx.x; tile_id < tiles; tile_id += gridDim.x) {
+    const long long r0 = tile_id / tiles_c * kTrTile;
+    const long long c0 = tile_id % tiles_c * kTrTile;
+    float v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const long long r = r0 + i * kRowsPerPass + tr, c = c0 + tc;
+      v[i] = (r < rows && c < cols) ? __ldcs(S + r * lds + c) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) tile[i * kRowsPerPass + tr][tc] = v[i];
+    __syncthreads();
+    // Row c of D holds column c of S: lane tc writes D[c0 + c][r0 + tc].
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const long long c = c0 + i * kRowsPerPass + tr, r = r0 + tc;
+      if (c < cols && r < rows) D[c * ldd + r] = tile[tc][i * kRowsPerPass + tr];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
@@ -115,6 +158,17 @@ cudaError_t launch_scale_c(void* C, int M, int N, long long ldc, int elem, float
   else
     scale_c_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(
         static_cast<__nv_bfloat16*>(C), M, N, ldc, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_f32(const float* S, long long rows, long long cols, long long lds,
+                                 float* D, long long ldd, int sms, cudaStream_t stream) {
+  const long long tiles = (rows + kTrTile - 1) / kTrTile * ((cols + kTrTile - 1) / kTrTile);
+  // 8 resident CTAs of 256 threads per SM; the loop strides over tiles.
+  long long blocks = (long long)(sms > 0 ? sms : 1) * 8 * 4;
+  if (blocks > tiles) blocks = tiles;
+  if (blocks < 1) blocks = 1;
+  transpose_f32_kernel<<<(unsigned)blocks, kTrThreads, 0, stream>>>(S, rows, cols, lds, D, ldd);
   return cudaGetLastError();
 }
 

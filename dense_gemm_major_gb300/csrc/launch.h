@@ -66,7 +66,9 @@ struct SgemmParams {
   // (in split-K mode splitk_reduce applies alpha and beta; for split tiles
   // with tail_ws the fixup kernel does).
   float alpha = 1.f, beta = 0.f;
-  int c_vec4;        // C rows may be written with 16-byte stores
+  int c_vec4;        // C rows may be written with 16-byte stores (C and ldc
+                     // 16-byte aligned; row-major C also needs N % 4 == 0,
+                     // a transposed C checks each 4-row block against M)
   // c_trans = 1: the kernel's output element (r, c) lives at C[c * ldc + r]
   // (the product is computed as C^T = B_st . A_st for operands both stored
   // transposed); C is then read and written element by element.
@@ -241,6 +243,12 @@ cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap*
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
                                  void* C, long long ldc, int elem, float alpha, float beta,
                                  cudaStream_t stream, int c_trans = 0);
+
+// D (cols x rows, row pitch ldd) := S^T for S rows x cols with row pitch lds
+// (FP32): packs an operand stored transposed into the row-major layout the
+// TMA-fed SGEMM reads.  D must not overlap S.
+cudaError_t launch_transpose_f32(const float* S, long long rows, long long cols, long long lds,
+                                 float* D, long long ldd, int sms, cudaStream_t stream);
 
 // C := beta * C on an M x N block (C is not read when beta == 0): the
 // product when K == 0 or alpha == 0.

@@ -122,6 +122,42 @@ __device__ __forceinline__ long long kc_index(const SgemmParams& p, int r, int c
   return kCT ? (long long)c * p.ldc + r : (long long)r * p.ldc + c;
 }
 
+// 4 x 4 transpose among the four lanes of a warp that share tc (their tr
+// sits in lane bits 1 and 4): before, slot s of lane t holds row 4s + t of
+// a 16-row block; after, slot r of lane t holds row 4t + r.  Two butterfly
+// steps, each swapping one bit of the lane's tr with the same bit of the
+// slot index.  All 32 lanes must take part.
+__device__ __forceinline__ void transpose4_lanes(float (&x)[4], int tr) {
+  {
+    const bool t0 = (tr & 1) != 0;
+    float a = t0 ? x[0] : x[1];
+    float b = t0 ? x[2] : x[3];
+    a = __shfl_xor_sync(0xffffffffu, a, 2);
+    b = __shfl_xor_sync(0xffffffffu, b, 2);
+    if (t0) {
+      x[0] = a;
+      x[2] = b;
+    } else {
+      x[1] = a;
+      x[3] = b;
+    }
+  }
+  {
+    const bool t1 = (tr & 2) != 0;
+    float a = t1 ? x[0] : x[2];
+    float b = t1 ? x[1] : x[3];
+    a = __shfl_xor_sync(0xffffffffu, a, 16);
+    b = __shfl_xor_sync(0xffffffffu, b, 16);
+    if (t1) {
+      x[0] = a;
+      x[1] = b;
+    } else {
+      x[2] = a;
+      x[3] = b;
+    }
+  }
+}
+
 // kTA / kTB: A stored K x M / B stored N x K, staged by the transposing
 // cp.async copies.  kTma: the operands that are not transposed come by TMA
 // (all others by cp.async); with one operand transposed the two kinds of
@@ -424,8 +460,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     // accumulators in place before any store (partial sums for a workspace
     // stay unscaled).  The old C of one row (TN values) is loaded at once so
     // that those loads overlap instead of each waiting behind a store.
-    if (part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
-      const bool vec4c = p.c_vec4 != 0 && !kCT;
+    if (!kCT && part == nullptr && (p.alpha != 1.f || p.beta != 0.f)) {
+      const bool vec4c = p.c_vec4 != 0;
   #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int gm = m0 + a_row0 + 4 * i;
@@ -439,10 +475,10 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
             if (vec4c && gn + 3 < p.N) {
               c = *reinterpret_cast<const float4*>(crow + gn);
             } else {
-              if (gn + 0 < p.N) c.x = kCT ? p.C[kc_index<kCT>(p, gm, gn + 0)] : crow[gn + 0];
-              if (gn + 1 < p.N) c.y = kCT ? p.C[kc_index<kCT>(p, gm, gn + 1)] : crow[gn + 1];
-              if (gn + 2 < p.N) c.z = kCT ? p.C[kc_index<kCT>(p, gm, gn + 2)] : crow[gn + 2];
-              if (gn + 3 < p.N) c.w = kCT ? p.C[kc_index<kCT>(p, gm, gn + 3)] : crow[gn + 3];
+              if (gn + 0 < p.N) c.x = crow[gn + 0];
+              if (gn + 1 < p.N) c.y = crow[gn + 1];
+              if (gn + 2 < p.N) c.z = crow[gn + 2];
+              if (gn + 3 < p.N) c.w = crow[gn + 3];
             }
           }
           old[h] = c;
@@ -459,6 +495,66 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           acc[i][2 * h + 1] = pack_pair(upd(hi.x, old[h].z), upd(hi.y, old[h].w));
         }
       }
+    }
+
+    if (kCT && part == nullptr) {
+      // C stored transposed: the kernel's element (gm, gn) is
+      // C[gn * ldc + gm], so a column of the tile is a row of C.  For each
+      // of its columns a thread holds rows tr + 4i; transposing among the
+      // four lanes of equal tc gives each lane four consecutive rows, stored
+      // (or, for a stream-K piece, added) as one 16-byte access, so a warp
+      // store writes whole 32-byte sectors.  C := alpha * (A.B) + beta * C
+      // is applied here, on the same 16 bytes.
+      const bool v4 = p.c_vec4 != 0;
+      const int gm_blk = m0 + a_row0 - tr;
+  #pragma unroll
+      for (int h = 0; h < NH; ++h) {
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int gn = n0 + b_col0 + 32 * h + q;
+  #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float x[4];
+  #pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              const float2 pr = unpack_pair(acc[4 * u + s][2 * h + (q >> 1)]);
+              x[s] = (q & 1) ? pr.y : pr.x;
+            }
+            transpose4_lanes(x, tr);
+            const int gm = gm_blk + 16 * u + 4 * tr;
+            if (gn >= p.N) continue;
+            float* dst = p.C + (long long)gn * p.ldc + gm;
+            if (v4 && gm + 3 < p.M) {
+              float4 v = make_float4(p.alpha * x[0], p.alpha * x[1], p.alpha * x[2],
+                                     p.alpha * x[3]);
+              if (add_into_c) {
+                atomicAdd(reinterpret_cast<float4*>(dst), v);
+              } else {
+                if (p.beta != 0.f) {
+                  const float4 o = *reinterpret_cast<const float4*>(dst);
+                  v = make_float4(fmaf(p.beta, o.x, v.x), fmaf(p.beta, o.y, v.y),
+                                  fmaf(p.beta, o.z, v.z), fmaf(p.beta, o.w, v.w));
+                }
+                *reinterpret_cast<float4*>(dst) = v;
+              }
+            } else {
+  #pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                if (gm + r >= p.M) break;
+                float v = p.alpha * x[r];
+                if (add_into_c) {
+                  atomicAdd(dst + r, v);
+                } else {
+                  if (p.beta != 0.f) v = fmaf(p.beta, dst[r], v);
+                  dst[r] = v;
+                }
+              }
+            }
+          }
+        }
+      }
+      g0 += nk;
+      continue;
     }
 
     // Epilogue: each store instruction of a warp covers four full 128-byte row

@@ -28,11 +28,14 @@
  *    work is queued on `stream` and the call returns without synchronising.
  *  - Device memory: a call whose output has too few tiles to fill the GPU
  *    and a long K runs as split-K and needs an FP32 workspace (at most
- *    64 MiB, see gemm_plan_t.workspace_bytes).  The library owns one
- *    workspace per (device, stream): it is allocated by the first call that
+ *    64 MiB, see gemm_plan_t.workspace_bytes; FP32 scaled calls also keep
+ *    stream-K partial tiles there).  gemm_f32_op with exactly one operand
+ *    transposed may copy it, transposed, into a second scratch array
+ *    (gemm_plan_t.pack_bytes, at most 1 GiB).  The library owns one of
+ *    each per (device, stream): it is allocated by the first call that
  *    needs it and grown, after synchronising that stream, when a later call
  *    needs more; it lives until the process exits.  Calls on different
- *    streams never share a workspace.  All other calls allocate nothing.
+ *    streams never share one.  All other calls allocate nothing.
  *  - Accumulation is FP32 in every type.  FP16 / BF16 results are rounded to
  *    nearest-even once, from the FP32 accumulator.
  *  - Errors: argument problems are reported synchronously, before anything
@@ -187,10 +190,15 @@ typedef enum gemm_op_t { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
  *  - FP16/BF16: both storages are read by TMA (a transposed A is an
  *    MN-major and a transposed B a K-major tcgen05 operand); the 16-byte
  *    alignment rule applies to lda and ldb in either storage.
- *  - FP32: a transposed operand is staged with 4-byte cp.async (TMA cannot
- *    transpose 4-byte elements), any alignment accepted; with exactly one
- *    operand transposed the other is staged by TMA when its base and
- *    leading dimension are 16-byte aligned (GEMM_PATH_SIMT_MIXED).
+ *  - FP32, exactly one operand transposed: when the product is large
+ *    enough (gemm_plan_t.pack) that operand is first copied, transposed,
+ *    into library scratch by an HBM-bound kernel and the row-major product
+ *    runs on the copy; otherwise it is staged with 4-byte cp.async (TMA
+ *    cannot transpose 4-byte elements) and the other operand by TMA when
+ *    its base and leading dimension are 16-byte aligned
+ *    (GEMM_PATH_SIMT_MIXED).  Any alignment is accepted either way.
+ *  - FP32, both transposed: computed as C^T = B_st . A_st (two row-major
+ *    arrays) with C stored transposed.
  *  - An op other than GEMM_OP_N / GEMM_OP_T is GEMM_ERR_INVALID_ARG.
  */
 gemm_status_t gemm_f32_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, float alpha,
@@ -259,6 +267,13 @@ typedef struct gemm_plan_t {
                         tiles go to a workspace, summed in slice order by a
                         second kernel                                     */
   long long workspace_bytes; /* device workspace that split-K needs        */
+  int pack;          /* FP32 with exactly one operand stored transposed:
+                        1 (A) or 2 (B) when that operand is first copied,
+                        transposed, into a row-major scratch array of
+                        pack_bytes by an HBM-bound kernel, and the product
+                        then runs as the row-major one (path and tiles
+                        above describe that run); 0 when nothing is packed */
+  long long pack_bytes;
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,

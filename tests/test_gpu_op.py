@@ -215,3 +215,40 @@ def test_op_splitk_scaled(dg, dtype, shape, op_a, op_b):
     A_st, B_st = _stored(A, op_a), _stored(B, op_b)
     _call(dg, dtype, op_a, op_b, A_st, B_st, C, M, N, K, alpha=0.5, beta=2.0)
     _check(dtype, op_a, op_b, A_st, B_st, C, alpha=0.5, beta=2.0, C_in=C_in)
+
+
+@pytest.mark.parametrize("op_a,op_b,shape,pad,packed", [
+    ("T", "N", (2000, 200, 600), 0, False),    # N = 200 reuses A too little: cp.async
+    ("N", "T", (200, 2000, 600), 0, False),    # M = 200: B staged transposed
+    ("T", "N", (700, 300, 333), 13, False),    # too small a product to pack
+    ("T", "N", (1024, 2048, 1025), 13, True),  # A packed, K ragged (packed rows padded)
+    ("N", "T", (1000, 2051, 1100), 5, True),   # B packed, N ragged
+    ("T", "N", (2048, 2048, 1200), 0, True),   # stream-K grid on packed A
+])
+def test_sgemm_packed_and_transposed_staging(dg, op_a, op_b, shape, pad, packed):
+    # One FP32 operand stored transposed: either packed into row-major
+    # scratch first (an HBM-bound transpose) or staged by the transposing
+    # cp.async loaders; the plan says which, the result matches the oracle
+    # either way, from stored arrays with padded, unaligned rows.
+    M, N, K = shape
+    A, B = _inputs("f32", M, N, K, 121 + M)
+    S_a, S_b = (A.t() if op_a == "T" else A), (B.t() if op_b == "T" else B)
+    Abuf = torch.full((S_a.shape[0], S_a.shape[1] + pad), float("nan"), device="cuda")
+    Bbuf = torch.full((S_b.shape[0], S_b.shape[1] + pad), float("nan"), device="cuda")
+    Abuf[:, :S_a.shape[1]] = S_a.cuda()
+    Bbuf[:, :S_b.shape[1]] = S_b.cuda()
+    A_st, B_st = Abuf[:, :S_a.shape[1]], Bbuf[:, :S_b.shape[1]]
+    st, plan = dg.gemm_plan_op("f32", op_a, op_b, M, N, K, 1.0, A_st.data_ptr(), Abuf.stride(0),
+                               B_st.data_ptr(), Bbuf.stride(0), 0.0, 1 << 44, N,
+                               torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == dg.GEMM_OK and (plan.pack != 0) == packed
+    if packed:
+        assert plan.pack == (1 if op_a == "T" else 2) and plan.path != dg.PATH_SIMT_MIXED
+    C = torch.full((M, N), float("nan"), device="cuda")
+    _call(dg, "f32", op_a, op_b, A_st, B_st, C, M, N, K)
+    _check("f32", op_a, op_b, A_st, B_st, C,
+           rows=workloads.sample_rows(M, 96, seed=M + K))
+    # a second call reuses the scratch copy on the same stream
+    C2 = torch.full((M, N), float("nan"), device="cuda")
+    _call(dg, "f32", op_a, op_b, A_st, B_st, C2, M, N, K)
+    assert torch.equal(C, C2)

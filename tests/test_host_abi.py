@@ -493,13 +493,15 @@ def test_op_plans_and_validation():
     assert dg.load().gemm_plan_op(0, 2, 0, M, N, K, 1.0, FAKE, K, FAKE + (1 << 24), N, 0.0,
                                   FAKE + (1 << 26), N, 152, ctypes.byref(dg.Plan())) \
         == dg.GEMM_ERR_INVALID_ARG
-    # FP32: a transposed operand is staged by cp.async; the other one by TMA
-    # when it is 16-byte aligned (mixed), else by cp.async too
+    # FP32: a transposed operand that is not packed (too small a product
+    # here) is staged by cp.async; the other one by TMA when it is 16-byte
+    # aligned (mixed), else by cp.async too
     assert plan("f32", "N", "N", 104, 200)[1].path == dg.PATH_SIMT_TMA
     assert plan("f32", "T", "N", 304, 200)[1].path == dg.PATH_SIMT_MIXED
     assert plan("f32", "N", "T", 104, 104)[1].path == dg.PATH_SIMT_MIXED
     assert plan("f32", "T", "N", 304, 201)[1].path == dg.PATH_SIMT_CPASYNC
     assert plan("f32", "N", "T", 101, 104)[1].path == dg.PATH_SIMT_CPASYNC
+    assert plan("f32", "T", "N", 304, 200)[1].pack == 0
     # both transposed: computed as C^T = B_st . A_st, two row-major arrays
     # (TMA when aligned), stored transposed; the plan describes that product
     st, p = plan("f32", "T", "T", 304, 104)
@@ -519,6 +521,10 @@ def test_op_plans_and_validation():
                               FAKE + (1 << 30), 4096, 0.0, FAKE + (2 << 30), 4096, 152)
     assert (p0.tiles, p0.ctas, p0.split_tiles, p0.cluster_ctas) == \
         (p1.tiles, p1.ctas, p1.split_tiles, p1.cluster_ctas)
+    # nothing is packed for FP16/BF16 (the tensor cores read either major
+    # order) or with both operands transposed (C^T = B_st . A_st)
+    assert plan("bf16", "N", "T", 104, 104)[1].pack == 0
+    assert plan("f32", "T", "T", 304, 104)[1].pack == 0
     # overlap uses the stored extent: A stored K x M spans (K-1) lda + M
     A = FAKE
     C = FAKE + 4 * ((K - 1) * M + M)          # just past A's last element
@@ -526,3 +532,38 @@ def test_op_plans_and_validation():
                            152)[0] == dg.GEMM_OK
     assert dg.gemm_plan_op("f32", "T", "N", M, N, K, 1.0, A, M, FAKE + (1 << 24), N, 0.0, C - 4,
                            N, 152)[0] == dg.GEMM_ERR_INVALID_ARG
+
+
+def test_sgemm_pack_decisions():
+    # One FP32 operand stored transposed is packed (copied transposed into
+    # row-major scratch) when the other output dimension reuses each of its
+    # elements at least 256 times, M * N * K >= 2^30 and the copy fits
+    # 1 GiB; the plan is then the row-major product's.
+    def plan(oa, ob, M, N, K):
+        lda = M if oa == "T" else K
+        ldb = K if ob == "T" else N
+        return dg.gemm_plan_op("f32", oa, ob, M, N, K, 1.0, FAKE, lda, FAKE + (1 << 36), ldb,
+                               0.0, FAKE + (1 << 38), N, 152)
+    def nn(M, N, K):
+        return dg.gemm_plan("f32", M, N, K, FAKE, K, FAKE + (1 << 36), N, FAKE + (1 << 38), N,
+                            152)[1]
+    for oa, ob, M, N, K in (("T", "N", 4096, 4096, 4096), ("N", "T", 4096, 4096, 4096),
+                            ("T", "N", 2048, 2048, 1000), ("N", "T", 256, 8192, 1024),
+                            ("N", "T", 4096, 128, 4096), ("T", "N", 128, 4096, 4096)):
+        st, p = plan(oa, ob, M, N, K)
+        q = nn(M, N, K)
+        packed = (M, (K + 3) // 4 * 4) if oa == "T" else (K, (N + 3) // 4 * 4)
+        assert st == dg.GEMM_OK and p.pack == (1 if oa == "T" else 2)
+        assert p.pack_bytes == packed[0] * packed[1] * 4
+        assert (p.path, p.tiles, p.ctas, p.block_n, p.split_tiles, p.splitk_slices) == \
+            (q.path, q.tiles, q.ctas, q.block_n, q.split_tiles, q.splitk_slices)
+    # too little reuse, or too small a product: staged transposed by cp.async
+    assert plan("T", "N", 4096, 255, 4096)[1].pack == 0
+    assert plan("N", "T", 255, 4096, 4096)[1].pack == 0
+    assert plan("T", "N", 4096, 256, 4096)[1].pack == 1
+    assert plan("T", "N", 1000, 1030, 777)[1].pack == 0
+    assert plan("N", "T", 1024, 1024, 1023)[1].pack == 0
+    assert plan("N", "T", 1024, 1024, 1024)[1].pack == 2
+    # over the 1 GiB cap: A stored 65536 x 8192 would need 2 GiB of scratch
+    st, p = plan("T", "N", 8192, 4096, 65536)
+    assert st == dg.GEMM_OK and p.pack == 0 and p.path == dg.PATH_SIMT_MIXED
