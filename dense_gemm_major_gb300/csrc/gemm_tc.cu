@@ -111,7 +111,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const T
   const int lane = threadIdx.x & 31;
   int ok = 1;
   if (lane == 0) {
-    ok = mbar_wait_bounded(bar, parity, p.timeout_ns, &bars->abort) ? 1 : 0;
+    // The producer and the MMA issuer spin; the epilogue warps, which wait a
+    // whole tile for an accumulator, suspend.
+    const bool got = fault_code == kFaultTcEpilogueWait
+                         ? mbar_wait_bounded(bar, parity, p.timeout_ns, &bars->abort)
+                         : mbar_wait_spin_bounded(bar, parity, p.timeout_ns, &bars->abort);
+    ok = got ? 1 : 0;
     if (!ok) {
       // Only the role that timed out raises its code; roles that stop
       // because another one gave up just follow.

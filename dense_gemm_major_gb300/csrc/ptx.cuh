@@ -101,6 +101,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// As mbar_wait_bounded, but every try is a plain try_wait (no suspend-time
+// hint), for the latency-critical waits of the TMA producer and the MMA
+// issuer: a thread that was suspended resumes later than the phase
+// completes (measured: 4096^3 FP16 on CTA pairs 94.2 -> 92.2 us).
+__device__ __forceinline__ bool mbar_wait_spin_bounded(uint32_t bar, uint32_t parity,
+                                                       uint64_t timeout_ns,
+                                                       const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* desc) {
