@@ -254,6 +254,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
     int local = 0;
     int nstore = 0;
+    const bool with_beta = p.beta != 0.f;
     // Rounds 64 FP32 columns (r0: 32, r1: the next 32) of this lane's row to
     // T, stages them 128-byte swizzled and TMA-stores the warp's 32 x 64 box
     // at tile column `col`.
@@ -287,11 +288,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const Unit w = unit_of(u, p, nk);
       const uint32_t b = local & 1;
       const uint32_t aph = (local >> 1) & 1u;
+      const int grow = w.tm * BM + q * 32 + lane;
+      const int col0 = w.tn * BN + w.n_off;
+      const T* c_in = static_cast<const T*>(p.c_in);
+      // (Split-K slices leave alpha and beta to the reduction.)
+      const bool old_needed = with_beta && w.slice < 0;
+      const int chunks = w.n_w / kTcEpiCols;
+      // The old C of chunk c is in old[c % 2], loaded two chunks ahead (the
+      // first two while the accumulator is still being computed).
+      uint4 old[2][8];
+      if (old_needed) {
+        load_old_row64<T>(old[0], c_in, p.ldc, p.M, p.N, grow, col0);
+        if (chunks > 1)
+          load_old_row64<T>(old[1], c_in, p.ldc, p.M, p.N, grow, col0 + kTcEpiCols);
+      }
       if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-      const int chunks = w.n_w / kTcEpiCols;
-      for (int c = 0; c < chunks; ++c) {
+#pragma unroll
+      for (int c = 0; c < BN / kTcEpiCols; ++c) {
+        if (c >= chunks) break;
         uint32_t r0[32], r1[32];
         tmem_ld32(t_row + c * kTcEpiCols, r0);
         tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
@@ -303,14 +319,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&bars->acc_empty[b]));
         }
         if (w.slice < 0) {
-          if (p.alpha != 1.f || p.beta != 0.f)
-            scale_row64<T>(r0, r1, p.alpha, p.beta, static_cast<const T*>(p.c_in), p.ldc, p.M,
-                           p.N, w.tm * BM + q * 32 + lane, w.tn * BN + w.n_off + c * kTcEpiCols);
+          if (p.alpha != 1.f || with_beta)
+            scale_row64<T>(r0, r1, p.alpha, p.beta, old[c & 1]);
+          if (old_needed && c + 2 < chunks)
+            load_old_row64<T>(old[c & 1], c_in, p.ldc, p.M, p.N, grow,
+                              col0 + (c + 2) * kTcEpiCols);
           store_box(r0, r1, w.tm, w.tn, w.n_off + c * kTcEpiCols);
         } else {
           // Split-K: this lane's row of the FP32 partial, columns beyond the
           // workspace width (ldw >= N, a multiple of 4) left out.
-          const int grow = w.tm * BM + q * 32 + lane;
           const int gcol = w.tn * BN + c * kTcEpiCols;
           if (grow < p.M) {
             float* dst = p.ws + (long long)w.slice * p.M * p.ldw + (long long)grow * p.ldw + gcol;

@@ -282,16 +282,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
     int local = 0;
     int nstore = 0;
+    const bool with_beta = p.beta != 0.f;
     for (int u = pair; u < num_units; u += npairs, ++local) {
       const Unit w = unit_of(u, p);
       const uint32_t b = local % kAccBufs;
       const uint32_t aph = (local / kAccBufs) & 1u;
+      const int row0 = w.tm * (2 * BM) + (int)rank * BM + q * 32;
+      const int col0 = w.tn * BN + w.n_off;
+      const T* c_in = static_cast<const T*>(p.c_in);
+      const int chunks = w.n_w / kTcEpiCols;
+      // The old C of chunk c is in old[c % 2], loaded two chunks ahead (the
+      // first two while the accumulator is still being computed).
+      uint4 old[2][8];
+      if (with_beta) {
+        load_old_row64<T>(old[0], c_in, p.ldc, p.M, p.N, row0 + lane, col0);
+        if (chunks > 1)
+          load_old_row64<T>(old[1], c_in, p.ldc, p.M, p.N, row0 + lane, col0 + kTcEpiCols);
+      }
       if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-      const int row0 = w.tm * (2 * BM) + (int)rank * BM + q * 32;
-      const int chunks = w.n_w / kTcEpiCols;
-      for (int c = 0; c < chunks; ++c) {
+#pragma unroll
+      for (int c = 0; c < BN / kTcEpiCols; ++c) {
+        if (c >= chunks) break;
         uint32_t r0[32], r1[32];
         tmem_ld32(t_row + c * kTcEpiCols, r0);
         tmem_ld32(t_row + c * kTcEpiCols + 32, r1);
@@ -302,9 +315,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[b]), 0));
         }
-        if (p.alpha != 1.f || p.beta != 0.f)
-          scale_row64<T>(r0, r1, p.alpha, p.beta, static_cast<const T*>(p.c_in), p.ldc, p.M, p.N,
-                         row0 + lane, w.tn * BN + w.n_off + c * kTcEpiCols);
+        if (p.alpha != 1.f || with_beta) scale_row64<T>(r0, r1, p.alpha, p.beta, old[c & 1]);
+        if (with_beta && c + 2 < chunks)
+          load_old_row64<T>(old[c & 1], c_in, p.ldc, p.M, p.N, row0 + lane,
+                            col0 + (c + 2) * kTcEpiCols);
         unsigned char* buf = stage0 + (nstore & 1) * kEpiBufBytes;
         if (lane == 0) tma_store_wait_read<1>();
         __syncwarp();

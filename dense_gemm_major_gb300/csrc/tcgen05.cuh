@@ -166,38 +166,55 @@ __device__ __forceinline__ float2 pair_to_f32<__nv_bfloat16>(uint32_t bits) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bits));
 }
 
+// The old C of row `row`, columns col..col+63 (element type T, leading
+// dimension ldc), as 8 groups of 8 raw elements; zero bits (the value 0)
+// outside M x N.  16-byte loads where a group of 8 is in bounds.  Issued by
+// the epilogue one chunk ahead of its use, and for a unit's first chunk
+// before the wait for the accumulator, so that its latency is hidden.
+template <typename T>
+__device__ __forceinline__ void load_old_row64(uint4 (&raw)[8], const T* c_in, long long ldc,
+                                               int M, int N, int row, int col) {
+  const unsigned short* src =
+      reinterpret_cast<const unsigned short*>(c_in) + (long long)row * ldc + col;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (row < M && col + 8 * g + 8 <= N) {
+      raw[g] = *reinterpret_cast<const uint4*>(src + 8 * g);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c0 = col + 8 * g + 2 * e;
+        const uint32_t lo = (row < M && c0 < N) ? src[8 * g + 2 * e] : 0u;
+        const uint32_t hi = (row < M && c0 + 1 < N) ? src[8 * g + 2 * e + 1] : 0u;
+        w[e] = lo | (hi << 16);
+      }
+      raw[g] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // v := alpha * v + beta * C_old on the 64 FP32 accumulator values (bits in
-// r0[0..31], r1[0..31]) of row `row`, columns col..col+63.  The old C
-// (element type T, leading dimension ldc) is read only when beta != 0, and
-// only inside M x N; 16-byte loads where a group of 8 is in bounds.
+// r0[0..31], r1[0..31]) of one row; `old` (from load_old_row64) is read
+// only when beta != 0.
 template <typename T>
 __device__ __forceinline__ void scale_row64(uint32_t (&r0)[32], uint32_t (&r1)[32], float alpha,
-                                            float beta, const T* c_in, long long ldc, int M,
-                                            int N, int row, int col) {
+                                            float beta, const uint4 (&old)[8]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     r0[j] = __float_as_uint(alpha * __uint_as_float(r0[j]));
     r1[j] = __float_as_uint(alpha * __uint_as_float(r1[j]));
   }
-  if (beta == 0.f || row >= M) return;
-  const T* src = c_in + (long long)row * ldc + col;
+  if (beta == 0.f) return;
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
     uint32_t* dst = g < 4 ? &r0[g * 8] : &r1[(g - 4) * 8];
-    float old[8];
-    if (col + 8 * g + 8 <= N) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(src + 8 * g);
-      const float2 a = pair_to_f32<T>(raw.x), b = pair_to_f32<T>(raw.y);
-      const float2 c = pair_to_f32<T>(raw.z), d = pair_to_f32<T>(raw.w);
-      old[0] = a.x; old[1] = a.y; old[2] = b.x; old[3] = b.y;
-      old[4] = c.x; old[5] = c.y; old[6] = d.x; old[7] = d.y;
-    } else {
+    const float2 a = pair_to_f32<T>(old[g].x), b = pair_to_f32<T>(old[g].y);
+    const float2 c = pair_to_f32<T>(old[g].z), d = pair_to_f32<T>(old[g].w);
+    const float o[8] = {a.x, a.y, b.x, b.y, c.x, c.y, d.x, d.y};
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        old[e] = (col + 8 * g + e < N) ? elem_to_f32<T>(src[8 * g + e]) : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[e] = __float_as_uint(fmaf(beta, old[e], __uint_as_float(dst[e])));
+    for (int e = 0; e < 8; ++e)
+      dst[e] = __float_as_uint(fmaf(beta, o[e], __uint_as_float(dst[e])));
   }
 }
 
