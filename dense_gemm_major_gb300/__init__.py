@@ -31,7 +31,8 @@ DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_device_check",
             "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
-            "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op")
+            "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
+            "gemm_host_blocks")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -88,6 +89,10 @@ def load() -> ctypes.CDLL:
     lib.gemm_plan_op.restype = i
     lib.gemm_plan_op.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, i,
                                  ctypes.POINTER(Plan)]
+    lib.gemm_host.restype = i
+    lib.gemm_host.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+    lib.gemm_host_blocks.restype = i
+    lib.gemm_host_blocks.argtypes = [i, i, i, i]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_status_string.argtypes = [i]
     lib.gemm_device_check.restype = i
@@ -214,6 +219,19 @@ _ENTRY_OP = {"f32": gemm_f32_op, "f16": gemm_f16_op, "bf16": gemm_bf16_op}
 def gemm_op(dtype: str, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
             stream=0) -> int:
     return _ENTRY_OP[dtype](op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_host(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+              stream=0) -> int:
+    """gemm_host: A, B, C are host addresses (see include/dense_gemm.h)."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return load().gemm_host(code, _OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B,
+                            ldb, beta, C, ldc, stream)
+
+
+def gemm_host_blocks(dtype, M, N, num_sms=152) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return load().gemm_host_blocks(code, M, N, num_sms)
 
 
 # ------------------------------------------------------------ torch wrapper

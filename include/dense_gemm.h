@@ -217,6 +217,37 @@ gemm_status_t gemm_bf16_op(gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K, 
                            gemm_bfloat16_t *C, int ldc,
                            cudaStream_t stream);
 
+/*
+ * C := alpha * op(A) . op(B) + beta * C with A, B and C in HOST memory
+ * (page-locked memory lets the copies overlap the computation; pageable
+ * memory works, with the copies the driver makes for it).  dtype: 0 = FP32
+ * (float arrays), 1 = FP16, 2 = BF16 (16-bit arrays).  The library copies
+ * B, then row blocks of A (and of C when beta != 0), into device staging
+ * buffers it owns, runs each block of rows of C as a gemm_*_op call on the
+ * caller's stream, and copies each block of C back as soon as it is done;
+ * the copies run on two side streams of the library, so the upload of the
+ * next block and the download of the previous one overlap the current
+ * block's kernels.  The call returns without synchronising: the host
+ * arrays must stay valid, and unmodified, until `stream` reaches this
+ * point.  Work queued earlier on `stream` happens first; work queued later
+ * on `stream` sees the new C.
+ *  - Argument rules of gemm_*_op, except that the host arrays need no
+ *    16-byte alignment (only element alignment).
+ *  - Device memory: staging for A, B and C (rows padded to 16 bytes), one
+ *    set per (device, stream), grown on demand after synchronising that
+ *    stream, kept until the process exits; calls on one stream from several
+ *    host threads are serialised on it.
+ *  - Results are those of gemm_*_op on each block of rows (FP32 blocks may
+ *    cut stream-K pieces elsewhere than one call on all M rows would, so
+ *    the last bits can differ; integer-valued inputs give the same bits).
+ */
+gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
+                        float alpha, const void *A, int lda, const void *B, int ldb,
+                        float beta, void *C, int ldc, cudaStream_t stream);
+/* Row blocks gemm_host cuts an M x N product into on a GPU of num_sms SMs
+ * (1, 2 or 4; blocks are multiples of 256 rows). */
+int gemm_host_blocks(int dtype, int M, int N, int num_sms);
+
 /* Static, never-null description of a status code. */
 const char *gemm_status_string(gemm_status_t status);
 

@@ -567,3 +567,32 @@ def test_sgemm_pack_decisions():
     # over the 1 GiB cap: A stored 65536 x 8192 would need 2 GiB of scratch
     st, p = plan("T", "N", 8192, 4096, 65536)
     assert st == dg.GEMM_OK and p.pack == 0 and p.path == dg.PATH_SIMT_MIXED
+
+
+def test_host_entry_blocks_and_validation():
+    # Row blocks: FP32 two while each block keeps a full grid of 128 x 256
+    # tiles, else one; FP16 / BF16 up to four blocks of whole 256-row units.
+    assert dg.gemm_host_blocks("f32", 4096, 4096, 152) == 2
+    assert dg.gemm_host_blocks("f32", 2048, 2048, 152) == 1
+    assert dg.gemm_host_blocks("f32", 8192, 1024, 152) == 1
+    assert dg.gemm_host_blocks("f16", 4096, 4096, 152) == 4
+    assert dg.gemm_host_blocks("bf16", 4097, 3000, 152) == 4
+    assert dg.gemm_host_blocks("f16", 300, 4096, 152) == 2
+    assert dg.gemm_host_blocks("f16", 256, 4096, 152) == 1
+    assert dg.gemm_host_blocks("bf16", 0, 4096, 152) == 1
+    # Argument errors are found before any CUDA call (no device needed)
+    H = 1 << 32
+    call = dg.gemm_host
+    assert call("f32", "N", "N", 0, 8, 8, 1.0, 0, 8, 0, 8, 0.0, 0, 8) == dg.GEMM_OK
+    assert call("f32", "N", "N", 8, 8, 8, 1.0, H, 8, H + 4096, 8, 0.0, H + 8192, 7) == \
+        dg.GEMM_ERR_INVALID_ARG                                     # ldc < N
+    assert call("f32", "N", "N", 8, 8, 8, 1.0, 0, 8, H + 4096, 8, 0.0, H + 8192, 8) == \
+        dg.GEMM_ERR_INVALID_ARG                                     # A null
+    assert call("f32", "T", "N", 8, 8, 4, 1.0, H, 7, H + 4096, 8, 0.0, H + 8192, 8) == \
+        dg.GEMM_ERR_INVALID_ARG                                     # A stored K x M, lda < M
+    assert call("f16", "N", "N", 8, 8, 8, 1.0, H + 1, 8, H + 4096, 8, 0.0, H + 8192, 8) == \
+        dg.GEMM_ERR_INVALID_ARG                                     # not element-aligned
+    assert call("f32", "N", "N", 8, 8, 8, 1.0, H, 8, H + 4096, 8, 0.0, H + 128, 8) == \
+        dg.GEMM_ERR_INVALID_ARG                                     # C overlaps A
+    assert dg.load().gemm_host(3, 0, 0, 8, 8, 8, 1.0, H, 8, H + 4096, 8, 0.0, H + 8192, 8,
+                               None) == dg.GEMM_ERR_INVALID_ARG     # unknown dtype
