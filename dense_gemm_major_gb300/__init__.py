@@ -261,15 +261,18 @@ def _operand(t, rows, cols):
 
 
 def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
-    """out = alpha * (A @ B) + beta * out for CUDA tensors of one dtype
-    (float32, float16, bfloat16), queued on ``stream`` (default: torch's
-    current stream).  A and B may be row-major or transposed views of
-    row-major arrays (e.g. ``X.t()``), which are read in place (op T); out
-    is row-major.  Row-padded views (row stride > width) are accepted;
-    beta != 0 needs ``out``."""
+    """out = alpha * (A @ B) + beta * out for tensors of one dtype (float32,
+    float16, bfloat16), queued on ``stream`` (default: torch's current
+    stream).  A and B may be row-major or transposed views of row-major
+    arrays (e.g. ``X.t()``), which are read in place (op T); out is
+    row-major.  Row-padded views (row stride > width) are accepted; beta != 0
+    needs ``out``.  CUDA tensors run on the device as queued work; CPU
+    tensors (page-locked or not) go through gemm_host, which stages them on
+    the GPU, and the call returns once out holds the result."""
     import torch
-    if A.device.type != "cuda" or B.device.type != "cuda":
-        raise ValueError("operands must be CUDA tensors")
+    on_host = A.device.type == "cpu" and B.device.type == "cpu"
+    if not on_host and (A.device.type != "cuda" or B.device.type != "cuda"):
+        raise ValueError("operands must be both CUDA tensors or both CPU tensors")
     if A.dtype != B.dtype:
         raise ValueError("A and B must have the same dtype")
     code = _torch_dtype_code(A)
@@ -280,13 +283,21 @@ def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
     if out is None:
         if beta != 0:
             raise ValueError("beta != 0 needs an existing out")
-        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    elif out.shape != (M, N) or out.dtype != A.dtype:
-        raise ValueError("out has the wrong shape or dtype")
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device, pin_memory=on_host)
+    elif out.shape != (M, N) or out.dtype != A.dtype or out.device.type != A.device.type:
+        raise ValueError("out has the wrong shape, dtype or device")
     if stream is None:
-        stream = torch.cuda.current_stream(A.device).cuda_stream
+        stream = (torch.cuda.current_stream() if on_host
+                  else torch.cuda.current_stream(A.device)).cuda_stream
     op_a, lda = _operand(A, M, K)
     op_b, ldb = _operand(B, K, N)
+    if on_host:
+        st = gemm_host(code, op_a, op_b, M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(),
+                       ldb, float(beta), out.data_ptr(), _ld(out, M, N), stream)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_host")
+        torch.cuda.synchronize()
+        return out
     if op_a == OP_N and op_b == OP_N and alpha == 1.0 and beta == 0.0:
         st = gemm(code, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
                   out.data_ptr(), _ld(out, M, N), stream)

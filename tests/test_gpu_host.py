@@ -151,3 +151,23 @@ def test_host_degenerate(dg):
     # M == 0: nothing happens
     assert dg.gemm_host("bf16", "N", "N", 0, 48, 16, 1.0, 0, 16, 0, 48, 0.0, 0, 48, s) == \
         dg.GEMM_OK
+
+
+def test_matmul_on_cpu_tensors(dg):
+    # matmul() hands CPU tensors to gemm_host and returns with the result in
+    # out; transposed views are read in place, pinned or pageable alike.
+    g = torch.Generator().manual_seed(11)
+    for tdt, dtype in ((torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")):
+        X = (torch.rand(700, 520, generator=g) - 0.5).to(tdt)
+        Y = (torch.rand(390, 700, generator=g) - 0.5).to(tdt)
+        for pin in (False, True):
+            Xh = X.pin_memory() if pin else X
+            Yh = Y.pin_memory() if pin else Y
+            out = dg.matmul(Xh.t(), Yh.t())                 # (520 x 700) @ (700 x 390)
+            assert out.device.type == "cpu" and out.shape == (520, 390)
+            ref = X.t().double() @ Y.t().double()
+            scale = X.t().double().abs() @ Y.t().double().abs()
+            err = ((out.double() - ref).abs() / scale).max().item()
+            assert err <= TOL[dtype], (dtype, pin, err)
+    with pytest.raises(ValueError):
+        dg.matmul(torch.ones(4, 4), torch.ones(4, 4, device="cuda"))
