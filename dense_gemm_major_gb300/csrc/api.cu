@@ -682,6 +682,14 @@ unsigned* current_fault_word() {
 }
 unsigned long long wait_bound_ns() { return wait_timeout_ns(); }
 
+bool pdl_enabled() {
+  static const bool v = [] {
+    const char* s = std::getenv("DENSE_GEMM_PDL");
+    return !(s != nullptr && std::strcmp(s, "0") == 0);
+  }();
+  return v;
+}
+
 }  // namespace dgemm
 
 extern "C" {

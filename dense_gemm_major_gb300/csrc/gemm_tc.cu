@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  wait_prior_grids();
+  allow_dependent_grids();
 
   uint32_t issued = 0;   // producer: k-tiles issued (lane 0 of warp 0)
 
@@ -379,9 +381,8 @@ cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtens
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<T, kAb, kAT, kBT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<T, kAb, kAT, kBT>
-      <<<grid, kTcThreads, kTcSmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
-  return cudaGetLastError();
+  return launch_gemm_kernel(gemm_tc_kernel<T, kAb, kAT, kBT>, dim3(grid), dim3(kTcThreads),
+                            kTcSmemBytes, stream, *tmA, *tmB, *tmC, p);
 }
 
 template <typename T, uint32_t kAb>

@@ -177,6 +177,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   cluster_sync_all();     // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  wait_prior_grids();
+  allow_dependent_grids();
   if (rank == 1 && threadIdx.x == 0) {
     // The pair's MMAs address both CTAs' TMEM at the even CTA's base.
     uint32_t leader_base;
@@ -381,9 +383,8 @@ cudaError_t launch_typed(const TcParams& p, const CUtensorMap* tmA, const CUtens
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kTc2SmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_pair_kernel<T, kAb, kAT, kBT>
-      <<<2 * pairs, kTcThreads, kTc2SmemBytes, stream>>>(*tmA, *tmB, *tmC, p);
-  return cudaGetLastError();
+  return launch_gemm_kernel(gemm_tc_pair_kernel<T, kAb, kAT, kBT>, dim3(2 * pairs),
+                            dim3(kTcThreads), kTc2SmemBytes, stream, *tmA, *tmB, *tmC, p);
 }
 
 template <typename T, uint32_t kAb>

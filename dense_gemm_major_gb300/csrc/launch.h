@@ -3,8 +3,9 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
-#include <cuda_runtime_api.h>
+#include <cuda_runtime.h>
 
 namespace dgemm {
 
@@ -272,6 +273,32 @@ inline int splitk_slices(int tiles, int slots, int nk) {
 // every device-side wait, from the C-ABI translation unit.
 unsigned* current_fault_word();
 unsigned long long wait_bound_ns();
+
+// Whether the GEMM kernels are launched as programmatic dependents of the
+// kernel before them (DENSE_GEMM_PDL=0 turns it off, for measurement).
+bool pdl_enabled();
+
+// Launches one of the GEMM kernels (SIMT, tcgen05 single CTAs or pairs),
+// which call wait_prior_grids() before their first global memory access,
+// with programmatic stream serialization: its CTAs can be scheduled, and
+// run their prologue (barriers, TMEM, descriptor prefetch), while the
+// previous kernel in the stream finishes.  Measured on GB300, back-to-back
+// FP16 GEMMs: 2048^3 18.5 -> 15.9 us, 4096^3 86.7 -> 84.4 us.
+template <typename... Params, typename... Args>
+cudaError_t launch_gemm_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- self test
 

@@ -119,6 +119,23 @@ __device__ __forceinline__ bool mbar_wait_spin_bounded(uint32_t bar, uint32_t pa
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with the
+// programmatic-stream-serialization attribute may start (run its prologue)
+// while the kernel before it in the stream is still running.
+// wait_prior_grids blocks until that kernel has completed and its memory
+// operations are visible (a no-op without the attribute): every global
+// memory access of the kernel comes after it.  allow_dependent_grids lets
+// the next kernel, if launched the same way, be scheduled as SMs free up;
+// it still waits for this kernel's completion before touching memory.
+__device__ __forceinline__ void wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_grids() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* desc) {

@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     if constexpr (!kCpB) tma_prefetch_desc(&tmB);
   }
   __syncthreads();
+  wait_prior_grids();
+  allow_dependent_grids();
 
   // Thread -> output mapping.  Warp (warp_m, warp_n) owns a 32 x (BN/2)
   // block; lane (tr, tc) owns rows tr + 4i (i < 8) and columns
@@ -696,9 +698,8 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>
-      <<<G, kSgemmThreads, sgemm_smem_bytes(TN), stream>>>(*tmA, *tmB, p);
-  e = cudaGetLastError();
+  e = launch_gemm_kernel(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>, dim3(G),
+                         dim3(kSgemmThreads), sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
   if (e != cudaSuccess || !cuts || p.tail_ws == nullptr) return e;
   const dim3 fixup_grid((unsigned)(G - 1), (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
   sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN), G);

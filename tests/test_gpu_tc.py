@@ -196,3 +196,44 @@ def test_tc_splitk_padded_c(dg, dtype):
     run_gemm(dg, A.cuda(), B.cuda(), C)
     compare(dtype, A, B, C)
     assert torch.all(Cbuf[:, N:] == -3.0), "padding columns of C were written"
+
+
+@pytest.mark.parametrize("dtype,shapes", [
+    ("f16", [(2048, 2048, 512), (2048, 1024, 2048), (2048, 256, 1024)]),    # pairs, then single CTAs
+    ("bf16", [(512, 512, 4096), (512, 1024, 512), (512, 2048, 1024)]),      # split-K, then parts
+    ("f32", [(1024, 1024, 1024), (1024, 2048, 1024), (1024, 512, 2048)]),   # stream-K, then split-K
+])
+def test_dependent_chain_without_sync(dg, dtype, shapes):
+    # Each product reads the one before as its A, all queued on one stream
+    # with no synchronisation: the kernels start early (programmatic
+    # dependent launch) but must not read their inputs before the previous
+    # kernel (and its zero / reduction kernels) has finished.  Small integer
+    # entries keep every FP32 partial sum exact, so each result is the exact
+    # product of the previous result and B, rounded once to the element type.
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    g = torch.Generator().manual_seed(17)
+    M, _, K0 = shapes[0]
+    X = torch.randint(-1, 2, (M, K0), generator=g).to(tdt).cuda()
+    Bs = []
+    for (_, N, K) in shapes:
+        Bs.append(torch.randint(-1, 2, (K, N), generator=g).to(tdt).cuda())
+    # Keep magnitudes small: about one B entry in 8 is nonzero
+    for B in Bs:
+        B[torch.rand(B.shape, generator=g).cuda() > 0.125] = 0
+    s = torch.cuda.current_stream().cuda_stream
+    cur = X
+    outs = []
+    for (_, N, K), B in zip(shapes, Bs):
+        C = torch.full((M, N), float("nan"), dtype=tdt, device="cuda")
+        assert dg.gemm(dtype, M, N, K, cur.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N,
+                       s) == dg.GEMM_OK
+        outs.append(C)
+        cur = C
+    torch.cuda.synchronize()
+    prev = X
+    for C, B in zip(outs, Bs):
+        exact = prev.double() @ B.double()
+        assert exact.abs().max().item() < 2 ** 24
+        assert torch.equal(C, exact.to(tdt))
+        prev = C
+    check_device(dg)
