@@ -302,13 +302,12 @@ def run_e2e(dg, cases, dev, stream, args):
     with A, B and C in pinned host memory: the host->device copies of A and
     B (and of the old C when beta != 0), the kernels and the device->host
     copy of C are all inside the timed events; gemm_host overlaps them
-    block by block."""
+    block by block, and the step's GEMMs run on separate streams."""
     host = []
     for c in cases:
         host.append({"A": c["A_cpu"].pin_memory(), "B": c["B_cpu"].pin_memory(),
                      "C_in": c["C_cpu"].pin_memory(),
                      "C": torch.empty(c["C"].shape, dtype=c["C"].dtype).pin_memory()})
-    sptr = stream.cuda_stream
     read_c = args.beta != 0.0
     if read_c:
         # Each step reads the C the one before wrote (C := alpha A.B + beta C
@@ -319,14 +318,26 @@ def run_e2e(dg, cases, dev, stream, args):
               + (h["C_in"].numel() * h["C_in"].element_size() if read_c else 0) for h in host)
     d2h = sum(h["C"].numel() * h["C"].element_size() for h in host)
 
+    # The GEMMs of a step are independent problems: each goes on its own
+    # stream (forked from and joined back to the timed stream), so one's
+    # copies can overlap another's kernels.
+    streams = [stream] + [torch.cuda.Stream(dev) for _ in cases[1:]]
+
     def step():
-        for c, h in zip(cases, host):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for c, h, s in zip(cases, host, streams):
             w = c["w"]
+            s.wait_event(fork)
             st = dg.gemm_host(w.dtype, "N", "N", w.M, w.N, w.K, args.alpha, h["A"].data_ptr(),
                               w.K, h["B"].data_ptr(), w.N, args.beta, h["C"].data_ptr(), w.N,
-                              sptr)
+                              s.cuda_stream)
             if st != dg.GEMM_OK:
                 raise RuntimeError(dg.status_string(st))
+        for s in streams[1:]:
+            join = torch.cuda.Event()
+            join.record(s)
+            stream.wait_event(join)
 
     steps = max(3, min(args.steps, 10))
     with torch.cuda.stream(stream):
