@@ -32,7 +32,7 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
-            "gemm_host_blocks")
+            "gemm_host_blocks", "gemm_host_k_blocks")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -93,6 +93,8 @@ def load() -> ctypes.CDLL:
     lib.gemm_host.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     lib.gemm_host_blocks.restype = i
     lib.gemm_host_blocks.argtypes = [i, i, i, i]
+    lib.gemm_host_k_blocks.restype = i
+    lib.gemm_host_k_blocks.argtypes = [i, i, i, i]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_status_string.argtypes = [i]
     lib.gemm_device_check.restype = i
@@ -232,6 +234,11 @@ def gemm_host(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
 def gemm_host_blocks(dtype, M, N, num_sms=152) -> int:
     code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
     return load().gemm_host_blocks(code, M, N, num_sms)
+
+
+def gemm_host_k_blocks(dtype, M, N, K) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return load().gemm_host_k_blocks(code, M, N, K)
 
 
 # ------------------------------------------------------------ torch wrapper

@@ -1,11 +1,12 @@
 // gemm_host: the product on operands and result in host memory.  The
 // library copies them to device staging buffers it owns and overlaps the
-// copies with the computation: C is cut into row blocks; while the GEMM of
-// block i runs on the caller's stream, the rows of A for block i + 1 go up
-// on one side stream and the finished rows of C of block i - 1 come back on
-// another.  B, which every block reads, goes up first.  Each block is an
-// ordinary gemm_*_op call on device memory, so every block takes the same
-// kernels and planning as a device call of its shape.
+// copies with the computation: C is cut into row blocks, and a large FP32
+// product also into two ranges of K; while the GEMM of one block runs on
+// the caller's stream, the operands of the next go up on one side stream
+// and the finished rows of C come back on another.  Each block is an
+// ordinary gemm_*_op call on device memory (a later K range with beta = 1
+// on the C the earlier one left), so every block takes the same kernels and
+// planning as a device call of its shape.
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -18,7 +19,8 @@
 
 namespace {
 
-constexpr int kMaxBlocks = 4;
+constexpr int kMaxBlocks = 4;    // row blocks
+constexpr int kMaxKBlocks = 2;   // ranges of K (FP32)
 constexpr int kRowAlign = 256;   // row blocks are whole CTA-pair tile rows
 
 struct HostStaging {
@@ -28,7 +30,7 @@ struct HostStaging {
   size_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t in[kMaxBlocks] = {}, out[kMaxBlocks] = {};
+  cudaEvent_t in[kMaxBlocks * kMaxKBlocks] = {}, out[kMaxBlocks] = {};
   std::mutex mu;   // one enqueue at a time per (device, stream)
 };
 
@@ -52,9 +54,10 @@ gemm_status_t staging_for(cudaStream_t stream, HostStaging** out) {
                 ok(cudaStreamCreateWithFlags(&n->down, cudaStreamNonBlocking)) &&
                 ok(cudaEventCreateWithFlags(&n->start, cudaEventDisableTiming)) &&
                 ok(cudaEventCreateWithFlags(&n->done, cudaEventDisableTiming));
+    for (int i = 0; good && i < kMaxBlocks * kMaxKBlocks; ++i)
+      good = ok(cudaEventCreateWithFlags(&n->in[i], cudaEventDisableTiming));
     for (int i = 0; good && i < kMaxBlocks; ++i)
-      good = ok(cudaEventCreateWithFlags(&n->in[i], cudaEventDisableTiming)) &&
-             ok(cudaEventCreateWithFlags(&n->out[i], cudaEventDisableTiming));
+      good = ok(cudaEventCreateWithFlags(&n->out[i], cudaEventDisableTiming));
     if (!good) {
       delete n;   // (any streams or events made are left to process exit)
       g_host.erase(std::make_pair(dev, stream));
@@ -133,6 +136,15 @@ extern "C" int gemm_host_blocks(int dtype, int M, int N, int num_sms) {
   return 1;
 }
 
+extern "C" int gemm_host_k_blocks(int dtype, int M, int N, int K) {
+  // FP32 only: the partial C between ranges stays FP32, where FP16 / BF16
+  // would round it to 16 bits once more.  Two ranges of at least 1024 when
+  // the product is large enough (>= 2^36 FLOPs) for the shorter first
+  // upload to matter against the extra launches and smaller grids.
+  if (dtype != 0 || K < 2048 || M <= 0 || N <= 0) return 1;
+  return 2.0 * M * N * K >= 68719476736.0 ? kMaxKBlocks : 1;
+}
+
 extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N,
                                    int K, float alpha, const void* A, int lda, const void* B,
                                    int ldb, float beta, void* C, int ldc, cudaStream_t stream) {
@@ -178,42 +190,63 @@ extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, in
 
   const int nb = gemm_host_blocks(dtype, M, N, sms);
   const int rows = nb == 1 ? M : (int)round_up((M + nb - 1) / nb, kRowAlign);
+  const int nkb = reads_ab ? gemm_host_k_blocks(dtype, M, N, K) : 1;
+  const int kspan = nkb == 1 ? K : (int)round_up((K + nkb - 1) / nkb, 128);
   unsigned char* const da = static_cast<unsigned char*>(h->a);
   unsigned char* const db = static_cast<unsigned char*>(h->b);
   unsigned char* const dc = static_cast<unsigned char*>(h->c);
   const unsigned char* const ha = static_cast<const unsigned char*>(A);
   const unsigned char* const hb = static_cast<const unsigned char*>(B);
   unsigned char* const hc = static_cast<unsigned char*>(C);
+  const auto up = [&](void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                       size_t height) {
+    return width == 0 || height == 0 ||
+           ok(cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height,
+                                cudaMemcpyHostToDevice, h->up));
+  };
 
   // Everything queued before this call on `stream` happens first.
   if (!ok(cudaEventRecord(h->start, stream)) || !ok(cudaStreamWaitEvent(h->up, h->start, 0)) ||
       !ok(cudaStreamWaitEvent(h->down, h->start, 0)))
     return GEMM_ERR_LAUNCH;
-  if (reads_ab && !ok(cudaMemcpy2DAsync(db, dlb * es, hb, (size_t)ldb * es, b_cols * es, b_rows,
-                                        cudaMemcpyHostToDevice, h->up)))
-    return GEMM_ERR_LAUNCH;
   for (int i = 0; i < nb; ++i) {
     const int r0 = i * rows;
     const int m = (M - r0) < rows ? (M - r0) : rows;
-    // This block's operand rows of A: rows r0.. of A stored M x K, or
-    // columns r0.. of A stored K x M.
-    const unsigned char* a_src = op_a ? ha + (size_t)r0 * es : ha + (size_t)r0 * lda * es;
-    unsigned char* a_dst = op_a ? da + (size_t)r0 * es : da + (size_t)r0 * dla * es;
-    const size_t a_w = (op_a ? (size_t)m : (size_t)K) * es;
-    const size_t a_h = op_a ? (size_t)K : (size_t)m;
-    if (reads_ab && !ok(cudaMemcpy2DAsync(a_dst, dla * es, a_src, (size_t)lda * es, a_w, a_h,
-                                          cudaMemcpyHostToDevice, h->up)))
-      return GEMM_ERR_LAUNCH;
     unsigned char* c_dev = dc + (size_t)r0 * dlc * es;
     unsigned char* c_host = hc + (size_t)r0 * ldc * es;
-    if (reads_c && !ok(cudaMemcpy2DAsync(c_dev, dlc * es, c_host, (size_t)ldc * es, (size_t)N * es,
-                                         m, cudaMemcpyHostToDevice, h->up)))
-      return GEMM_ERR_LAUNCH;
-    if (!ok(cudaEventRecord(h->in[i], h->up)) || !ok(cudaStreamWaitEvent(stream, h->in[i], 0)))
-      return GEMM_ERR_LAUNCH;
-    st = run_device(dtype, op_a, op_b, m, N, K, alpha, reads_ab ? a_dst : nullptr, (int)dla,
-                    reads_ab ? db : nullptr, (int)dlb, beta, c_dev, (int)dlc, stream);
-    if (st != GEMM_OK) return st;
+    for (int j = 0; j < nkb; ++j) {
+      const int k0 = j * kspan;
+      const int kk = (K - k0) < kspan ? (K - k0) : kspan;
+      // B's rows k0.. (stored K x N) or columns k0.. (stored N x K), once.
+      unsigned char* b_blk = op_b ? db + (size_t)k0 * es : db + (size_t)k0 * dlb * es;
+      if (reads_ab && i == 0) {
+        const unsigned char* b_src = op_b ? hb + (size_t)k0 * es : hb + (size_t)k0 * ldb * es;
+        if (!up(b_blk, dlb * es, b_src, (size_t)ldb * es,
+                (op_b ? (size_t)kk : (size_t)N) * es, op_b ? (size_t)N : (size_t)kk))
+          return GEMM_ERR_LAUNCH;
+      }
+      // A's rows r0.. and columns k0.. (stored M x K), or rows k0.. and
+      // columns r0.. (stored K x M).
+      const size_t a_off = op_a ? (size_t)k0 * dla + r0 : (size_t)r0 * dla + k0;
+      unsigned char* a_blk = da + a_off * es;
+      if (reads_ab) {
+        const size_t h_off = op_a ? (size_t)k0 * lda + r0 : (size_t)r0 * lda + k0;
+        if (!up(a_blk, dla * es, ha + h_off * es, (size_t)lda * es,
+                (op_a ? (size_t)m : (size_t)kk) * es, op_a ? (size_t)kk : (size_t)m))
+          return GEMM_ERR_LAUNCH;
+      }
+      if (j == 0 && reads_c &&
+          !up(c_dev, dlc * es, c_host, (size_t)ldc * es, (size_t)N * es, (size_t)m))
+        return GEMM_ERR_LAUNCH;
+      cudaEvent_t in = h->in[i * kMaxKBlocks + j];
+      if (!ok(cudaEventRecord(in, h->up)) || !ok(cudaStreamWaitEvent(stream, in, 0)))
+        return GEMM_ERR_LAUNCH;
+      // A later range of K adds onto the C the earlier one left.
+      st = run_device(dtype, op_a, op_b, m, N, reads_ab ? kk : K, alpha,
+                      reads_ab ? a_blk : nullptr, (int)dla, reads_ab ? b_blk : nullptr, (int)dlb,
+                      j == 0 ? beta : 1.f, c_dev, (int)dlc, stream);
+      if (st != GEMM_OK) return st;
+    }
     if (!ok(cudaEventRecord(h->out[i], stream)) ||
         !ok(cudaStreamWaitEvent(h->down, h->out[i], 0)) ||
         !ok(cudaMemcpy2DAsync(c_host, (size_t)ldc * es, c_dev, dlc * es, (size_t)N * es, m,

@@ -74,6 +74,9 @@ def _rows(M, blocks):
 
 @pytest.mark.parametrize("dtype,shape,op_a,op_b,pad", [
     ("f32", (4096, 4096, 512), "N", "N", 0),     # two row blocks
+    ("f32", (4096, 4096, 4096), "N", "N", 0),    # two row blocks x two ranges of K
+    ("f32", (4096, 3000, 4100), "T", "N", 3),    # ranges of K on A stored K x M (packed)
+    ("f32", (2304, 4096, 8192), "N", "T", 0),    # ranges of K on B stored N x K
     ("f32", (1000, 1030, 777), "N", "N", 3),     # one block, unaligned host rows
     ("f32", (4096, 2048, 300), "T", "N", 1),     # A stored K x M: column blocks of it
     ("f16", (4096, 4096, 512), "N", "N", 0),     # four blocks
@@ -94,11 +97,14 @@ def test_host_parity(dg, dtype, shape, op_a, op_b, pad):
     _check(dtype, op_a, op_b, A_st, B_st, C, _rows(M, nb))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-def test_host_scaled_integer_exact(dg, dtype):
-    # alpha / beta with the old C uploaded block by block; integer entries
-    # make every order of summation exact, so the bits are the oracle's.
-    M, N, K = 2304, 1536, 256
+@pytest.mark.parametrize("dtype,shape", [("f32", (2304, 1536, 256)), ("f16", (2304, 1536, 256)),
+                                         ("bf16", (2304, 1536, 256)),
+                                         ("f32", (4096, 2048, 4096))])   # with ranges of K
+def test_host_scaled_integer_exact(dg, dtype, shape):
+    # alpha / beta with the old C uploaded block by block (the second range
+    # of K adds with beta = 1); integer entries make every order of
+    # summation exact, so the bits are the oracle's.
+    M, N, K = shape
     w = workloads.Workload("host_int", dtype, M, N, K, "int", 5, -2, 2)
     A, B = workloads.make(w)
     C_in = torch.randint(-3, 4, (M, N), generator=torch.Generator().manual_seed(6)).to(A.dtype)
