@@ -664,7 +664,9 @@ __global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int
 }
 
 // Zeroes C on the tile cut by boundary blockIdx.x + 1 (if any) before its
-// two pieces add into it.
+// two pieces add into it; block y takes rows y, y + gridDim.y, ... of the
+// tile, with 16-byte stores when C's rows allow them.
+constexpr int kZeroRowSplit = 16;
 __global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn,
                                                               int G) {
   const int tile = cut_tile(p, (int)blockIdx.x + 1, G);
@@ -673,10 +675,16 @@ __global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams 
   grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
   const int rows = min(BM, p.M - tm * BM);
   const int cols = min(bn, p.N - tn * bn);
-  for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
-    const int r = idx / cols;
-    const int c = idx - r * cols;
-    p.C[c_index(p, tm * BM + r, tn * bn + c)] = 0.f;
+  const bool vec = p.c_vec4 != 0 && !p.c_trans && cols % 4 == 0;
+  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    if (vec) {
+      float4* row = reinterpret_cast<float4*>(p.C + (long long)(tm * BM + r) * p.ldc + tn * bn);
+      for (int c = threadIdx.x; c < cols / 4; c += blockDim.x)
+        row[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int c = threadIdx.x; c < cols; c += blockDim.x)
+        p.C[c_index(p, tm * BM + r, tn * bn + c)] = 0.f;
+    }
   }
 }
 
@@ -694,7 +702,8 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
   const int G = p.slices > 1 ? tiles * p.slices : p.grid;
   const bool cuts = p.slices == 1 && p.split_tiles > 0;
   if (cuts && p.tail_ws == nullptr) {
-    sgemm_zero_split_tiles<<<G - 1, 256, 0, stream>>>(p, sgemm_bn(TN), G);
+    sgemm_zero_split_tiles<<<dim3((unsigned)(G - 1), kZeroRowSplit), 256, 0, stream>>>(
+        p, sgemm_bn(TN), G);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
