@@ -54,7 +54,7 @@ class Plan(ctypes.Structure):
                 ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int),
                 ("cluster_ctas", ctypes.c_int), ("splitk_slices", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_longlong), ("pack", ctypes.c_int),
-                ("pack_bytes", ctypes.c_longlong)]
+                ("pack_bytes", ctypes.c_longlong), ("split_in_k", ctypes.c_int)]
 
 
 _lib = None

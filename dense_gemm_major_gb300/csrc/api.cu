@@ -48,8 +48,11 @@ DeviceInfo g_devices[kMaxDevices];
 struct Workspace {
   float* ptr = nullptr;
   size_t bytes = 0;
+  unsigned epoch = 0;   // kWsFlags: the last epoch handed to a launch
 };
-constexpr int kWsPartials = 0, kWsPack = 1;
+// kWsFlags holds the hand-over flags of the pair kernel's K split: zeroed
+// when (re)allocated, then only ever set to a launch's epoch and cleared.
+constexpr int kWsPartials = 0, kWsPack = 1, kWsFlags = 2;
 std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_workspaces;   // guarded by g_mu
 
 gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out,
@@ -78,9 +81,23 @@ gemm_status_t get_workspace(cudaStream_t stream, size_t bytes, float** out,
       return GEMM_ERR_LAUNCH;
     }
     w.bytes = bytes;
+    if (use == kWsFlags && cudaMemsetAsync(w.ptr, 0, bytes, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
   }
   *out = w.ptr;
   return GEMM_OK;
+}
+
+// The next epoch of the K-split flags of (current device, stream); never 0.
+unsigned next_epoch(cudaStream_t stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) cudaGetLastError();
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace& w = g_workspaces[std::make_tuple(dev, stream, kWsFlags)];
+  if (++w.epoch == 0) w.epoch = 1;
+  return w.epoch;
 }
 
 constexpr long long kSplitkWorkspaceCap = 64ll << 20;   // bytes
@@ -198,6 +215,16 @@ int forced_sgemm_pack() {
     if (std::strcmp(s, "0") == 0) return 0;
     if (std::strcmp(s, "1") == 0) return 1;
     return -1;
+  }();
+  return v;
+}
+
+// Measurement override: DENSE_GEMM_TC_KSPLIT=0 turns off the K split of the
+// pair kernel's last partial round (its column split then applies).
+bool tc_ksplit_disabled() {
+  static const bool v = [] {
+    const char* s = std::getenv("DENSE_GEMM_TC_KSPLIT");
+    return s != nullptr && std::strcmp(s, "0") == 0;
   }();
   return v;
 }
@@ -447,8 +474,17 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
                                        : tiles1 + (long long)parts.split_tiles * (parts.parts - 1);
     return units < sms ? (int)units : sms;
   };
+  const int nk_pair = ceil_div(K, dgemm::kTc2BK);
+  // The pair kernel's last partial round: K ranges when K is long enough,
+  // else column parts.
+  const auto pair_split = [&]() {
+    const dgemm::TcSplit ks = tc_ksplit_disabled()
+                                  ? dgemm::TcSplit{0, 1}
+                                  : dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair);
+    return ks.split_tiles ? ks : dgemm::tc_pair_split(pair_tiles, pairs);
+  };
   const auto pair_busy = [&]() {
-    const dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
+    const dgemm::TcSplit sp = pair_split();
     const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
     return 2 * (units < pairs ? units : pairs);
   };
@@ -461,10 +497,15 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     plan->block_k = dgemm::kTc2BK;
     plan->stages = dgemm::kTc2Stages;
     plan->tiles = pair_tiles;
-    dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
+    dgemm::TcSplit sp = pair_split();
     if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
     plan->split_tiles = sp.split_tiles;
     plan->split_pieces = sp.parts;
+    plan->split_in_k = sp.split_tiles > 0 && !tc_ksplit_disabled() &&
+                       dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair).split_tiles > 0;
+    if (plan->split_in_k)
+      plan->workspace_bytes = (long long)sp.split_tiles * (sp.parts - 1) * 2 * dgemm::kTc2BM *
+                              dgemm::kTc2BN * 4;
     plan->splitk_slices = 1;
     const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
     plan->ctas = 2 * (units < pairs ? units : pairs);
@@ -655,6 +696,18 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.ldc = ldc;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
+    if (plan.split_in_k) {
+      // Partials of the K pieces before the last, and their flags.
+      p.ksplit = 1;
+      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.kpart);
+      if (st != GEMM_OK) return st;
+      float* flags = nullptr;
+      st = get_workspace(stream, (size_t)plan.split_tiles * (plan.split_pieces - 1) * 8 * 4,
+                         &flags, kWsFlags);
+      if (st != GEMM_OK) return st;
+      p.kflag = reinterpret_cast<unsigned*>(flags);
+      p.epoch = next_epoch(stream);
+    }
     if (plan.cluster_ctas == 2)
       e = dgemm::launch_gemm_tc_pair(dtype, p, &tmA, &tmB, &tmC, plan.ctas / 2, stream);
     else

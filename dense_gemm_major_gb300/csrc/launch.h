@@ -173,6 +173,16 @@ struct TcParams {
   int full_tiles;
   int split_tiles;
   int parts;
+  // Pair kernel, ksplit = 1 (parts = 2): the split tiles' units are instead
+  // two ranges of K over the whole tile.  Piece 0 stores its FP32
+  // accumulator at kpart (one 128 x 256 block per CTA and split tile) and
+  // sets its flags to `epoch`; piece 1 waits for them, adds the partial to
+  // its own accumulator, applies alpha / beta, stores C and clears the
+  // flags.  kflag: one word per (split tile, CTA, epilogue warp).
+  int ksplit = 0;
+  float* kpart = nullptr;
+  unsigned* kflag = nullptr;
+  unsigned epoch = 0;
   unsigned* fault;
   unsigned long long timeout_ns;
 };
@@ -225,6 +235,28 @@ inline TcSplit tc_pair_split(int tiles, int pairs) {
   TcSplit sp{0, 1};
   const int rem = tiles % pairs;
   if (rem == 0 || 2 * rem > pairs) return sp;
+  sp.split_tiles = rem;
+  sp.parts = 2;
+  return sp;
+}
+
+// K split of the last partial round for the pair kernel: when the leftover
+// tiles fit the round twice over and K has at least kTc2KsplitMinK 128-deep
+// stages, each leftover tile becomes two full-width units over two ranges
+// of K; {0, 1} otherwise (the column split then applies).  Full-width units
+// keep the operand feed per SM of whole tiles, where half-width column parts
+// run at ~70 % of that rate.  The first range is kTc2KsplitLead stages
+// shorter than half, so that the second piece's MMAs still run while the
+// first stores its FP32 partial (~3.5 us, about six stages).  The hand-over
+// (that store, and ~1.6 us more in the finishing epilogue) only pays for
+// long K, measured on GB300: 4096^2 x 8192 FP16 174.1 -> 168.5 us, 8192^3
+// BF16 593.6 -> 588 us, 4096^3 92.2 both ways, K = 2048 8-10 % slower.
+constexpr int kTc2KsplitMinK = 48;
+constexpr int kTc2KsplitLead = 3;
+inline TcSplit tc_pair_ksplit(int tiles, int pairs, int nk) {
+  TcSplit sp{0, 1};
+  const int rem = tiles % pairs;
+  if (rem == 0 || tiles < pairs || 2 * rem > pairs || nk < kTc2KsplitMinK) return sp;
   sp.split_tiles = rem;
   sp.parts = 2;
   return sp;

@@ -119,6 +119,32 @@ __device__ __forceinline__ bool mbar_wait_spin_bounded(uint32_t bar, uint32_t pa
   }
 }
 
+// Release store / acquire poll of a 32-bit flag in global memory, for
+// handing a partial result from one CTA to another of the same grid.
+__device__ __forceinline__ void flag_store_release(unsigned* f, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned flag_load_acquire(const unsigned* f) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  return v;
+}
+// Waits until *f == v.  Returns false if `timeout_ns` elapses first or
+// `*abort` becomes non-zero.
+__device__ __forceinline__ bool flag_wait_equal(const unsigned* f, unsigned v, uint64_t timeout_ns,
+                                                const volatile int* abort) {
+  if (flag_load_acquire(f) == v) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (flag_load_acquire(f) == v) return true;
+    if ((it & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // Programmatic dependent launch: a kernel launched with the
@@ -200,6 +226,19 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// 16-byte cp.async global -> shared through L2 only (data another SM just
+// wrote), completed by commit / wait_group.
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -215,6 +254,7 @@ enum FaultCode : unsigned {
   kFaultSelftestWait = 1u << 4,
   kFaultDrainWait = 1u << 5,
   kFaultTcPairTmem = 1u << 6,   // the two CTAs of a pair got different TMEM bases
+  kFaultTcPartialWait = 1u << 7,   // a K-split piece's partial never arrived
 };
 
 __device__ __forceinline__ void raise_fault(unsigned* fault, unsigned code) {

@@ -309,6 +309,12 @@ typedef struct gemm_plan_t {
                         then runs as the row-major one (path and tiles
                         above describe that run); 0 when nothing is packed */
   long long pack_bytes;
+  int split_in_k;    /* FP16/BF16 CTA pairs: 1 when the split_tiles tiles of
+                        the last partial round are cut into split_pieces
+                        ranges of K over all 256 columns (the last piece
+                        adds the others' FP32 partials, kept in the
+                        workspace, before it stores the tile) instead of
+                        column parts                                       */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,

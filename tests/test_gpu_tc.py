@@ -1,8 +1,10 @@
 """GPU parity of the FP16 / BF16 tcgen05 GEMM against the CPU oracle,
 called through the C ABI."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from parity import check_device, compare, gpu_lib, padded, run_gemm
 
@@ -237,3 +239,53 @@ def test_dependent_chain_without_sync(dg, dtype, shapes):
         assert torch.equal(C, exact.to(tdt))
         prev = C
     check_device(dg)
+
+
+@pytest.mark.parametrize("dtype,shape", [("f16", (4096, 4096, 8192)),     # 28 leftover tiles
+                                         ("bf16", (1280, 4864, 6144)),    # 19 leftover tiles
+                                         ("f16", (4096, 2816, 6200))])    # ragged K
+def test_pair_k_split_last_round(dg, dtype, shape):
+    # The pair kernel's last partial round as two full-width K pieces: the
+    # first hands its FP32 partial to the second through the workspace and
+    # a flag.  NaN-poisoned C; sampled rows cover every tile row.
+    M, N, K = shape
+    plan = _plan(dg, dtype, M, N, K)
+    assert plan.cluster_ctas == 2 and plan.split_in_k == 1 and plan.split_pieces == 2, \
+        (plan.cluster_ctas, plan.split_in_k, plan.split_pieces)
+    w = workloads.Workload(f"{dtype}_ksplit", dtype, M, N, K, "normal", 73)
+    A, B = workloads.make(w)
+    C = run_gemm(dg, A.cuda(), B.cuda())
+    rows = sorted({r for t in range(0, M, 256) for r in (t, t + 127, t + 128, min(t + 255, M - 1))})
+    compare(dtype, A, B, C, rows=np.asarray(rows))
+    # the same call again reuses the workspace and the flags (next epoch)
+    C2 = run_gemm(dg, A.cuda(), B.cuda())
+    assert torch.equal(C, C2)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_pair_k_split_integer_scaled_exact(dg, dtype):
+    # Integer entries: the two pieces' sums and alpha * sum + beta * C are
+    # exact in FP32 and in the output type, so the bits are the oracle's.
+    M, N, K = 4096, 4096, 6144
+    plan = _plan(dg, dtype, M, N, K)
+    assert plan.split_in_k == 1
+    lo, hi = (-1, 1)
+    w = workloads.Workload(f"{dtype}_ksplit_int", dtype, M, N, K, "int", 74, lo, hi)
+    A, B = workloads.make(w)
+    B = B.clone()
+    B[torch.rand(B.shape, generator=torch.Generator().manual_seed(75)) > 0.25] = 0   # |sums| small
+    g = torch.Generator().manual_seed(76)
+    C_in = torch.randint(-4, 5, (M, N), generator=g).to(A.dtype)
+    C = C_in.cuda()
+    Ad, Bd = A.cuda(), B.cuda()
+    st = dg.gemm_ex(dtype, M, N, K, 2.0, Ad.data_ptr(), K, Bd.data_ptr(), N, -1.0, C.data_ptr(), N,
+                    torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK
+    check_device(dg)
+    rows = workloads.sample_rows(M, 64, seed=77)
+    a = workloads.to_numpy_bits(A)
+    b = workloads.to_numpy_bits(B)
+    ref, S = oracle.gemm_scaled(dtype, 2.0, a, b, -1.0, workloads.to_numpy_bits(C_in), rows=rows)
+    expect = oracle.decode(dtype, oracle.round_rn(dtype, ref))
+    got = C.float().cpu().numpy().astype(np.float64)[rows]
+    assert np.array_equal(got, expect)

@@ -603,3 +603,28 @@ def test_host_entry_blocks_and_validation():
         dg.GEMM_ERR_INVALID_ARG                                     # C overlaps A
     assert dg.load().gemm_host(3, 0, 0, 8, 8, 8, 1.0, H, 8, H + 4096, 8, 0.0, H + 8192, 8,
                                None) == dg.GEMM_ERR_INVALID_ARG     # unknown dtype
+
+
+def test_pair_last_round_k_split_plans():
+    # The CTA-pair kernel's last partial round: when the leftover tiles fit
+    # the round twice and K has at least 48 stages of 128, each leftover
+    # tile runs as two full-width units over two ranges of K (the first
+    # piece's FP32 partial in the workspace); else as column parts.
+    def plan(dt, M, N, K):
+        return dg.gemm_plan(dt, M, N, K, FAKE, K, FAKE + (1 << 34), N, FAKE + (1 << 36), N, 152)[1]
+    tile = 256 * 256 * 4
+    p = plan("f16", 4096, 4096, 8192)              # 256 tiles = 3 x 76 + 28, 64 stages
+    assert (p.cluster_ctas, p.split_tiles, p.split_pieces, p.split_in_k) == (2, 28, 2, 1)
+    assert p.workspace_bytes == 28 * tile
+    p = plan("bf16", 1280, 4864, 6144)             # 95 tiles = 76 + 19, 48 stages
+    assert (p.cluster_ctas, p.split_tiles, p.split_pieces, p.split_in_k) == (2, 19, 2, 1)
+    assert p.workspace_bytes == 19 * tile
+    p = plan("f16", 4096, 4096, 4096)              # 32 stages: columns
+    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (28, 2, 0)
+    assert p.workspace_bytes == 0
+    p = plan("f16", 4096, 4096, 6016)              # 47 stages: columns
+    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (28, 2, 0)
+    p = plan("bf16", 8192, 8192, 8192)             # 1024 tiles = 13 x 76 + 36
+    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (36, 2, 1)
+    p = plan("f16", 8192, 4096, 8192)              # 512 tiles = 6 x 76 + 56: too many
+    assert p.split_in_k == 0
