@@ -32,7 +32,7 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
-            "gemm_host_blocks", "gemm_host_k_blocks")
+            "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -105,6 +105,8 @@ def load() -> ctypes.CDLL:
     lib.gemm_smem_layout_offset.argtypes = [i, i, i]
     lib.gemm_selftest_timeout.restype = i
     lib.gemm_selftest_timeout.argtypes = [ctypes.c_uint, vp]
+    lib.gemm_selftest_flag_timeout.restype = i
+    lib.gemm_selftest_flag_timeout.argtypes = [ctypes.c_uint, vp]
     _lib = lib
     return lib
 
@@ -178,6 +180,10 @@ def gemm_smem_layout_offset(layout: int, row: int, col: int) -> int:
 
 def gemm_selftest_timeout(timeout_us: int, stream=0) -> int:
     return load().gemm_selftest_timeout(timeout_us, stream)
+
+
+def gemm_selftest_flag_timeout(timeout_us: int, stream=0) -> int:
+    return load().gemm_selftest_flag_timeout(timeout_us, stream)
 
 def gemm_plan_op(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms=152):
     """Returns (status, Plan) of a call with operand storages."""

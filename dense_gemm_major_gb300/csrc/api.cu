@@ -881,4 +881,16 @@ gemm_status_t gemm_selftest_timeout(unsigned timeout_us, cudaStream_t stream) {
   return GEMM_OK;
 }
 
+gemm_status_t gemm_selftest_flag_timeout(unsigned timeout_us, cudaStream_t stream) {
+  DeviceInfo* dev = nullptr;
+  gemm_status_t st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  if (dgemm::launch_selftest_flag_timeout(dev->fault, (unsigned long long)timeout_us * 1000ull,
+                                          stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
 }  // extern "C"

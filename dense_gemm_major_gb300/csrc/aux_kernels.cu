@@ -23,6 +23,16 @@ __global__ void selftest_timeout_kernel(unsigned* fault, unsigned long long time
   if (!mbar_wait_bounded(b, 0, timeout_ns, nullptr)) raise_fault(fault, kFaultSelftestWait);
 }
 
+// One thread waits for a global flag that nothing sets (the K-split
+// hand-over's wait); it gives up after timeout_ns and records
+// kFaultTcPartialWait.
+__device__ unsigned g_selftest_flag;   // stays 0
+__global__ void selftest_flag_kernel(unsigned* fault, unsigned long long timeout_ns) {
+  if (threadIdx.x != 0) return;
+  if (!flag_wait_equal(&g_selftest_flag, 1u, timeout_ns, nullptr))
+    raise_fault(fault, kFaultTcPartialWait);
+}
+
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
 template <>
@@ -169,6 +179,12 @@ cudaError_t launch_transpose_f32(const float* S, long long rows, long long cols,
   if (blocks > tiles) blocks = tiles;
   if (blocks < 1) blocks = 1;
   transpose_f32_kernel<<<(unsigned)blocks, kTrThreads, 0, stream>>>(S, rows, cols, lds, D, ldd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_flag_timeout(unsigned* fault, unsigned long long timeout_ns,
+                                         cudaStream_t stream) {
+  selftest_flag_kernel<<<1, 32, 0, stream>>>(fault, timeout_ns);
   return cudaGetLastError();
 }
 

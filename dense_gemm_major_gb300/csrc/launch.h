@@ -338,5 +338,9 @@ cudaError_t launch_gemm_kernel(void (*kernel)(Params...), dim3 grid, dim3 block,
 // wait gives up, records kFaultSelftestWait and the kernel returns.
 cudaError_t launch_selftest_timeout(unsigned* fault, unsigned long long timeout_ns,
                                     cudaStream_t stream);
+// Waits on a global flag that nothing sets (the K-split hand-over's wait)
+// with a `timeout_ns` bound; records kFaultTcPartialWait and returns.
+cudaError_t launch_selftest_flag_timeout(unsigned* fault, unsigned long long timeout_ns,
+                                         cudaStream_t stream);
 
 }  // namespace dgemm

@@ -352,6 +352,13 @@ int gemm_smem_layout_offset(int layout, int row, int col);
  * the context stays usable.
  */
 gemm_status_t gemm_selftest_timeout(unsigned timeout_us, cudaStream_t stream);
+/*
+ * The same for the other kind of wait: one thread polls a global flag that
+ * nothing sets (the wait with which the FP16/BF16 pair kernel hands an FP32
+ * partial from one K piece to the other), bounded by `timeout_us`; the
+ * fault word then has bit 7 (partial never arrived) set.
+ */
+gemm_status_t gemm_selftest_flag_timeout(unsigned timeout_us, cudaStream_t stream);
 
 #if defined(__cplusplus)
 }

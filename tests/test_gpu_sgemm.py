@@ -135,6 +135,17 @@ def test_bounded_wait_self_test_reports_timeout(dg):
     _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)
 
 
+def test_bounded_flag_wait_self_test_reports_timeout(dg):
+    # The K-split hand-over's flag wait, on a flag nothing sets.
+    stream = torch.cuda.current_stream().cuda_stream
+    assert dg.gemm_selftest_flag_timeout(20000, stream) == dg.GEMM_OK
+    st, bits = dg.gemm_device_check(stream)
+    assert st == dg.GEMM_ERR_DEVICE_TIMEOUT and bits & (1 << 7)
+    st, bits = dg.gemm_device_check(stream)
+    assert st == dg.GEMM_OK and bits == 0
+    _run_workload(dg, workloads.WORKLOADS["f32_256_int"], exact=True)
+
+
 # Hybrid stream-K schedules: whole-tile waves, then equal k-tile ranges per
 # CTA; a range boundary inside a tile cuts it into two pieces that add into
 # zeroed C (beta = 0) or meet in the tail workspace (beta != 0).  C starts as
