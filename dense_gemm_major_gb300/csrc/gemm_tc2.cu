@@ -339,8 +339,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         if (chunks > 1)
           load_old_row64<T>(old[1], c_in, p.ldc, p.M, p.N, row0 + lane, col0 + kTcEpiCols);
       }
-      if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
-      tc_fence_after();
       if (finish) {
         // Piece 0's partial: chunk 0 into this warp's staging buffers (free
         // once its earlier stores have read them), chunks 1.. into the ring,
