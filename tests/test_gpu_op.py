@@ -252,3 +252,22 @@ def test_sgemm_packed_and_transposed_staging(dg, op_a, op_b, shape, pad, packed)
     C2 = torch.full((M, N), float("nan"), device="cuda")
     _call(dg, "f32", op_a, op_b, A_st, B_st, C2, M, N, K)
     assert torch.equal(C, C2)
+
+
+@pytest.mark.parametrize("op_a,op_b", OPS)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_op_pair_k_split_scaled(dg, dtype, op_a, op_b):
+    # The pair kernel's K split of the last round (48+ stages of K, 28
+    # leftover tiles) with operands stored transposed and alpha / beta.
+    M, N, K = 4096, 4096, 6144
+    st, plan = dg.gemm_plan_op(dtype, op_a, op_b, M, N, K, 0.5, 1 << 40,
+                               K if op_a == "N" else M, 1 << 41, N if op_b == "N" else K, 2.0,
+                               1 << 42, N, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert st == dg.GEMM_OK and plan.split_in_k == 1
+    A, B = _inputs(dtype, M, N, K, 131, "normal")
+    C_in = (torch.rand((M, N), generator=torch.Generator().manual_seed(132)) * 2 - 1).to(A.dtype)
+    C = C_in.cuda()
+    A_st, B_st = _stored(A, op_a), _stored(B, op_b)
+    _call(dg, dtype, op_a, op_b, A_st, B_st, C, M, N, K, alpha=0.5, beta=2.0)
+    _check(dtype, op_a, op_b, A_st, B_st, C, rows=workloads.sample_rows(M, 32, seed=133),
+           alpha=0.5, beta=2.0, C_in=C_in)
