@@ -177,3 +177,16 @@ def test_matmul_on_cpu_tensors(dg):
             assert err <= TOL[dtype], (dtype, pin, err)
     with pytest.raises(ValueError):
         dg.matmul(torch.ones(4, 4), torch.ones(4, 4, device="cuda"))
+
+
+def test_host_k_blocks_scaled_transposed(dg):
+    # FP32, both operands stored transposed, alpha / beta: two row blocks x
+    # two ranges of K, the second range adding onto the first's C.
+    M, N, K = 4096, 2304, 4096
+    assert dg.gemm_host_k_blocks("f32", M, N, K) == 2
+    A, B = workloads.make(workloads.Workload("host_kb", "f32", M, N, K, "uniform", 141, -2, 2))
+    C_in = torch.rand((M, N), generator=torch.Generator().manual_seed(142)) * 2 - 1
+    A_st, B_st = _host(A.t().contiguous(), 3), _host(B.t().contiguous(), 1)
+    C = _host(C_in.clone(), 2)
+    _run(dg, "f32", "T", "T", A_st, B_st, C, M, N, K, alpha=-0.75, beta=1.5)
+    _check("f32", "T", "T", A_st, B_st, C, _rows(M, 2), alpha=-0.75, beta=1.5, C_in=C_in)
