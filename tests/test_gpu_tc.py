@@ -243,7 +243,8 @@ def test_dependent_chain_without_sync(dg, dtype, shapes):
 
 @pytest.mark.parametrize("dtype,shape", [("f16", (4096, 4096, 8192)),     # 28 leftover tiles
                                          ("bf16", (1280, 4864, 6144)),    # 19 leftover tiles
-                                         ("f16", (4096, 2816, 6200))])    # ragged K
+                                         ("f16", (4096, 2816, 6200)),     # ragged K
+                                         ("bf16", (4000, 4000, 6144))])   # ragged M and N
 def test_pair_k_split_last_round(dg, dtype, shape):
     # The pair kernel's last partial round as two full-width K pieces: the
     # first hands its FP32 partial to the second through the workspace and
@@ -255,7 +256,7 @@ def test_pair_k_split_last_round(dg, dtype, shape):
     w = workloads.Workload(f"{dtype}_ksplit", dtype, M, N, K, "normal", 73)
     A, B = workloads.make(w)
     C = run_gemm(dg, A.cuda(), B.cuda())
-    rows = sorted({r for t in range(0, M, 256) for r in (t, t + 127, t + 128, min(t + 255, M - 1))})
+    rows = sorted({min(r, M - 1) for t in range(0, M, 256) for r in (t, t + 127, t + 128, t + 255)})
     compare(dtype, A, B, C, rows=np.asarray(rows))
     # the same call again reuses the workspace and the flags (next epoch)
     C2 = run_gemm(dg, A.cuda(), B.cuda())
