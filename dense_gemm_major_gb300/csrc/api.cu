@@ -283,7 +283,8 @@ int forced_sgemm_tn() {
 // (share 1), a smaller one fills tiles / slots (twice that when it runs as
 // two k-halves per tile).  Relative speeds measured on GB300 at 4096^3 and
 // 8192 x 8192 x 4096: wide 1.00, narrow/1 0.96, narrow/2 0.95.
-int sgemm_pick_tn(int M, int N, int K, int sms) {
+int sgemm_pick_tn(int M, int N, int K, int sms, double* score_out = nullptr) {
+  if (score_out != nullptr) *score_out = 1.0;
   if (const int forced = forced_sgemm_tn()) return forced;
   const int nk = ceil_div(K, dgemm::kSgemmBK);
   struct Cfg {
@@ -310,8 +311,17 @@ int sgemm_pick_tn(int M, int N, int K, int sms) {
       best = c.tn;
     }
   }
+  if (score_out != nullptr) *score_out = best_score;
   return best;
 }
+
+// Below this score of the best whole-K configuration (sgemm_pick_tn), an
+// FP32 grid runs as split-K.  Measured on GB300: 1024^3 as two k-halves per
+// narrow tile (score 0.81) 55.8 us against 60.4 us as 4 slices; 1000 x 1030
+// x 777 (0.91) 59.7 against 67.8 us; 1024 x 2048 x 2048 (0.84, wide) 168
+// against 186 us; but 768 x 768 x 4096 (0.45) 101 us as 8 slices against
+// 178 us.
+constexpr double kSgemmSplitkBelowScore = 0.6;
 
 // FP32 plan of the problem as the SGEMM kernel sees it (M x N output, A and
 // B with storage ops op_a / op_b, a16 / b16: base and leading dimension
@@ -329,10 +339,13 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
     plan->path = GEMM_PATH_SIMT_CPASYNC;
   const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
   const int nk_all = ceil_div(K, dgemm::kSgemmBK);
-  // A grid of narrow tiles that fills at most half of the CTA slots runs
-  // as split-K (k-slices into a workspace, then a reduction).
-  const int slices = forced_sgemm_tn() ? 1
-                                       : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
+  // A grid that no whole-K configuration keeps busy enough runs as split-K
+  // (k-slices of narrow tiles into a workspace, then a reduction).
+  double best_score = 1.0;
+  sgemm_pick_tn(M, N, K, sms, &best_score);
+  const int slices = forced_sgemm_tn() || best_score >= kSgemmSplitkBelowScore
+                         ? 1
+                         : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
   if (slices > 1) {
     plan->block_m = dgemm::kSgemmBM;
     plan->block_n = dgemm::sgemm_bn(8);

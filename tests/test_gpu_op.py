@@ -78,7 +78,8 @@ SHAPES = [
     ("f32", (1, 8, 8)),            # one narrow tile, one k-tile
     ("f32", (129, 264, 72)),       # ragged in every dimension
     ("f32", (300, 520, 64)),       # narrow tiles
-    ("f32", (1000, 1030, 777)),    # split-K
+    ("f32", (1000, 1030, 777)),    # two k-halves per narrow tile
+    ("f32", (768, 768, 4096)),     # split-K
     ("f32", (2048, 2048, 256)),    # wide tiles, last partial wave in k-halves
     ("f16", (129, 264, 72)),       # ragged single-CTA tile
     ("bf16", (1000, 2000, 504)),   # single CTAs, column parts

@@ -187,11 +187,16 @@ def test_plan_paths():
     ok, p = dg.gemm_plan("f32", 1000, 1030, 777, FAKE, 777, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_CPASYNC
-    # 72 tiles fill less than half of the 304 slots: split-K, 4 slices of
-    # 6-7 k-tiles each into a 4 x 1000 x 1032 FP32 workspace
-    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 0
-    assert (p.splitk_slices, p.ctas) == (4, 288)
-    assert p.workspace_bytes == 4 * 1000 * 1032 * 4
+    # 72 narrow tiles as two k-halves each keep 144 of the 152 SMs busy
+    # (score 0.91): no split-K; every tile is cut once, no workspace
+    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 72
+    assert (p.splitk_slices, p.ctas, p.workspace_bytes) == (1, 144, 0)
+    # 36 narrow tiles over K = 4096 (best whole-K score 0.45): split-K, 8
+    # slices of 16 k-tiles into an 8 x 768 x 768 FP32 workspace
+    ok, p = dg.gemm_plan("f32", 768, 768, 4096, FAKE, 4096, FAKE + (1 << 30), 768,
+                         FAKE + (2 << 30), 768)
+    assert (p.tiles, p.splitk_slices, p.ctas) == (36, 8, 288)
+    assert p.workspace_bytes == 8 * 768 * 768 * 4
     # misaligned base pointer (4-byte aligned only)
     ok, p = dg.gemm_plan("f32", 64, 64, 64, FAKE + 4, 64, FAKE + (1 << 30), 64,
                          FAKE + (2 << 30), 64)

@@ -50,9 +50,9 @@ def test_noalloc_matches_gemm_f32_on_two_calls(shape):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
-    # 150 tiles -> 2 k-slices of 1280 x 1920 FP32 = 19.7 MB > 16 MiB
+    # 36 tiles -> 8 k-slices of 768 x 768 FP32 = 18.9 MB > 16 MiB
     dg = gpu_lib()
-    M, N, K = 1280, 1920, 4096
+    M, N, K = 768, 768, 4096
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     _, plan = dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)
     assert plan.splitk_slices > 1 and plan.workspace_bytes > (16 << 20)
