@@ -189,7 +189,22 @@ extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, in
     return GEMM_ERR_LAUNCH;
 
   const int nb = gemm_host_blocks(dtype, M, N, sms);
+  // Row block i is rows [start(i), start(i + 1)), block boundaries whole
+  // 256-row units.  FP16 / BF16: equal blocks.  FP32 (two blocks): the last
+  // as small as still gives every SM a 128 x 256 tile, so the least of C is
+  // left to download after the last kernel (4096^2: 2816 + 1280 rows).
   const int rows = nb == 1 ? M : (int)round_up((M + nb - 1) / nb, kRowAlign);
+  int split = rows;   // FP32, two blocks: the first row of the second
+  if (dtype == 0 && nb == 2) {
+    const int tiles_n = (N + 255) / 256;
+    const long long need = round_up((long long)((sms + tiles_n - 1) / tiles_n) * 128, kRowAlign);
+    if (need < M - rows) split = (int)((M - need) / kRowAlign * kRowAlign);
+  }
+  const auto start = [&](int i) {
+    if (dtype == 0 && nb == 2) return i == 0 ? 0 : (i == 1 ? split : M);
+    const long long r = (long long)i * rows;
+    return r < M ? (int)r : M;
+  };
   const int nkb = reads_ab ? gemm_host_k_blocks(dtype, M, N, K) : 1;
   // The first range of K is the shorter one: only its share of A and B
   // has to arrive before the first kernel, and the first kernel still
@@ -214,8 +229,8 @@ extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, in
       !ok(cudaStreamWaitEvent(h->down, h->start, 0)))
     return GEMM_ERR_LAUNCH;
   for (int i = 0; i < nb; ++i) {
-    const int r0 = i * rows;
-    const int m = (M - r0) < rows ? (M - r0) : rows;
+    const int r0 = start(i);
+    const int m = start(i + 1) - r0;
     unsigned char* c_dev = dc + (size_t)r0 * dlc * es;
     unsigned char* c_host = hc + (size_t)r0 * ldc * es;
     for (int j = 0; j < nkb; ++j) {

@@ -61,11 +61,10 @@ def _check(dtype, op_a, op_b, A_st, B_st, C, rows, alpha=1.0, beta=0.0, C_in=Non
 
 
 def _rows(M, blocks):
-    """Sampled rows: both sides of every block boundary, the ends, random."""
-    step = -(-M // blocks) if blocks > 1 else M
-    step = -(-step // 256) * 256
+    """Sampled rows: both sides of every 256-row boundary (every possible
+    block boundary), the ends, random."""
     fixed = {0, M - 1}
-    for r in range(step, M, step):
+    for r in range(256, M, 256):
         fixed.update({r - 1, r})
     rng = np.random.default_rng(M)
     fixed.update(int(x) for x in rng.integers(0, M, 24))
