@@ -32,7 +32,8 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_plan", "gemm_smem_layout_offset", "gemm_selftest_timeout", "gemm_f32_noalloc",
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
-            "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout")
+            "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout",
+            "gemm_plan_resident", "gemm_pair_clusters")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -89,6 +90,11 @@ def load() -> ctypes.CDLL:
     lib.gemm_plan_op.restype = i
     lib.gemm_plan_op.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, i,
                                  ctypes.POINTER(Plan)]
+    lib.gemm_plan_resident.restype = i
+    lib.gemm_plan_resident.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, i, i,
+                                       ctypes.POINTER(Plan)]
+    lib.gemm_pair_clusters.restype = i
+    lib.gemm_pair_clusters.argtypes = []
     lib.gemm_host.restype = i
     lib.gemm_host.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     lib.gemm_host_blocks.restype = i
@@ -194,6 +200,22 @@ def gemm_plan_op(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc
     return st, plan
 
 
+def gemm_plan_resident(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                       num_sms=152, pair_clusters=0):
+    """Returns (status, Plan) for a device holding only `pair_clusters` CTA
+    pairs at once (0: every SM)."""
+    plan = Plan()
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    st = load().gemm_plan_resident(code, _OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A,
+                                   lda, B, ldb, beta, C, ldc, num_sms, pair_clusters,
+                                   ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_pair_clusters() -> int:
+    return load().gemm_pair_clusters()
+
+
 def gemm_f32_op(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:
     return load().gemm_f32_op(_OP_CODES[op_a], _OP_CODES[op_b], M, N, K, alpha, A, lda, B, ldb,
                               beta, C, ldc, stream)
@@ -281,7 +303,8 @@ def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
     row-major.  Row-padded views (row stride > width) are accepted; beta != 0
     needs ``out``.  CUDA tensors run on the device as queued work; CPU
     tensors (page-locked or not) go through gemm_host, which stages them on
-    the GPU, and the call returns once out holds the result."""
+    the GPU, and the call returns once out holds the result (raising
+    GemmError if a device-side wait gave up on the way)."""
     import torch
     on_host = A.device.type == "cpu" and B.device.type == "cpu"
     if not on_host and (A.device.type != "cuda" or B.device.type != "cuda"):
@@ -309,7 +332,11 @@ def matmul(A, B, out=None, stream=None, alpha=1.0, beta=0.0):
                        ldb, float(beta), out.data_ptr(), _ld(out, M, N), stream)
         if st != GEMM_OK:
             raise GemmError(st, "gemm_host")
-        torch.cuda.synchronize()
+        # Waits for the result and reads the device fault word: a bounded
+        # device wait that gave up means out does not hold the product.
+        st, bits = gemm_device_check(stream)
+        if st != GEMM_OK:
+            raise GemmError(st, f"gemm_host (fault bits {bits:#x})")
         return out
     if op_a == OP_N and op_b == OP_N and alpha == 1.0 and beta == 0.0:
         st = gemm(code, M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,

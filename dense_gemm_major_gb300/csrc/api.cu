@@ -35,6 +35,9 @@ struct DeviceInfo {
   bool probed = false;
   bool supported = false;
   int sms = 0;
+  // 2-CTA clusters of the pair kernel that fit on the device at once
+  // (cudaOccupancyMaxActiveClusters; 0 if the query failed).
+  int pair_clusters = 0;
   unsigned* fault = nullptr;  // device address of g_fault_word
 };
 
@@ -153,6 +156,7 @@ gemm_status_t current_device(DeviceInfo** out) {
       d.supported = false;
     }
     d.fault = static_cast<unsigned*>(addr);
+    if (d.supported) d.pair_clusters = dgemm::tc_pair_resident_clusters();
   }
   if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
   *out = &d;
@@ -394,9 +398,11 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   return GEMM_OK;
 }
 
+// pair_clusters: CTA pairs of the pair kernel that can be resident at once
+// (0: num_sms / 2, every SM).
 gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
                         const void* A, int lda, const void* B, int ldb, float beta, const void* C,
-                        int ldc, int num_sms, gemm_plan_t* plan) {
+                        int ldc, int num_sms, int pair_clusters, gemm_plan_t* plan) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
@@ -474,7 +480,14 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   // pair kernel was measured 1.06-1.17x faster (2048^3: 21.2 vs 22.6 us;
   // 2048 x 2048 x 8192: 54.3 vs 63.5 us), so it wins unless
   // 1.15 x its busy SMs < the single kernel's.
-  const int pairs = sms / 2;
+  // The pair grid is persistent: at most as many pairs as fit at once.  A
+  // hand-over of FP32 partials between pairs (the K split) polls for a
+  // partial that another pair computes, so it needs every pair of the grid
+  // resident together; when fewer clusters than sms / 2 fit (a GPU shared
+  // with other work, or partitioned), it is not used.
+  const int all_pairs = sms / 2;
+  const int pairs = pair_clusters > 0 && pair_clusters < all_pairs ? pair_clusters : all_pairs;
+  const bool handover = pair_clusters <= 0 || pair_clusters >= all_pairs;
   const int pair_tiles = ceil_div(M, 2 * dgemm::kTc2BM) * ceil_div(N, dgemm::kTc2BN);
   const int forced = forced_tc_kernel();
   const auto single_busy = [&]() {
@@ -491,7 +504,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   // The pair kernel's last partial round: K ranges when K is long enough,
   // else column parts.
   const auto pair_split = [&]() {
-    const dgemm::TcSplit ks = tc_ksplit_disabled()
+    const dgemm::TcSplit ks = (tc_ksplit_disabled() || !handover)
                                   ? dgemm::TcSplit{0, 1}
                                   : dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair);
     return ks.split_tiles ? ks : dgemm::tc_pair_split(pair_tiles, pairs);
@@ -514,7 +527,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
     plan->split_tiles = sp.split_tiles;
     plan->split_pieces = sp.parts;
-    plan->split_in_k = sp.split_tiles > 0 && !tc_ksplit_disabled() &&
+    plan->split_in_k = sp.split_tiles > 0 && !tc_ksplit_disabled() && handover &&
                        dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair).split_tiles > 0;
     if (plan->split_in_k)
       plan->workspace_bytes = (long long)sp.split_tiles * (sp.parts - 1) * 2 * dgemm::kTc2BM *
@@ -565,7 +578,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
                   cudaStream_t stream) {
   gemm_plan_t plan;
   gemm_status_t st =
-      plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, &plan);
+      plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, 0, &plan);
   if (st != GEMM_OK) return st;
   if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
   DeviceInfo* dev = nullptr;
@@ -573,7 +586,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
   if (st != GEMM_OK) return st;
   // Re-plan with the device's SM count (validation above needs no device).
   st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms,
-                 &plan);
+                 dev->pair_clusters, &plan);
   if (st != GEMM_OK) return st;
   cudaError_t e = cudaSuccess;
 
@@ -852,21 +865,36 @@ gemm_status_t gemm_device_check(cudaStream_t stream, unsigned* fault_bits) {
 gemm_status_t gemm_plan(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
                         int ldb, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
   return plan_impl(dtype, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc,
-                   num_sms, plan);
+                   num_sms, 0, plan);
 }
 
 gemm_status_t gemm_plan_ex(int dtype, int M, int N, int K, float alpha, const void* A, int lda,
                            const void* B, int ldb, float beta, const void* C, int ldc,
                            int num_sms, gemm_plan_t* plan) {
   return plan_impl(dtype, GEMM_OP_N, GEMM_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                   num_sms, plan);
+                   num_sms, 0, plan);
 }
 
 gemm_status_t gemm_plan_op(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
                            float alpha, const void* A, int lda, const void* B, int ldb,
                            float beta, const void* C, int ldc, int num_sms, gemm_plan_t* plan) {
-  return plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms,
+  return plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms, 0,
                    plan);
+}
+
+gemm_status_t gemm_plan_resident(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
+                                 float alpha, const void* A, int lda, const void* B, int ldb,
+                                 float beta, const void* C, int ldc, int num_sms,
+                                 int pair_clusters, gemm_plan_t* plan) {
+  if (pair_clusters < 0) return GEMM_ERR_INVALID_ARG;
+  return plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms,
+                   pair_clusters, plan);
+}
+
+int gemm_pair_clusters(void) {
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != GEMM_OK) return -1;
+  return dev->pair_clusters;
 }
 
 int gemm_smem_layout_offset(int layout, int row, int col) {

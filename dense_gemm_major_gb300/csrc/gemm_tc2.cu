@@ -78,19 +78,6 @@ struct alignas(8) Barriers {
   int abort;
 };
 
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi);
-template <>
-__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <>
-__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // Work unit u of the pair-persistent grid: 256 x 256 tile (tm, tn), the
 // columns [n_off, n_off + n_w) of it (all 256, or one of two 128-column
 // parts of a tile of the last partial round) and the k-tiles [kb, ke).
@@ -517,6 +504,27 @@ cudaError_t launch_ops(const TcParams& p, const CUtensorMap* tmA, const CUtensor
 }  // namespace
 
 static_assert(sizeof(Barriers) <= 256, "barrier block must fit its reserved space");
+
+int tc_pair_resident_clusters() {
+  // Every instance has the same block size and shared memory, so one
+  // stands for all.
+  const auto kernel = gemm_tc_pair_kernel<__half, 0, false, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTc2SmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTc2SmemBytes;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
 
 cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap* tmA,
                                 const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,

@@ -262,6 +262,11 @@ inline TcSplit tc_pair_ksplit(int tiles, int pairs, int nk) {
   return sp;
 }
 
+// 2-CTA clusters of the pair kernel (its shared memory and block size) that
+// the current device can hold at once (cudaOccupancyMaxActiveClusters), or 0
+// if the query fails.
+int tc_pair_resident_clusters();
+
 // tiles_m / tiles_n in p count 256 x 256 tiles; grid = 2 * pairs CTAs.
 cudaError_t launch_gemm_tc_pair(int dtype, const TcParams& p, const CUtensorMap* tmA,
                                 const CUtensorMap* tmB, const CUtensorMap* tmC, int pairs,

@@ -332,6 +332,25 @@ gemm_status_t gemm_plan_op(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int
                            float beta, const void *C, int ldc, int num_sms, gemm_plan_t *plan);
 
 /*
+ * As gemm_plan_op, for a device on which only `pair_clusters` CTA pairs of
+ * the FP16/BF16 pair kernel can be resident at once (0: num_sms / 2, every
+ * SM; negative: GEMM_ERR_INVALID_ARG).  The pair kernel runs a persistent
+ * grid of at most that many pairs.  Its K split hands an FP32 partial from
+ * one pair to another, and the receiving pair polls for it; that needs
+ * every pair of the grid resident together, so with fewer pairs than
+ * num_sms / 2 the split is not planned.  The dispatcher plans with the
+ * count cudaOccupancyMaxActiveClusters gives for the current device.
+ */
+gemm_status_t gemm_plan_resident(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N, int K,
+                                 float alpha, const void *A, int lda, const void *B, int ldb,
+                                 float beta, const void *C, int ldc, int num_sms,
+                                 int pair_clusters, gemm_plan_t *plan);
+/* The resident-pair count the dispatcher uses for the current device (its
+ * first call on a device queries it), 0 if the query failed, -1 if there is
+ * no supported device. */
+int gemm_pair_clusters(void);
+
+/*
  * Shared-memory layout of the kernels' operand tiles, as an element offset
  * inside one stage (for host-side bank-conflict and bijectivity checks of
  * the swizzle; wingedge777 section 4 derives its SWIZZLE_A the same way).

@@ -140,9 +140,11 @@ def test_host_calls_keep_stream_order(dg):
     assert dg.gemm_host("f32", "N", "N", M, N, N, 1.0, C1.data_ptr(), N, B2_h.data_ptr(), N,
                         0.0, C2.data_ptr(), N, s) == dg.GEMM_OK
     torch.cuda.synchronize()
-    ref1 = A.double() @ B.double()
-    ref2 = ref1 @ B2.double()          # all partial sums are exact in FP32
-    assert torch.equal(C1.double(), ref1) and torch.equal(C2.double(), ref2)
+    # Every partial sum is an integer below 2^24, so both products are exact
+    # in FP32 and the oracle's sums are the expected values bit for bit.
+    ref1, _ = oracle.gemm("f32", A.numpy(), B.numpy(), with_scale=False)
+    ref2, _ = oracle.gemm("f32", ref1.astype(np.float32), B2.numpy(), with_scale=False)
+    assert np.array_equal(C1.double().numpy(), ref1) and np.array_equal(C2.double().numpy(), ref2)
 
 
 def test_host_degenerate(dg):
@@ -170,12 +172,29 @@ def test_matmul_on_cpu_tensors(dg):
             Yh = Y.pin_memory() if pin else Y
             out = dg.matmul(Xh.t(), Yh.t())                 # (520 x 700) @ (700 x 390)
             assert out.device.type == "cpu" and out.shape == (520, 390)
-            ref = X.t().double() @ Y.t().double()
-            scale = X.t().double().abs() @ Y.t().double().abs()
-            err = ((out.double() - ref).abs() / scale).max().item()
-            assert err <= TOL[dtype], (dtype, pin, err)
+            # X holds A stored transposed (K x M), Y holds B stored N x K.
+            ref, S = oracle.gemm(dtype, workloads.to_numpy_bits(X),
+                                 workloads.to_numpy_bits(Y), op_a="T", op_b="T")
+            err, idx, bad_zero = oracle.normalized_error(out.double().numpy(), ref, S)
+            assert bad_zero == 0 and err <= TOL[dtype], (dtype, pin, err, idx)
     with pytest.raises(ValueError):
         dg.matmul(torch.ones(4, 4), torch.ones(4, 4, device="cuda"))
+
+
+def test_matmul_on_cpu_tensors_reports_a_device_fault(dg):
+    # A bounded device wait that gave up before the call (here the flag-wait
+    # self-test, queued on the same stream) is read from the fault word when
+    # matmul() waits for its result: the call raises instead of returning.
+    s = torch.cuda.current_stream().cuda_stream
+    assert dg.gemm_selftest_flag_timeout(20000, s) == dg.GEMM_OK
+    with pytest.raises(dg.GemmError) as err:
+        dg.matmul(torch.ones(64, 32), torch.ones(32, 48))
+    assert err.value.status == dg.GEMM_ERR_DEVICE_TIMEOUT
+    # The word was cleared; the next call succeeds.
+    out = dg.matmul(torch.ones(64, 32), torch.ones(32, 48))
+    assert torch.all(out == 32.0)
+    st, bits = dg.gemm_device_check(s)
+    assert st == dg.GEMM_OK and bits == 0
 
 
 def test_host_k_blocks_scaled_transposed(dg):

@@ -189,10 +189,12 @@ def test_matmul_reads_transposed_views(dg):
         Y = (torch.rand(640, 512, generator=torch.Generator().manual_seed(6)) - 0.5).to(tdt).cuda()
         out_t = dg.matmul(X.t(), Y.t())                 # (384 x 512) @ (512 x 640)
         out_r = dg.matmul(X.t().contiguous(), Y.t().contiguous())
-        ref = X.t().double() @ Y.t().double()
-        scale = X.t().double().abs() @ Y.t().double().abs()
-        err = ((out_t.double() - ref).abs() / scale).max().item()
-        assert err <= TOL[dtype], (dtype, err)
+        # X holds A stored transposed (K x M), Y holds B stored N x K.
+        ref, S = oracle.gemm(dtype, workloads.to_numpy_bits(X), workloads.to_numpy_bits(Y),
+                             op_a="T", op_b="T")
+        got = out_t.float().cpu().numpy().astype(np.float64)
+        err, idx, bad_zero = oracle.normalized_error(got, ref, S)
+        assert bad_zero == 0 and err <= TOL[dtype], (dtype, err, idx)
         if dtype == "f32":
             assert torch.equal(out_t, out_r)
 

@@ -633,3 +633,27 @@ def test_pair_last_round_k_split_plans():
     assert (p.split_tiles, p.split_pieces, p.split_in_k) == (36, 2, 1)
     p = plan("f16", 8192, 4096, 8192)              # 512 tiles = 6 x 76 + 56: too many
     assert p.split_in_k == 0
+
+
+def test_pair_plan_with_fewer_resident_clusters():
+    # A device that holds fewer CTA pairs at once than num_sms / 2 (shared
+    # or partitioned): the persistent pair grid shrinks to what fits, and no
+    # pair is left polling for a partial from another pair.
+    def plan(dt, M, N, K, clusters):
+        st, p = dg.gemm_plan_resident(dt, "N", "N", M, N, K, 1.0, FAKE, K, FAKE + (1 << 34), N,
+                                      0.0, FAKE + (1 << 36), N, 152, clusters)
+        assert st == dg.GEMM_OK
+        return p
+    full = plan("f16", 4096, 4096, 8192, 0)
+    assert (full.cluster_ctas, full.split_in_k, full.ctas) == (2, 1, 152)
+    same = plan("f16", 4096, 4096, 8192, 76)       # every pair fits: as planned
+    assert (same.split_in_k, same.ctas, same.workspace_bytes) == \
+        (1, 152, full.workspace_bytes)
+    more = plan("f16", 4096, 4096, 8192, 80)       # more than the SMs allow: as planned
+    assert (more.split_in_k, more.ctas) == (1, 152)
+    few = plan("f16", 4096, 4096, 8192, 72)        # 144 of 152 SMs
+    assert (few.cluster_ctas, few.split_in_k, few.ctas, few.workspace_bytes) == (2, 0, 144, 0)
+    few = plan("bf16", 8192, 8192, 8192, 60)        # 120 of 152: single CTAs keep more busy
+    assert (few.cluster_ctas, few.split_in_k, few.ctas) == (1, 0, 152)
+    assert dg.gemm_plan_resident("f16", "N", "N", 64, 64, 64, 1.0, FAKE, 64, FAKE + 8192, 64,
+                                 0.0, FAKE + 16384, 64, 152, -1)[0] == dg.GEMM_ERR_INVALID_ARG
