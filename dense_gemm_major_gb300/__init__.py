@@ -33,7 +33,7 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
             "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout",
-            "gemm_plan_resident", "gemm_pair_clusters")
+            "gemm_plan_resident", "gemm_pair_clusters", "gemm_pair_units")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -55,7 +55,8 @@ class Plan(ctypes.Structure):
                 ("split_tiles", ctypes.c_int), ("split_pieces", ctypes.c_int),
                 ("cluster_ctas", ctypes.c_int), ("splitk_slices", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_longlong), ("pack", ctypes.c_int),
-                ("pack_bytes", ctypes.c_longlong), ("split_in_k", ctypes.c_int)]
+                ("pack_bytes", ctypes.c_longlong), ("split_in_k", ctypes.c_int),
+                ("streamk_first_tile", ctypes.c_int)]
 
 
 _lib = None
@@ -93,6 +94,9 @@ def load() -> ctypes.CDLL:
     lib.gemm_plan_resident.restype = i
     lib.gemm_plan_resident.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, i, i,
                                        ctypes.POINTER(Plan)]
+    lib.gemm_pair_units.restype = i
+    lib.gemm_pair_units.argtypes = [ctypes.POINTER(Plan), i, i, i, i,
+                                    ctypes.POINTER(ctypes.c_int), i]
     lib.gemm_pair_clusters.restype = i
     lib.gemm_pair_clusters.argtypes = []
     lib.gemm_host.restype = i
@@ -210,6 +214,17 @@ def gemm_plan_resident(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, 
                                    lda, B, ldb, beta, C, ldc, num_sms, pair_clusters,
                                    ctypes.byref(plan))
     return st, plan
+
+
+def gemm_pair_units(plan, M, N, K, pair):
+    """The units CTA pair `pair` of a pair-kernel plan runs, in order, as
+    tuples (tm, tn, n_off, n_w, kb, ke, kind, slot)."""
+    n = load().gemm_pair_units(ctypes.byref(plan), M, N, K, pair, None, 0)
+    if n < 0:
+        raise ValueError("gemm_pair_units: not a CTA-pair plan or bad arguments")
+    buf = (ctypes.c_int * (8 * max(n, 1)))()
+    load().gemm_pair_units(ctypes.byref(plan), M, N, K, pair, buf, n)
+    return [tuple(buf[8 * j: 8 * j + 8]) for j in range(n)]
 
 
 def gemm_pair_clusters() -> int:

@@ -223,11 +223,12 @@ int forced_sgemm_pack() {
   return v;
 }
 
-// Measurement override: DENSE_GEMM_TC_KSPLIT=0 turns off the K split of the
-// pair kernel's last partial round (its column split then applies).
-bool tc_ksplit_disabled() {
+// Measurement override: DENSE_GEMM_TC_STREAMK=0 turns off the pair kernel's
+// stream-K share (its last partial round then runs as column parts, or as
+// it is).
+bool tc_streamk_disabled() {
   static const bool v = [] {
-    const char* s = std::getenv("DENSE_GEMM_TC_KSPLIT");
+    const char* s = std::getenv("DENSE_GEMM_TC_STREAMK");
     return s != nullptr && std::strcmp(s, "0") == 0;
   }();
   return v;
@@ -501,16 +502,15 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     return units < sms ? (int)units : sms;
   };
   const int nk_pair = ceil_div(K, dgemm::kTc2BK);
-  // The pair kernel's last partial round: K ranges when K is long enough,
-  // else column parts.
-  const auto pair_split = [&]() {
-    const dgemm::TcSplit ks = (tc_ksplit_disabled() || !handover)
-                                  ? dgemm::TcSplit{0, 1}
-                                  : dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair);
-    return ks.split_tiles ? ks : dgemm::tc_pair_split(pair_tiles, pairs);
-  };
+  // The pair kernel's tiles beyond whole rounds: a stream-K share of the
+  // last two rounds when K is long enough, else the last round's tiles as
+  // column parts when they fit it twice.
+  const int sk_first = (tc_streamk_disabled() || !handover)
+                           ? -1
+                           : dgemm::tc_pair_streamk_first(pair_tiles, pairs, nk_pair);
   const auto pair_busy = [&]() {
-    const dgemm::TcSplit sp = pair_split();
+    if (sk_first >= 0) return 2 * pairs;
+    const dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
     const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
     return 2 * (units < pairs ? units : pairs);
   };
@@ -523,18 +523,25 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     plan->block_k = dgemm::kTc2BK;
     plan->stages = dgemm::kTc2Stages;
     plan->tiles = pair_tiles;
-    dgemm::TcSplit sp = pair_split();
-    if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
-    plan->split_tiles = sp.split_tiles;
-    plan->split_pieces = sp.parts;
-    plan->split_in_k = sp.split_tiles > 0 && !tc_ksplit_disabled() && handover &&
-                       dgemm::tc_pair_ksplit(pair_tiles, pairs, nk_pair).split_tiles > 0;
-    if (plan->split_in_k)
-      plan->workspace_bytes = (long long)sp.split_tiles * (sp.parts - 1) * 2 * dgemm::kTc2BM *
-                              dgemm::kTc2BN * 4;
     plan->splitk_slices = 1;
-    const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
-    plan->ctas = 2 * (units < pairs ? units : pairs);
+    if (sk_first >= 0) {
+      // Cut tiles: a head on one pair, a tail on the next; one 256 x 256
+      // FP32 head partial per range boundary in the workspace.
+      plan->split_tiles = dgemm::tc_pair_streamk_cuts(pair_tiles - sk_first, pairs, nk_pair);
+      plan->split_pieces = plan->split_tiles ? 2 : 1;
+      plan->split_in_k = 1;
+      plan->streamk_first_tile = sk_first;
+      plan->workspace_bytes = (long long)pairs * 2 * dgemm::kTc2BM * dgemm::kTc2BN * 4;
+      plan->ctas = 2 * pairs;
+    } else {
+      dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
+      if (tc_split_disabled()) sp = dgemm::TcSplit{0, 1};
+      plan->split_tiles = sp.split_tiles;
+      plan->split_pieces = sp.parts;
+      plan->streamk_first_tile = -1;
+      const int units = pair_tiles + sp.split_tiles * (sp.parts - 1);
+      plan->ctas = 2 * (units < pairs ? units : pairs);
+    }
     plan->smem_bytes = dgemm::kTc2SmemBytes;
     return GEMM_OK;
   }
@@ -571,6 +578,27 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   plan->ctas = units < sms ? units : sms;
   plan->smem_bytes = dgemm::kTcSmemBytes;
   return GEMM_OK;
+}
+
+// The tile-schedule fields of TcParams for an FP16/BF16 plan (single CTAs
+// or pairs); the kernels and gemm_pair_units read them the same way.
+void tc_schedule_params(const gemm_plan_t& plan, int M, int N, dgemm::TcParams* p) {
+  p->tiles_m = ceil_div(M, plan.block_m);
+  p->tiles_n = ceil_div(N, plan.block_n);
+  p->group_m = tc_group_override() > 0 ? tc_group_override() : dgemm::kTcGroupM;
+  p->full_tiles = plan.tiles - plan.split_tiles;
+  p->split_tiles = plan.split_tiles;
+  p->parts = plan.split_pieces;
+  p->slices = plan.splitk_slices;
+  p->sk = 0;
+  if (plan.cluster_ctas == 2 && plan.split_in_k) {
+    p->sk = 1;
+    p->sk_first_tile = plan.streamk_first_tile;
+    p->sk_tiles = plan.tiles - plan.streamk_first_tile;
+    p->full_tiles = plan.tiles;
+    p->split_tiles = 0;
+    p->parts = 1;
+  }
 }
 
 gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alpha, const void* A,
@@ -703,13 +731,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.K = K;
     p.op_a = op_a;
     p.op_b = op_b;
-    p.tiles_m = ceil_div(M, plan.block_m);
-    p.tiles_n = ceil_div(N, plan.block_n);
-    p.group_m = tc_group_override() > 0 ? tc_group_override() : dgemm::kTcGroupM;
-    p.full_tiles = plan.tiles - plan.split_tiles;
-    p.split_tiles = plan.split_tiles;
-    p.parts = plan.split_pieces;
-    p.slices = plan.splitk_slices;
+    tc_schedule_params(plan, M, N, &p);
     p.ws = nullptr;
     p.ldw = ((long long)N + 3) / 4 * 4;
     if (p.slices > 1) {
@@ -722,14 +744,13 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.ldc = ldc;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
-    if (plan.split_in_k) {
-      // Partials of the K pieces before the last, and their flags.
-      p.ksplit = 1;
+    if (plan.cluster_ctas == 2 && plan.split_in_k) {
+      // Stream-K share: head partials and their flags, one per range
+      // boundary (boundary 0 is unused).
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.kpart);
       if (st != GEMM_OK) return st;
       float* flags = nullptr;
-      st = get_workspace(stream, (size_t)plan.split_tiles * (plan.split_pieces - 1) * 8 * 4,
-                         &flags, kWsFlags);
+      st = get_workspace(stream, (size_t)(plan.ctas / 2) * 8 * 4, &flags, kWsFlags);
       if (st != GEMM_OK) return st;
       p.kflag = reinterpret_cast<unsigned*>(flags);
       p.epoch = next_epoch(stream);
@@ -889,6 +910,24 @@ gemm_status_t gemm_plan_resident(int dtype, gemm_op_t op_a, gemm_op_t op_b, int 
   if (pair_clusters < 0) return GEMM_ERR_INVALID_ARG;
   return plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, num_sms,
                    pair_clusters, plan);
+}
+
+int gemm_pair_units(const gemm_plan_t* plan, int M, int N, int K, int pair, int* units,
+                    int max_units) {
+  if (plan == nullptr || plan->path != GEMM_PATH_TC_TMA || plan->cluster_ctas != 2 || M <= 0 ||
+      N <= 0 || K <= 0 || pair < 0 || pair >= plan->ctas / 2 || max_units < 0 ||
+      (max_units > 0 && units == nullptr))
+    return -1;
+  dgemm::TcParams p;
+  tc_schedule_params(*plan, M, N, &p);
+  const int nk = ceil_div(K, dgemm::kTc2BK);
+  const dgemm::TcPairSched s = dgemm::tc_pair_sched(pair, plan->ctas / 2, p, nk);
+  for (int j = 0; j < s.n && j < max_units; ++j) {
+    const dgemm::TcUnit w = dgemm::tc_pair_unit(s, j, plan->ctas / 2, p, nk);
+    const int v[8] = {w.tm, w.tn, w.n_off, w.n_w, w.kb, w.ke, w.kind, w.slot};
+    for (int i = 0; i < 8; ++i) units[8 * j + i] = v[i];
+  }
+  return s.n;
 }
 
 int gemm_pair_clusters(void) {

@@ -78,60 +78,16 @@ struct alignas(8) Barriers {
   int abort;
 };
 
-// Work unit u of the pair-persistent grid: 256 x 256 tile (tm, tn), the
-// columns [n_off, n_off + n_w) of it (all 256, or one of two 128-column
-// parts of a tile of the last partial round) and the k-tiles [kb, ke).
-// With the K split (p.ksplit) a last-round tile is instead two units over
-// all columns, piece 0 taking the first nk / 2 - kTc2KsplitLead k-tiles and
-// piece 1 the rest; slot is the tile's index among the split tiles.
-struct Unit {
-  int tm, tn, n_off, n_w, kb, ke;
-  int piece;   // -1: the whole K range; else the K piece, parts - 1 finishing
-  int slot;
-};
-__device__ __forceinline__ Unit unit_of(int u, const TcParams& p, int nk) {
-  Unit w;
-  int tile;
-  w.n_off = 0;
-  w.n_w = BN;
-  w.kb = 0;
-  w.ke = nk;
-  w.piece = -1;
-  w.slot = 0;
-  if (u < p.full_tiles) {
-    tile = u;
-  } else {
-    const int j = u - p.full_tiles;
-    tile = p.full_tiles + j / p.parts;
-    const int h = j % p.parts;
-    if (p.ksplit) {
-      // Two pieces: the first kTc2KsplitLead stages short of half of K.
-      const int cut = nk / 2 - kTc2KsplitLead;
-      w.kb = h == 0 ? 0 : cut;
-      w.ke = h == 0 ? cut : nk;
-      w.piece = h;
-      w.slot = j / p.parts;
-    } else {
-      w.n_w = BN / p.parts;
-      w.n_off = h * w.n_w;
-    }
-  }
-  grouped_tile(tile, p.tiles_m, p.tiles_n, p.group_m, w.tm, w.tn);
-  return w;
-}
-
-// The FP32 partial of K piece h (< parts - 1) of split slot `slot`, this CTA
-// (rank) and epilogue warp q: 32 rows x 256 columns, laid out so that lane
-// l's 16-byte store j of 64-column chunk c lands at ((c * 16 + j) * 32 + l)
-// x 4 floats from the block start (a warp's store is 512 contiguous bytes).
-__device__ __forceinline__ float* partial_block(const TcParams& p, int slot, int h, int rank,
-                                                int q) {
-  const long long blk = (((long long)slot * (p.parts - 1) + h) * 2 + rank) * 4 + q;
+// The FP32 head partial of boundary `slot`, CTA `rank`, epilogue warp q:
+// 32 rows x 256 columns, lane-major: the 16-byte group g (columns 4g ..
+// 4g + 3) of lane l's row lands at (g * 32 + l) x 4 floats from the block
+// start, so that a warp's store or load of one g is 512 contiguous bytes.
+__device__ __forceinline__ float* partial_block(const TcParams& p, int slot, int rank, int q) {
+  const long long blk = ((long long)slot * 2 + rank) * 4 + q;
   return p.kpart + blk * (32 * BN);
 }
-__device__ __forceinline__ unsigned* partial_flag(const TcParams& p, int slot, int h, int rank,
-                                                  int q) {
-  return p.kflag + ((((long long)slot * (p.parts - 1) + h) * 2 + rank) * 4 + q);
+__device__ __forceinline__ unsigned* partial_flag(const TcParams& p, int slot, int rank, int q) {
+  return p.kflag + (((long long)slot * 2 + rank) * 4 + q);
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcParams& p,
@@ -168,10 +124,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();     // 0: issues the MMAs
-  const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
-  const int num_units = p.full_tiles + p.split_tiles * p.parts;
   const int nk = (p.K + BK - 1) / BK;
+  const TcPairSched sched = tc_pair_sched(blockIdx.x >> 1, npairs, p, nk);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -214,8 +169,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------ TMA producer (both CTAs)
     uint32_t it = 0;
     bool ok = true;
-    for (int u = pair; u < num_units && ok; u += npairs) {
-      const Unit w = unit_of(u, p, nk);
+    for (int j = 0; j < sched.n && ok; ++j) {
+      const TcUnit w = tc_pair_unit(sched, j, npairs, p, nk);
       const int half = w.n_w / 2;          // columns of B this CTA stages
       const int boxes = half / 64;
       for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
@@ -228,25 +183,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           if (rank == 0)
             mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * (kABytes + boxes * kBBoxBytes));
           const uint32_t adst = smem_u32(sA + s * kABytes);
+          const uint32_t bdst = smem_u32(sB + s * kBBytes);
           const int m = w.tm * (2 * BM) + (int)rank * BM;
           for (int kb = 0; kb < kKBlocks; ++kb) {
             const int k = kt * BK + kb * 64;
             if constexpr (!kAT) {   // K-major: one 128-row box per k-block
               tma_load_2d_pair(adst + kb * kAKBlock, &tmA, fb, k, m);
             } else {   // A stored K x M: two 64-row (m) blocks, MN-major
-              for (int j = 0; j < BM / 64; ++j)
-                tma_load_2d_pair(adst + j * kMNBlock + kb * kBox64, &tmA, fb, m + j * 64, k);
+              for (int jj = 0; jj < BM / 64; ++jj)
+                tma_load_2d_pair(adst + jj * kMNBlock + kb * kBox64, &tmA, fb, m + jj * 64, k);
             }
-          }
-          const uint32_t bdst = smem_u32(sB + s * kBBytes);
-          for (int j = 0; j < boxes; ++j) {
-            const int n = w.tn * BN + w.n_off + (int)rank * half + j * 64;
-            for (int kb = 0; kb < kKBlocks; ++kb) {
-              const int k = kt * BK + kb * 64;
+            for (int jj = 0; jj < boxes; ++jj) {
+              const int n = w.tn * BN + w.n_off + (int)rank * half + jj * 64;
               if constexpr (!kBT)   // MN-major: 64-column blocks of BK rows
-                tma_load_2d_pair(bdst + j * kMNBlock + kb * kBox64, &tmB, fb, n, k);
+                tma_load_2d_pair(bdst + jj * kMNBlock + kb * kBox64, &tmB, fb, n, k);
               else   // B stored N x K: 64 rows (n) of 64 k per box, K-major
-                tma_load_2d_pair(bdst + kb * kBKBlock + j * kBox64, &tmB, fb, k, n);
+                tma_load_2d_pair(bdst + kb * kBKBlock + jj * kBox64, &tmB, fb, k, n);
             }
           }
           issued = it + 1;
@@ -258,14 +210,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------ MMA issuer (even CTA)
     if (rank == 0) {
       uint32_t it = 0;
-      int local = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok; u += npairs, ++local) {
-        const Unit w = unit_of(u, p, nk);
+      for (int j = 0; j < sched.n && ok; ++j) {
+        const TcUnit w = tc_pair_unit(sched, j, npairs, p, nk);
         const uint32_t idesc = instr_desc(kAbType, 2 * BM, (uint32_t)w.n_w, kAT ? 1u : 0u,
                                           kBT ? 0u : 1u);
-        const uint32_t b = local % kAccBufs;
-        const uint32_t aph = (local / kAccBufs) & 1u;
+        const uint32_t b = j % kAccBufs;
+        const uint32_t aph = (j / kAccBufs) & 1u;
         ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
         if (!ok) break;
         tc_fence_after();
@@ -302,21 +253,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     const int q = warp & 3;
     const int ew = warp - 2;
     unsigned char* stage0 = sEpi + ew * 2 * kEpiBufBytes;
-    int local = 0;
     int nstore = 0;
     const bool with_beta = p.beta != 0.f;
-    for (int u = pair; u < num_units; u += npairs, ++local) {
-      const Unit w = unit_of(u, p, nk);
-      const uint32_t b = local % kAccBufs;
-      const uint32_t aph = (local / kAccBufs) & 1u;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(q * 32) << 16);
+    for (int j = 0; j < sched.n; ++j) {
+      const TcUnit w = tc_pair_unit(sched, j, npairs, p, nk);
+      const uint32_t b = j % kAccBufs;
+      const uint32_t aph = (j / kAccBufs) & 1u;
       const int row0 = w.tm * (2 * BM) + (int)rank * BM + q * 32;
       const int col0 = w.tn * BN + w.n_off;
       const T* c_in = static_cast<const T*>(p.c_in);
       const int chunks = w.n_w / kTcEpiCols;
-      // K split: pieces before the last store their FP32 accumulator; the
-      // last piece adds theirs to its own and finishes the tile.
-      const bool keep_partial = w.piece >= 0 && w.piece < p.parts - 1;
-      const bool finish = w.piece >= 0 && !keep_partial;
+      // A head stores its FP32 accumulator for the next pair; a tail (always
+      // the pair's last unit) adds that partial to its own and finishes the
+      // tile.
+      const bool keep_partial = w.kind == kTcUnitHead;
+      const bool finish = w.kind == kTcUnitTail;
       const bool beta_here = with_beta && !keep_partial;
       // The old C of chunk c is in old[c % 2], loaded two chunks ahead (the
       // first two while the accumulator is still being computed).
@@ -327,13 +279,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           load_old_row64<T>(old[1], c_in, p.ldc, p.M, p.N, row0 + lane, col0 + kTcEpiCols);
       }
       if (finish) {
-        // Piece 0's partial: chunk 0 into this warp's staging buffers (free
-        // once its earlier stores have read them), chunks 1.. into the ring,
-        // free once this unit's MMAs are done; both by 16-byte cp.async, the
-        // lane-major layout giving each lane its own row's values.
+        // The head's partial (stored early in the other pair's share, long
+        // before this last unit ends): chunk 0 into this warp's staging
+        // buffers (free once its earlier stores have read them) while the
+        // MMAs still run, chunks 1.. into the ring once they are done; both
+        // by 16-byte cp.async, the lane-major layout giving each lane its
+        // own row's values.
         int ok = 1;
         if (lane == 0) {
-          ok = flag_wait_equal(partial_flag(p, w.slot, 0, (int)rank, q), p.epoch, p.timeout_ns,
+          ok = flag_wait_equal(partial_flag(p, w.slot, (int)rank, q), p.epoch, p.timeout_ns,
                                &bars->abort)
                    ? 1
                    : 0;
@@ -345,26 +299,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         }
         if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
         __threadfence();
-        const float4* pb = reinterpret_cast<const float4*>(partial_block(p, w.slot, 0, (int)rank, q));
+        const float4* pb = reinterpret_cast<const float4*>(partial_block(p, w.slot, (int)rank, q));
         const uint32_t st0 = smem_u32(stage0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) cp_async_16_cg(st0 + (j * 32 + lane) * 16, pb + j * 32 + lane);
+        for (int jj = 0; jj < 16; ++jj)
+          cp_async_16_cg(st0 + (jj * 32 + lane) * 16, pb + jj * 32 + lane);
         cp_async_commit();
       }
       if (!warp_wait(smem_u32(&bars->acc_full[b]), aph, p, bars, kFaultTcEpilogueWait)) break;
       tc_fence_after();
-      // Ring space of this warp for partial chunks 1..3 (8 KB each).
+      // Ring space of this warp for partial chunks 1..3 (8 KB each): the
+      // tail is the pair's last unit, so no stage is loaded any more.
       const uint32_t ring_part = smem_u32(sA) + (uint32_t)q * 3u * 8192u;
       if (finish) {
-        const float4* pb = reinterpret_cast<const float4*>(partial_block(p, w.slot, 0, (int)rank, q));
+        const float4* pb = reinterpret_cast<const float4*>(partial_block(p, w.slot, (int)rank, q));
         for (int c = 1; c < chunks; ++c)
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            cp_async_16_cg(ring_part + (uint32_t)(c - 1) * 8192u + (j * 32 + lane) * 16,
-                           pb + (c * 16 + j) * 32 + lane);
+          for (int jj = 0; jj < 16; ++jj)
+            cp_async_16_cg(ring_part + (uint32_t)(c - 1) * 8192u + (jj * 32 + lane) * 16,
+                           pb + (c * 16 + jj) * 32 + lane);
         cp_async_commit();
       }
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      const uint32_t t_row = t_lane + b * BN;
 #pragma unroll
       for (int c = 0; c < BN / kTcEpiCols; ++c) {
         if (c >= chunks) break;
@@ -379,30 +335,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[b]), 0));
         }
         if (keep_partial) {
-          float4* dst = reinterpret_cast<float4*>(partial_block(p, w.slot, w.piece, (int)rank, q)) +
+          float4* dst = reinterpret_cast<float4*>(partial_block(p, w.slot, (int)rank, q)) +
                         c * 16 * 32 + lane;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t* src = j < 8 ? &r0[j * 4] : &r1[(j - 8) * 4];
-            __stcg(dst + j * 32, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
-                                             __uint_as_float(src[2]), __uint_as_float(src[3])));
+          for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t* src = jj < 8 ? &r0[jj * 4] : &r1[(jj - 8) * 4];
+            __stcg(dst + jj * 32, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                              __uint_as_float(src[2]), __uint_as_float(src[3])));
           }
           continue;
         }
         if (finish) {
-          // Own piece + piece 0's partial, from shared memory.
+          // Own sum + the head's partial, from shared memory.
           if (c == 0)
             cp_async_wait_group<1>();
           else if (c == 1)
             cp_async_wait_group<0>();
           const uint32_t src = c == 0 ? smem_u32(stage0) : ring_part + (uint32_t)(c - 1) * 8192u;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int jj = 0; jj < 16; ++jj) {
             float4 v;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                          : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                         : "r"(src + (j * 32 + lane) * 16));
-            uint32_t* d = j < 8 ? &r0[j * 4] : &r1[(j - 8) * 4];
+                         : "r"(src + (jj * 32 + lane) * 16));
+            uint32_t* d = jj < 8 ? &r0[jj * 4] : &r1[(jj - 8) * 4];
             d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
             d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
             d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
@@ -441,13 +397,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         // Every lane's partial is in L2 before the flag says so.
         __threadfence();
         __syncwarp();
-        if (lane == 0) flag_store_release(partial_flag(p, w.slot, w.piece, (int)rank, q), p.epoch);
+        if (lane == 0) flag_store_release(partial_flag(p, w.slot, (int)rank, q), p.epoch);
       } else if (finish) {
         // The partial is consumed: clear the flag for the next launch (which
         // uses another epoch anyway, but may be a graph replay of this one
         // with the same epoch).
         __syncwarp();
-        if (lane == 0) *partial_flag(p, w.slot, 0, (int)rank, q) = 0u;
+        if (lane == 0) *partial_flag(p, w.slot, (int)rank, q) = 0u;
       }
     }
     if (lane == 0) tma_store_wait_all<0>();

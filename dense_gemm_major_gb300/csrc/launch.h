@@ -173,13 +173,19 @@ struct TcParams {
   int full_tiles;
   int split_tiles;
   int parts;
-  // Pair kernel, ksplit = 1 (parts = 2): the split tiles' units are instead
-  // two ranges of K over the whole tile.  Piece 0 stores its FP32
-  // accumulator at kpart (one 128 x 256 block per CTA and split tile) and
-  // sets its flags to `epoch`; piece 1 waits for them, adds the partial to
-  // its own accumulator, applies alpha / beta, stores C and clears the
-  // flags.  kflag: one word per (split tile, CTA, epilogue warp).
-  int ksplit = 0;
+  // Pair kernel, sk = 1 (stream-K share): tiles [0, sk_first_tile) run as
+  // whole tiles in rounds of the grid's pairs, and the sk_tiles tiles after
+  // them are shared out as equal ranges of (tile, k-tile) steps, one range
+  // per pair (sk_tiles >= pairs, so a tile is cut at most once).  The head
+  // of a cut tile (k-tiles before the cut) stores its FP32 accumulator at
+  // kpart (one 128 x 256 block per CTA and range boundary) and sets its
+  // flags to `epoch`; the pair running the tail waits for them in its last
+  // epilogue, adds the partial to its own accumulator, then clears the
+  // flags.  kflag: one word per (range boundary, CTA, epilogue warp).
+  // full_tiles, split_tiles and parts are unused in this mode.
+  int sk = 0;
+  int sk_first_tile = 0;
+  int sk_tiles = 0;
   float* kpart = nullptr;
   unsigned* kflag = nullptr;
   unsigned epoch = 0;
@@ -240,26 +246,148 @@ inline TcSplit tc_pair_split(int tiles, int pairs) {
   return sp;
 }
 
-// K split of the last partial round for the pair kernel: when the leftover
-// tiles fit the round twice over and K has at least kTc2KsplitMinK 128-deep
-// stages, each leftover tile becomes two full-width units over two ranges
-// of K; {0, 1} otherwise (the column split then applies).  Full-width units
-// keep the operand feed per SM of whole tiles, where half-width column parts
-// run at ~70 % of that rate.  The first range is kTc2KsplitLead stages
-// shorter than half, so that the second piece's MMAs still run while the
-// first stores its FP32 partial (~3.5 us, about six stages).  The hand-over
-// (that store, and ~1.6 us more in the finishing epilogue) only pays for
-// long K, measured on GB300: 4096^2 x 8192 FP16 174.1 -> 168.5 us, 8192^3
-// BF16 593.6 -> 588 us, 4096^3 92.2 both ways, K = 2048 8-10 % slower.
-constexpr int kTc2KsplitMinK = 48;
-constexpr int kTc2KsplitLead = 3;
-inline TcSplit tc_pair_ksplit(int tiles, int pairs, int nk) {
-  TcSplit sp{0, 1};
-  const int rem = tiles % pairs;
-  if (rem == 0 || tiles < pairs || 2 * rem > pairs || nk < kTc2KsplitMinK) return sp;
-  sp.split_tiles = rem;
-  sp.parts = 2;
-  return sp;
+// Stream-K share of the pair kernel (TcParams::sk): when the tiles do not
+// fill whole rounds of `pairs`, the last partial round and the round before
+// it (or the two rounds before it) are shared out as equal ranges of
+// (tile, k-tile) steps instead of running as a partial round.  A range is
+// then share = R nk / P k-tiles for R shared tiles, and a tail ends at
+// least share - nk k-tiles after the head it needs: the one round is taken
+// when that leaves kTc2StreamkSlack k-tiles for the head's partial to be
+// stored (about 4 us), else two.  Needs at least kTc2StreamkMinK k-tiles
+// per tile: measured on GB300 against the partial round (column parts),
+// 4096^2 x K FP16: K = 8192 164.5 vs 174.8 us, 4096 90.8 vs 93.9, 2048
+// 54.0 vs 53.9, 1024 39.6 vs 33.4; BF16 4097 x 3000 x 1536 43.7 vs 39.6.  Returns the first tile of the share (a multiple of pairs), or
+// -1 for no share.
+constexpr int kTc2StreamkMinK = 3072 / kTc2BK;
+constexpr int kTc2StreamkSlack = 1024 / kTc2BK;
+inline int tc_pair_streamk_first(int tiles, int pairs, int nk) {
+  if (pairs < 2 || tiles < pairs || tiles % pairs == 0 || nk < kTc2StreamkMinK) return -1;
+  for (int r = 1; r <= 2 && tiles / pairs >= r; ++r) {
+    const int first = (tiles / pairs - r) * pairs;
+    const long long slack = (long long)(tiles - first - pairs) * nk / pairs;
+    if (slack >= kTc2StreamkSlack) return first;
+  }
+  return -1;
+}
+
+// Tiles a stream-K share of `tiles` tiles (>= pairs) of nk k-tiles over
+// `pairs` ranges cuts: boundaries q * tiles * nk / pairs, q = 1 .. pairs - 1,
+// that fall inside a tile (the kernel's rule).
+inline int tc_pair_streamk_cuts(int tiles, int pairs, int nk) {
+  const long long total = (long long)tiles * nk;
+  int cuts = 0;
+  for (int q = 1; q < pairs; ++q)
+    if (((long long)q * total / pairs) % nk != 0) ++cuts;
+  return cuts;
+}
+
+// Work unit of the pair-persistent grid: 256 x 256 tile (tm, tn), the
+// columns [n_off, n_off + n_w) of it (all 256, or one of two 128-column
+// parts of a tile of a last partial round) and the k-tiles [kb, ke).
+//
+// Two schedules (TcParams::sk):
+//  * sk = 0: pair q computes units q, q + P, q + 2P, ... of the unit list
+//    (whole tiles, then the column parts of the split tiles), P pairs;
+//  * sk = 1 (stream-K share): tiles [0, D) (D = sk_first_tile, a multiple of
+//    P) are whole units in rounds of P, pair q taking q, q + P, ...; the
+//    R = sk_tiles tiles after them are one iteration space of R * nk
+//    (tile, k-tile) steps, of which pair q takes the steps
+//    [q R nk / P, (q + 1) R nk / P) -- at least one tile's worth, since
+//    R >= P, so a range boundary cuts a tile at most once.  A cut tile is
+//    two units: its head (k-tiles [0, h)) on the pair whose range ends
+//    inside it, and its tail (k-tiles [h, nk)) on the next pair.  A pair
+//    runs its whole tiles of the rounds first (all pairs in step, so that
+//    the rounds' operands are shared in L2), then its head, which stores
+//    the FP32 accumulator to the workspace and raises a flag, then the
+//    whole tiles of its range, and its tail last: the tail's epilogue adds
+//    the previous pair's head partial (stored one share earlier) to its own
+//    accumulator, in that fixed order, and finishes the tile.
+constexpr int kTcUnitWhole = 0, kTcUnitHead = 1, kTcUnitTail = 2;
+struct TcUnit {
+  int tm, tn, n_off, n_w, kb, ke;
+  int kind;    // kTcUnitWhole, kTcUnitHead or kTcUnitTail
+  int slot;    // head / tail: the range boundary that cuts the tile (1 .. P - 1)
+};
+
+// The units of one pair, in the order it runs them.
+struct TcPairSched {
+  int n;                   // number of units
+  int has_head, has_tail;  // stream-K: unit nd is a head, unit n - 1 a tail
+  int nd;                  // stream-K: whole tiles of the rounds before the share
+  int w0, nw;              // stream-K: whole tiles [w0, w0 + nw) of the share
+  int head_tile, head_ke, tail_tile, tail_kb;
+  int pair;
+};
+__host__ __device__ inline TcPairSched tc_pair_sched(int pair, int npairs, const TcParams& p,
+                                                     int nk) {
+  TcPairSched s;
+  s.pair = pair;
+  s.has_head = s.has_tail = 0;
+  s.nd = s.w0 = s.nw = 0;
+  s.head_tile = s.head_ke = s.tail_tile = s.tail_kb = 0;
+  if (!p.sk) {
+    const int num_units = p.full_tiles + p.split_tiles * p.parts;
+    s.n = pair < num_units ? (num_units - pair + npairs - 1) / npairs : 0;
+    return s;
+  }
+  const long long total = (long long)p.sk_tiles * nk;
+  const long long b = (long long)pair * total / npairs;
+  const long long e = (long long)(pair + 1) * total / npairs;
+  s.has_head = (e % nk) != 0;
+  s.has_tail = (b % nk) != 0;
+  s.nd = p.sk_first_tile / npairs;
+  const int first_whole = (int)((b + nk - 1) / nk);
+  s.w0 = p.sk_first_tile + first_whole;
+  s.nw = (int)(e / nk) - first_whole;
+  s.head_tile = p.sk_first_tile + (int)(e / nk);
+  s.head_ke = (int)(e % nk);
+  s.tail_tile = p.sk_first_tile + (int)(b / nk);
+  s.tail_kb = (int)(b % nk);
+  s.n = s.has_head + s.nd + s.nw + s.has_tail;
+  return s;
+}
+
+// Unit j (0 <= j < s.n) of the pair that s describes.
+__host__ __device__ inline TcUnit tc_pair_unit(const TcPairSched& s, int j, int npairs,
+                                               const TcParams& p, int nk) {
+  TcUnit w;
+  int tile;
+  w.n_off = 0;
+  w.n_w = kTc2BN;
+  w.kb = 0;
+  w.ke = nk;
+  w.kind = kTcUnitWhole;
+  w.slot = 0;
+  if (!p.sk) {
+    const int u = s.pair + j * npairs;
+    if (u < p.full_tiles) {
+      tile = u;
+    } else {
+      const int i = u - p.full_tiles;
+      tile = p.full_tiles + i / p.parts;
+      w.n_w = kTc2BN / p.parts;
+      w.n_off = (i % p.parts) * w.n_w;
+    }
+  } else if (j < s.nd) {
+    tile = s.pair + j * npairs;
+  } else if (s.has_head && j == s.nd) {
+    tile = s.head_tile;
+    w.ke = s.head_ke;
+    w.kind = kTcUnitHead;
+    w.slot = s.pair + 1;
+  } else {
+    const int i = j - s.nd - s.has_head;
+    if (i < s.nw) {
+      tile = s.w0 + i;
+    } else {
+      tile = s.tail_tile;
+      w.kb = s.tail_kb;
+      w.kind = kTcUnitTail;
+      w.slot = s.pair;
+    }
+  }
+  grouped_tile(tile, p.tiles_m, p.tiles_n, p.group_m, w.tm, w.tn);
+  return w;
 }
 
 // 2-CTA clusters of the pair kernel (its shared memory and block size) that

@@ -290,12 +290,14 @@ typedef struct gemm_plan_t {
   int split_tiles;   /* FP32: tiles the stream-K schedule cuts into two
                         pieces (k-ranges of two CTAs); FP16/BF16: tiles
                         of the last partial round (or of a small grid)
-                        run as split_pieces column parts                 */
+                        run as split_pieces column parts, or, with
+                        split_in_k, the tiles the stream-K share cuts    */
   int split_pieces;  /* 1 when nothing is split.  FP32: 2, the pieces'
                         FP32 partials are added into zeroed C (or, with
                         beta != 0, combined from a workspace).  FP16/BF16:
                         2 or 4 column parts of the output tile, each over
-                        the full K range                                  */
+                        the full K range; with split_in_k, 2 (the head
+                        and the tail of a cut tile)                       */
   int cluster_ctas;  /* FP16/BF16: 2 when CTA pairs (tcgen05 cta_group::2)
                         compute 256 x 256 tiles, else 1                   */
   int splitk_slices; /* > 1: the grid is too small for the GPU, so each tile
@@ -310,12 +312,18 @@ typedef struct gemm_plan_t {
                         then runs as the row-major one (path and tiles
                         above describe that run); 0 when nothing is packed */
   long long pack_bytes;
-  int split_in_k;    /* FP16/BF16 CTA pairs: 1 when the split_tiles tiles of
-                        the last partial round are cut into split_pieces
-                        ranges of K over all 256 columns (the last piece
-                        adds the others' FP32 partials, kept in the
-                        workspace, before it stores the tile) instead of
-                        column parts                                       */
+  int split_in_k;    /* FP16/BF16 CTA pairs: 1 when the tiles from
+                        streamk_first_tile on (the last partial round and
+                        the round before it) are shared out among the
+                        pairs as equal ranges of (tile, k-tile) work.  A
+                        tile cut by a range boundary runs as a head (the
+                        k-tiles before the cut, its FP32 accumulator kept
+                        in the workspace) on one pair and a tail on the
+                        next, whose epilogue adds that partial to its own
+                        FP32 sum (in a fixed order, so results are
+                        reproducible) before it stores the tile           */
+  int streamk_first_tile; /* with split_in_k: first tile of the share (the
+                        tiles before it run whole, in rounds)             */
 } gemm_plan_t;
 gemm_status_t gemm_plan(int dtype, int M, int N, int K,
                         const void *A, int lda, const void *B, int ldb,
@@ -345,6 +353,18 @@ gemm_status_t gemm_plan_resident(int dtype, gemm_op_t op_a, gemm_op_t op_b, int 
                                  float alpha, const void *A, int lda, const void *B, int ldb,
                                  float beta, const void *C, int ldc, int num_sms,
                                  int pair_clusters, gemm_plan_t *plan);
+/*
+ * Inspection of a CTA-pair plan (plan->cluster_ctas == 2) for an M x N x K
+ * problem: writes the work units that pair `pair` (0 <= pair < ctas / 2)
+ * runs, in order, as 8 ints each -- tile row, tile column (of 256 x 256
+ * tiles), first column within the tile, columns, first and end k-tile (of
+ * plan->block_k), kind (0 whole, 1 head of a tile cut by the stream-K share, 2 tail
+ * of one) and the range boundary of a head or tail -- up to max_units of
+ * them, and returns how many units the pair runs (-1 for bad arguments).
+ * Host logic only: the kernel computes the same list on the device.
+ */
+int gemm_pair_units(const gemm_plan_t *plan, int M, int N, int K, int pair, int *units,
+                    int max_units);
 /* The resident-pair count the dispatcher uses for the current device (its
  * first call on a device queries it), 0 if the query failed, -1 if there is
  * no supported device. */

@@ -259,9 +259,10 @@ def test_sgemm_packed_and_transposed_staging(dg, op_a, op_b, shape, pad, packed)
 
 @pytest.mark.parametrize("op_a,op_b", OPS)
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_op_pair_k_split_scaled(dg, dtype, op_a, op_b):
-    # The pair kernel's K split of the last round (48+ stages of K, 28
-    # leftover tiles) with operands stored transposed and alpha / beta.
+def test_op_pair_streamk_scaled(dg, dtype, op_a, op_b):
+    # The pair kernel's stream-K share of the last two rounds (72 tiles cut
+    # into a head and a tail) with operands stored transposed and alpha /
+    # beta.
     M, N, K = 4096, 4096, 6144
     st, plan = dg.gemm_plan_op(dtype, op_a, op_b, M, N, K, 0.5, 1 << 40,
                                K if op_a == "N" else M, 1 << 41, N if op_b == "N" else K, 2.0,

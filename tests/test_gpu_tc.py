@@ -247,14 +247,18 @@ def test_dependent_chain_without_sync(dg, dtype, shapes):
     check_device(dg)
 
 
-@pytest.mark.parametrize("dtype,shape", [("f16", (4096, 4096, 8192)),     # 28 leftover tiles
-                                         ("bf16", (1280, 4864, 6144)),    # 19 leftover tiles
+@pytest.mark.parametrize("dtype,shape", [("f16", (4096, 4096, 8192)),     # 256 = 3 x 76 + 28 tiles
+                                         ("bf16", (1280, 4864, 6144)),    # 95 tiles, no whole round
                                          ("f16", (4096, 2816, 6200)),     # ragged K
-                                         ("bf16", (4000, 4000, 6144))])   # ragged M and N
-def test_pair_k_split_last_round(dg, dtype, shape):
-    # The pair kernel's last partial round as two full-width K pieces: the
-    # first hands its FP32 partial to the second through the workspace and
-    # a flag.  NaN-poisoned C; sampled rows cover every tile row.
+                                         ("bf16", (4000, 4000, 6144)),    # ragged M and N
+                                         ("f16", (4096, 4096, 4096)),     # the bench shape
+                                         ("bf16", (4096, 4096, 3072))])   # 24 k-tiles
+def test_pair_streamk_share(dg, dtype, shape):
+    # The pair kernel's last two rounds as a stream-K share: a tile cut by a
+    # range boundary runs as a head on one pair, whose FP32 partial goes
+    # through the workspace and a flag to the tail on the next pair, which
+    # adds it in its epilogue.  NaN-poisoned C; sampled rows cover every
+    # tile row.
     M, N, K = shape
     plan = _plan(dg, dtype, M, N, K)
     assert plan.cluster_ctas == 2 and plan.split_in_k == 1 and plan.split_pieces == 2, \
@@ -270,9 +274,10 @@ def test_pair_k_split_last_round(dg, dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_pair_k_split_integer_scaled_exact(dg, dtype):
-    # Integer entries: the two pieces' sums and alpha * sum + beta * C are
-    # exact in FP32 and in the output type, so the bits are the oracle's.
+def test_pair_streamk_integer_scaled_exact(dg, dtype):
+    # Integer entries: the heads' partial sums, the tails' continued sums and
+    # alpha * sum + beta * C are exact in FP32 and in the output type, so the
+    # bits are the oracle's.
     M, N, K = 4096, 4096, 6144
     plan = _plan(dg, dtype, M, N, K)
     assert plan.split_in_k == 1

@@ -5,6 +5,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 import pytest
 
 import __graft_entry__
@@ -209,11 +211,12 @@ def test_plan_paths():
         ok, p = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,
                              FAKE + (2 << 30), 4096, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA
-        # CTA pairs: 256 tiles of 256 x 256 = 3 x 76 + 28; the last 28 tiles
-        # run as 2 column parts
+        # CTA pairs: 256 tiles of 256 x 256 = 3 x 76 + 28; the last 104
+        # tiles are a stream-K share (72 of them cut into a head and a tail)
         assert (p.cluster_ctas, p.block_m, p.block_n, p.block_k, p.stages) == (2, 256, 256, 128, 3)
         assert p.tiles == 16 * 16 and p.ctas == 152
-        assert (p.split_tiles, p.split_pieces) == (28, 2)
+        assert (p.split_in_k, p.streamk_first_tile, p.split_tiles, p.split_pieces) == \
+            (1, 152, 72, 2)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
         assert ok == dg.GEMM_OK and p.path == dg.PATH_TC_TMA and p.tiles == 17 * 12
@@ -242,14 +245,15 @@ def test_plan_paths():
         ok, p = dg.gemm_plan(dt, 256, 256, 65536, FAKE, 65536, FAKE + (1 << 34), 256,
                              FAKE + (2 << 34), 256, num_sms=152)
         assert (p.tiles, p.splitk_slices, p.ctas) == (2, 32, 64)
-        # 8192^3: 1024 pair tiles = 13 x 76 + 36 -> 2 parts; the edge shape:
-        # 204 pair tiles = 2 x 76 + 52 -> no split
+        # 8192^3: 1024 pair tiles = 13 x 76 + 36 -> stream-K share of the
+        # last 112; the edge shape: 204 pair tiles = 2 x 76 + 52, but only 12
+        # k-tiles -> a partial last round (52 tiles do not fit it twice)
         ok, p = dg.gemm_plan(dt, 8192, 8192, 8192, FAKE, 8192, FAKE + (1 << 30), 8192,
                              FAKE + (2 << 30), 8192, num_sms=152)
-        assert (p.cluster_ctas, p.split_tiles, p.split_pieces) == (2, 36, 2)
+        assert (p.cluster_ctas, p.split_in_k, p.streamk_first_tile) == (2, 1, 912)
         ok, p = dg.gemm_plan(dt, 4097, 3000, 1536, FAKE, 1536, FAKE + (1 << 30), 3000,
                              FAKE + (2 << 30), 3000, num_sms=152)
-        assert (p.split_tiles, p.split_pieces) == (0, 1)
+        assert (p.split_in_k, p.split_tiles, p.split_pieces) == (0, 0, 1)
         # fewer pair tiles than SM pairs (2048 x 1024: 32 tiles): still pairs,
         # as two column parts each, 128 SMs busy like 64 single-CTA tiles in
         # two parts would keep
@@ -610,29 +614,79 @@ def test_host_entry_blocks_and_validation():
                                None) == dg.GEMM_ERR_INVALID_ARG     # unknown dtype
 
 
-def test_pair_last_round_k_split_plans():
-    # The CTA-pair kernel's last partial round: when the leftover tiles fit
-    # the round twice and K has at least 48 stages of 128, each leftover
-    # tile runs as two full-width units over two ranges of K (the first
-    # piece's FP32 partial in the workspace); else as column parts.
+def test_pair_streamk_plans():
+    # The CTA-pair kernel's tiles beyond whole rounds: with at least 24
+    # k-tiles of 128 the last partial round and the round before it (or the
+    # two before it, when one leaves a range less than 8 k-tiles beyond a
+    # tile) are shared out as equal ranges of (tile, k-tile) work (one head
+    # partial per range boundary in the workspace); with fewer, the last
+    # round's tiles run as column parts when they fit it twice.
     def plan(dt, M, N, K):
         return dg.gemm_plan(dt, M, N, K, FAKE, K, FAKE + (1 << 34), N, FAKE + (1 << 36), N, 152)[1]
-    tile = 256 * 256 * 4
-    p = plan("f16", 4096, 4096, 8192)              # 256 tiles = 3 x 76 + 28, 64 stages
-    assert (p.cluster_ctas, p.split_tiles, p.split_pieces, p.split_in_k) == (2, 28, 2, 1)
-    assert p.workspace_bytes == 28 * tile
-    p = plan("bf16", 1280, 4864, 6144)             # 95 tiles = 76 + 19, 48 stages
-    assert (p.cluster_ctas, p.split_tiles, p.split_pieces, p.split_in_k) == (2, 19, 2, 1)
-    assert p.workspace_bytes == 19 * tile
-    p = plan("f16", 4096, 4096, 4096)              # 32 stages: columns
-    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (28, 2, 0)
-    assert p.workspace_bytes == 0
-    p = plan("f16", 4096, 4096, 6016)              # 47 stages: columns
-    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (28, 2, 0)
+    ws = 76 * 256 * 256 * 4
+    p = plan("f16", 4096, 4096, 4096)              # 256 tiles = 3 x 76 + 28
+    assert (p.cluster_ctas, p.ctas, p.split_in_k, p.streamk_first_tile) == (2, 152, 1, 152)
+    assert (p.split_tiles, p.split_pieces, p.workspace_bytes) == (72, 2, ws)
     p = plan("bf16", 8192, 8192, 8192)             # 1024 tiles = 13 x 76 + 36
-    assert (p.split_tiles, p.split_pieces, p.split_in_k) == (36, 2, 1)
-    p = plan("f16", 8192, 4096, 8192)              # 512 tiles = 6 x 76 + 56: too many
+    assert (p.split_in_k, p.streamk_first_tile, p.ctas) == (1, 912, 152)
+    p = plan("bf16", 4096, 4096, 3072)             # 24 k-tiles: 28 x 24 / 76 = 8.8 beyond
+    assert (p.split_in_k, p.streamk_first_tile) == (1, 152)
+    p = plan("f16", 4096, 4608, 2816)              # 288 tiles, 22 k-tiles: too short
     assert p.split_in_k == 0
+    p = plan("f16", 4096, 4096, 2944)              # 23 k-tiles: column parts
+    assert (p.split_in_k, p.split_tiles, p.split_pieces, p.workspace_bytes) == (0, 28, 2, 0)
+    p = plan("f16", 1280, 4864, 3328)              # 95 tiles, 26 k-tiles: 19 x 26 / 76 < 8,
+    assert (p.split_in_k, p.ctas) == (0, 152)      # no second round to widen into
+    p = plan("f16", 4096, 4608, 4096)              # 16 x 18 = 288 tiles = 3 x 76 + 60
+    assert (p.split_in_k, p.streamk_first_tile) == (1, 152)
+    p = plan("f16", 4864, 4096, 4096)              # 19 x 16 = 304 = 4 x 76: whole rounds
+    assert (p.split_in_k, p.split_tiles, p.ctas) == (0, 0, 152)
+    p = plan("f16", 2048, 2048, 2048)              # 64 tiles: one partial round
+    assert (p.split_in_k, p.ctas) == (0, 128)
+
+
+@pytest.mark.parametrize("dt,M,N,K", [("f16", 4096, 4096, 4096), ("bf16", 8192, 8192, 8192),
+                                      ("bf16", 4097, 3000, 1536), ("f16", 4000, 4000, 6200),
+                                      ("bf16", 4096, 4096, 3072), ("f16", 4864, 2560, 4096),
+                                      ("f16", 2304, 4096, 1024), ("bf16", 4096, 4096, 896),
+                                      ("f16", 1280, 4864, 6144), ("bf16", 2048, 2048, 2048)])
+def test_pair_schedule_covers_every_k_tile_once(dt, M, N, K):
+    # The units every pair runs (the kernel's own schedule code, run on the
+    # host): each (tile, column, k-tile) exactly once; a cut tile is one head
+    # (on pair q - 1 right after its whole tiles of the rounds, k-tiles
+    # [0, h)) and one tail (last unit of pair q, k-tiles [h, nk)) for
+    # boundary q; whole units have every k-tile; pairs get equal work within
+    # one k-tile of a full-width tile; the rounds before the share are in
+    # step (unit i of every pair is a tile of round i).
+    st, p = dg.gemm_plan(dt, M, N, K, FAKE, K, FAKE + (1 << 34), N, FAKE + (1 << 36), N, 152)
+    assert st == dg.GEMM_OK and p.cluster_ctas == 2
+    pairs = p.ctas // 2
+    tm_n, tn_n, nk = -(-M // 256), -(-N // 256), -(-K // p.block_k)
+    cover = np.zeros((tm_n, tn_n, 256, nk), dtype=np.int32)
+    heads, tails, work = {}, {}, []
+    for q in range(pairs):
+        units = dg.gemm_pair_units(p, M, N, K, q)
+        w_q = 0
+        for j, (tm, tn, n_off, n_w, kb, ke, kind, slot) in enumerate(units):
+            assert 0 <= tm < tm_n and 0 <= tn < tn_n and 0 <= kb < ke <= nk
+            cover[tm, tn, n_off:n_off + n_w, kb:ke] += 1
+            w_q += (ke - kb) * n_w
+            if kind == 1:
+                assert j == p.streamk_first_tile // pairs and kb == 0 and ke < nk
+                assert slot == q + 1 and n_w == 256
+                heads[slot] = (tm, tn, ke)
+            elif kind == 2:
+                assert j == len(units) - 1 and kb > 0 and ke == nk and slot == q and n_w == 256
+                tails[slot] = (tm, tn, kb)
+            else:
+                assert kind == 0 and (kb, ke) == (0, nk)
+        work.append(w_q)
+    assert np.all(cover == 1)
+    assert heads == tails
+    assert len(heads) == (p.split_tiles if p.split_in_k else 0)
+    if p.split_in_k:
+        assert max(work) - min(work) <= 256
+        assert p.workspace_bytes >= (max(heads, default=0) + 1) * 256 * 256 * 4
 
 
 def test_pair_plan_with_fewer_resident_clusters():
