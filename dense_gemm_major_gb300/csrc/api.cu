@@ -710,7 +710,8 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
         dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     alignas(64) CUtensorMap tmA, tmB, tmC;
     // A: {K, M} with 64 x 128 boxes, or as stored K x M ({M, K}, 64 x 64
-    // boxes); B: {N, K} with 64 x 64 boxes, or as stored N x K ({K, N}).
+    // boxes); B: {N, K} with 64 x 64 boxes (64 x 128 for CTA pairs: one box
+    // per 64-column block and stage), or as stored N x K ({K, N}).
     const bool enc_a =
         op_a ? encode_2d(&tmA, dt, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda * 2, 64,
                          dgemm::kTcBK, CU_TENSOR_MAP_SWIZZLE_128B)
@@ -720,7 +721,8 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
         op_b ? encode_2d(&tmB, dt, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb * 2, dgemm::kTcBK,
                          64, CU_TENSOR_MAP_SWIZZLE_128B)
              : encode_2d(&tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb * 2, 64,
-                         dgemm::kTcBK, CU_TENSOR_MAP_SWIZZLE_128B);
+                         plan.cluster_ctas == 2 ? dgemm::kTc2BK : dgemm::kTcBK,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!enc_a || !enc_b ||
         !encode_2d(&tmC, dt, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * 2, dgemm::kTcEpiCols,
                    32, CU_TENSOR_MAP_SWIZZLE_128B))
