@@ -144,6 +144,174 @@ def job_tflops(step_flops: float, step_ms: float, ws: int) -> float:
     return ws * step_flops / (step_ms * 1e-3) / 1e12
 
 
+# ------------------------------------------------------------ measured peaks and extra legs
+
+def ffma_probe(dg, dev, stream, sms, seconds=0.15):
+    """Measured FP32 FFMA throughput (the SGEMM roofline's denominator):
+    the library's register-only fma.rn.f32x2 probe on every SM, timed with
+    CUDA events on the launching stream, with the SM clock sampled while it
+    runs.  Returns TFLOP/s, the median clock and TFLOP/s per GHz."""
+    blocks = 4 * sms
+    out = torch.empty(blocks * dg.gemm_probe_ffma_threads(), dtype=torch.float32, device=dev)
+    iters = 20000
+    st, fl = dg.gemm_probe_ffma(blocks, iters, out.data_ptr(), stream.cuda_stream)
+    if st != dg.GEMM_OK:
+        raise RuntimeError(f"ffma probe: {dg.status_string(st)}")
+    torch.cuda.synchronize(dev)
+    # Size one launch to ~seconds / 5 from a first timing.
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        dg.gemm_probe_ffma(blocks, iters, out.data_ptr(), stream.cuda_stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    iters = max(iters, int(iters * (seconds / 5) / max(e0.elapsed_time(e1) * 1e-3, 1e-6)))
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            st, fl = dg.gemm_probe_ffma(blocks, iters, out.data_ptr(), stream.cuda_stream)
+            e1.record(stream)
+            times.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = statistics.median(a.elapsed_time(b) for a, b in times)
+    tf = fl / (ms * 1e-3) / 1e12
+    mhz = clocks["sm_mhz"] if clocks else None
+    return {"tflops": round(tf, 2), "ms_per_launch": round(ms, 3), "flops_per_launch": fl,
+            "launch": f"{blocks} CTAs x {dg.gemm_probe_ffma_threads()} threads, 16 independent "
+                      f"fma.rn.f32x2 chains x {iters} iterations per thread",
+            "sm_mhz": mhz, "tflops_per_ghz": round(tf / (mhz / 1000.0), 3) if mhz else None,
+            "clocks": clocks}
+
+
+# The scope's configurations (the seeded workloads), with the oracle rows
+# checked per configuration: all rows where the oracle is quick, else a
+# deterministic sample (first and last rows, both sides of tile edges,
+# random rows).
+CONFIG_ROWS = {"f32_256": None, "f32_256_int": None, "f32_2048": 128, "f32_4096": 128,
+               "f16_4096": 128, "bf16_8192": 96, "f32_edge": None, "bf16_edge": 256}
+TOLERANCE = {"f32": 1e-5, "f16": 2e-3, "bf16": 1e-2}
+
+
+def run_configs(dg, dev, stream, sms, ffma_peak, ffma_measured, tensor_peak, peaks_src,
+                reps=15, check=True):
+    """Every configuration: CUDA-event time per call (L2 flushed before
+    each, median of `reps` after 3 warm-ups), TFLOP/s, the fraction of its
+    roofline, and the oracle comparison on sampled rows (bit-exact for the
+    integer-valued copy)."""
+    import oracle
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for name in CONFIG_ROWS:
+        w = workloads.WORKLOADS[name]
+        A_cpu, B_cpu = workloads.make(w)
+        A, B = A_cpu.to(dev), B_cpu.to(dev)
+        C = torch.full((w.M, w.N), float("nan"), dtype=A.dtype, device=dev)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                st = dg.gemm(w.dtype, w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                             C.data_ptr(), w.N, stream.cuda_stream)
+                e1.record(stream)
+                if st != dg.GEMM_OK:
+                    raise RuntimeError(f"{name}: {dg.status_string(st)}")
+                if i >= 3:
+                    times.append((e0, e1))
+        st, bits = dg.gemm_device_check(stream.cuda_stream)
+        if st != dg.GEMM_OK:
+            raise RuntimeError(f"{name}: device check {dg.status_string(st)} ({bits:#x})")
+        ms = statistics.median(a.elapsed_time(b) for a, b in times)
+        tf = w.flops / (ms * 1e-3) / 1e12
+        _, plan = dg.gemm_plan(w.dtype, w.M, w.N, w.K, A.data_ptr(), w.K, B.data_ptr(), w.N,
+                               C.data_ptr(), w.N, sms)
+        entry = {"shape": [w.M, w.N, w.K], "dtype": w.dtype, "inputs": f"{w.dist} seed {w.seed}",
+                 "ms_median": round(ms, 4), "tflops": round(tf, 2)}
+        if w.dtype == "f32":
+            entry.update({"peak_tflops": round(ffma_peak, 1), "frac_of_peak": round(tf / ffma_peak, 4),
+                          "peak_kind": "FFMA, derived: SMs x 128 lanes x 2 x max SM clock"})
+            if ffma_measured:
+                entry["frac_of_measured_ffma"] = round(tf / ffma_measured, 4)
+        else:
+            entry.update({"peak_tflops": round(tensor_peak, 1), "frac_of_peak": round(tf / tensor_peak, 4),
+                          "peak_kind": f"dense BF16/FP16 tensor, {peaks_src} burst"})
+        entry["plan"] = {"path": plan.path, "ctas": plan.ctas, "cluster_ctas": plan.cluster_ctas,
+                         "split_tiles": plan.split_tiles, "stream_k": plan.split_in_k,
+                         "splitk_slices": plan.splitk_slices}
+        if check:
+            nrows = CONFIG_ROWS[name]
+            rows = None if nrows is None else workloads.sample_rows(w.M, nrows, seed=w.seed)
+            ref, S = oracle.gemm(w.dtype, workloads.to_numpy_bits(A_cpu),
+                                 workloads.to_numpy_bits(B_cpu), rows=rows)
+            got = C.float().cpu().numpy().astype(np.float64)
+            if rows is not None:
+                got = got[rows]
+            if w.dist == "int":
+                exact = bool(np.array_equal(got, ref))
+                entry["parity_on_sample"] = {"rows": int(got.shape[0]), "bit_exact": exact,
+                                             "pass": exact}
+            else:
+                err, idx, bad = oracle.normalized_error(got, ref, S)
+                entry["parity_on_sample"] = {"rows": int(got.shape[0]),
+                                             "max_normalised_error": err,
+                                             "tolerance": TOLERANCE[w.dtype],
+                                             "pass": bool(err <= TOLERANCE[w.dtype] and bad == 0)}
+        out[name] = entry
+        del A, B, C
+    return out
+
+
+def run_sustained(dg, cases, dev, stream, seconds=1.0):
+    """Each GEMM of the step back to back for about `seconds` (no L2 flush
+    in between), timed with CUDA events around the whole run, with the SM
+    clock sampled throughout: TFLOP/s at the clock the power cap settles at,
+    and TFLOP/s per GHz, which compares runs taken at different clocks."""
+    out = {}
+    for c in cases:
+        w = c["w"]
+
+        def call():
+            st = dg.gemm(w.dtype, w.M, w.N, w.K, c["A"].data_ptr(), w.K, c["B"].data_ptr(),
+                         w.N, c["C"].data_ptr(), w.N, stream.cuda_stream)
+            if st != dg.GEMM_OK:
+                raise RuntimeError(f"{w.name}: {dg.status_string(st)}")
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                call()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        n = max(10, int(seconds / max(e0.elapsed_time(e1) * 1e-3 / 5, 1e-6)))
+        sampler = ClockSampler(dev.index)
+        sampler.start()
+        with torch.cuda.stream(stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                call()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks = sampler.stop()
+        st, bits = dg.gemm_device_check(stream.cuda_stream)
+        if st != dg.GEMM_OK:
+            raise RuntimeError(f"{w.name}: device check {dg.status_string(st)} ({bits:#x})")
+        ms = e0.elapsed_time(e1)
+        tf = n * w.flops / (ms * 1e-3) / 1e12
+        mhz = clocks["sm_mhz"] if clocks else None
+        out[w.name] = {"calls": n, "seconds": round(ms / 1000, 3), "tflops": round(tf, 2),
+                       "sm_mhz": mhz,
+                       "tflops_per_ghz": round(tf / (mhz / 1000.0), 2) if mhz else None,
+                       "clocks": clocks}
+    return out
+
+
 # ------------------------------------------------------------ our arm
 
 def run_ours(args, ws, rank, local):
@@ -257,8 +425,10 @@ def run_ours(args, ws, rank, local):
     roofline = {"bound": "alu" if dominant.startswith("f32") else "tensor",
                 "achieved": dk["tflops"], "peak": dk["peak_tflops"], "unit": "TFLOP/s",
                 "frac": dk["frac_of_peak"], "traffic": traffic,
-                "kernel": dominant, "peak_source": "derived from unit counts and max SM clock"
-                if dominant.startswith("f32") else f"{peaks_src} (MEASURED_PEAKS.json bf16_tflops)"}
+                "kernel": dominant, "peak_source": "derived from unit counts and max SM clock "
+                "(152 SMs x 128 FFMA lanes x 2 x sm_max_mhz); the FFMA probe's measured rate is "
+                "in measured_peak" if dominant.startswith("f32")
+                else f"{peaks_src} (MEASURED_PEAKS.json bf16_tflops)"}
     roofline_tensor = None
     tname = next((n for n in per_kernel if not n.startswith("f32")), None)
     if tname is not None:
@@ -270,6 +440,18 @@ def run_ours(args, ws, rank, local):
 
     # End to end through the C ABI with host buffers.
     e2e = None if args.no_e2e else run_e2e(dg, cases, dev, stream, args)
+
+    # The measured FFMA peak, every configuration, and the sustained leg.
+    ffma = None if args.no_extra else ffma_probe(dg, dev, stream, sms)
+    if ffma is not None:
+        roofline["measured_peak"] = {"ffma_tflops": ffma["tflops"], "sm_mhz": ffma["sm_mhz"],
+                                     "frac": round(roofline["achieved"] / ffma["tflops"], 4)
+                                     if dominant.startswith("f32") else None,
+                                     "source": "gemm_probe_ffma (fma.rn.f32x2, registers only)"}
+    configs = None if args.no_extra else run_configs(
+        dg, dev, stream, sms, ffma_peak, ffma["tflops"] if ffma else None, tensor_peak, peaks_src,
+        check=not args.no_cpu_baseline)
+    sustained = None if args.no_extra else run_sustained(dg, cases, dev, stream)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
@@ -285,6 +467,11 @@ def run_ours(args, ws, rank, local):
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "device": {"name": props.name, "sms": sms},
     }
+    if not args.no_extra:
+        out["peaks"] = {"ffma": ffma, "tensor_bf16_burst": tensor_peak,
+                        "tensor_source": f"{peaks_src} (MEASURED_PEAKS.json bf16_tflops)"}
+        out["configs"] = configs
+        out["sustained"] = sustained
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         if args.beta != 0.0:
             # One call on the seeded old C, so the sample check sees a single update.
@@ -479,6 +666,8 @@ def main():
                     help="time budget of the CPU oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the FFMA probe, the per-configuration table and the sustained leg")
     ap.add_argument("--alpha", type=float, default=1.0, help="scale of A.B (default 1)")
     ap.add_argument("--beta", type=float, default=0.0, help="scale of the old C (default 0)")
     ap.add_argument("--workloads", default=",".join(STEP_WORKLOADS),

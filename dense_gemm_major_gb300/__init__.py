@@ -33,7 +33,8 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
             "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout",
-            "gemm_plan_resident", "gemm_pair_clusters", "gemm_pair_units")
+            "gemm_plan_resident", "gemm_pair_clusters", "gemm_pair_units", "gemm_probe_ffma",
+            "gemm_probe_ffma_threads")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
 # (A as K x M, B as N x K).
@@ -97,6 +98,10 @@ def load() -> ctypes.CDLL:
     lib.gemm_pair_units.restype = i
     lib.gemm_pair_units.argtypes = [ctypes.POINTER(Plan), i, i, i, i,
                                     ctypes.POINTER(ctypes.c_int), i]
+    lib.gemm_probe_ffma.restype = i
+    lib.gemm_probe_ffma.argtypes = [i, i, vp, vp, ctypes.POINTER(ctypes.c_double)]
+    lib.gemm_probe_ffma_threads.restype = i
+    lib.gemm_probe_ffma_threads.argtypes = []
     lib.gemm_pair_clusters.restype = i
     lib.gemm_pair_clusters.argtypes = []
     lib.gemm_host.restype = i
@@ -225,6 +230,17 @@ def gemm_pair_units(plan, M, N, K, pair):
     buf = (ctypes.c_int * (8 * max(n, 1)))()
     load().gemm_pair_units(ctypes.byref(plan), M, N, K, pair, buf, n)
     return [tuple(buf[8 * j: 8 * j + 8]) for j in range(n)]
+
+
+def gemm_probe_ffma(blocks, iters, out, stream=0):
+    """Launches the FFMA throughput probe; returns (status, flops)."""
+    fl = ctypes.c_double(0.0)
+    st = load().gemm_probe_ffma(blocks, iters, out, stream, ctypes.byref(fl))
+    return st, fl.value
+
+
+def gemm_probe_ffma_threads() -> int:
+    return load().gemm_probe_ffma_threads()
 
 
 def gemm_pair_clusters() -> int:

@@ -106,6 +106,16 @@ __device__ __forceinline__ Unit unit_of(int u, const TcParams& p, int nk) {
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+// A single thread's bounded wait (the MMA issuer's): spins on the barrier;
+// on giving up records the fault (once per CTA) and raises the abort flag.
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const TcParams& p,
+                                            Barriers* bars, unsigned fault_code) {
+  if (mbar_wait_spin_bounded(bar, parity, p.timeout_ns, &bars->abort)) return true;
+  if (!*(volatile int*)&bars->abort) raise_fault(p.fault, fault_code);
+  *(volatile int*)&bars->abort = 1;
+  return false;
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcParams& p,
                                           Barriers* bars, unsigned fault_code) {
   const int lane = threadIdx.x & 31;
@@ -210,27 +220,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-
-    uint32_t it = 0;
-    int local = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
-      const Unit w = unit_of(u, p, nk);
-      const uint32_t idesc = instr_desc(kAbType, BM, (uint32_t)w.n_w, kAT ? 1u : 0u,
-                                        kBT ? 0u : 1u);
-      const uint32_t b = local & 1;
-      const uint32_t aph = (local >> 1) & 1u;
-      ok = warp_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + b * BN;
-      for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
-        const uint32_t s = it % S;
-        const uint32_t ph = (it / S) & 1u;
-        ok = warp_wait(smem_u32(&bars->full[s]), ph, p, bars, kFaultTcMmaWait);
+    // One thread waits and issues, with no warp-wide synchronisation between
+    // stages (as in the pair kernel, where that bookkeeping had left the
+    // tensor pipe idle for part of every stage).
+    if (lane == 0) {
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
+        const Unit w = unit_of(u, p, nk);
+        const uint32_t idesc = instr_desc(kAbType, BM, (uint32_t)w.n_w, kAT ? 1u : 0u,
+                                          kBT ? 0u : 1u);
+        const uint32_t b = local & 1;
+        const uint32_t aph = (local >> 1) & 1u;
+        ok = thread_wait(smem_u32(&bars->acc_empty[b]), aph ^ 1u, p, bars, kFaultTcMmaWait);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
+          const uint32_t s = it % S;
+          const uint32_t ph = (it / S) & 1u;
+          ok = thread_wait(smem_u32(&bars->full[s]), ph, p, bars, kFaultTcMmaWait);
+          if (!ok) break;
+          tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kABytes);
           const uint32_t b0 = smem_u32(sB + s * kBBytes);
 #pragma unroll
@@ -243,12 +255,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           mma_commit(smem_u32(&bars->empty[s]));   // frees the stage when the MMAs finish
         }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->acc_full[b]));   // accumulator ready
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&bars->acc_full[b]));   // accumulator ready
-      __syncwarp();
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;                    // TMEM lane quadrant of this warp

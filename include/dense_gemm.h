@@ -400,6 +400,22 @@ gemm_status_t gemm_selftest_timeout(unsigned timeout_us, cudaStream_t stream);
  */
 gemm_status_t gemm_selftest_flag_timeout(unsigned timeout_us, cudaStream_t stream);
 
+/*
+ * FP32 FFMA throughput probe: the SGEMM roofline's denominator, measured
+ * rather than derived from unit counts (the m.lqnn.cn SGEMM article,
+ * sections 1.1-1.2, states a kernel's efficiency against the card's FP32
+ * peak).  Launches `blocks` CTAs of gemm_probe_ffma_threads() threads on
+ * `stream`; each thread runs `iters` iterations of 16 independent packed
+ * FMAs (fma.rn.f32x2, 4 FLOPs each) on registers only and writes one float
+ * to out[block * threads + thread] (device memory, caller-owned, at least
+ * blocks * threads floats).  *flops (may be NULL) receives the launch's
+ * floating-point operations; the caller times the launch (CUDA events on
+ * `stream`).  Non-positive sizes or a NULL out: GEMM_ERR_INVALID_ARG.
+ */
+gemm_status_t gemm_probe_ffma(int blocks, int iters, float *out, cudaStream_t stream,
+                              double *flops);
+int gemm_probe_ffma_threads(void);
+
 #if defined(__cplusplus)
 }
 #endif
