@@ -234,6 +234,17 @@ bool tc_streamk_disabled() {
   return v;
 }
 
+// Measurement override: DENSE_GEMM_TC_SK_ROUNDS=2 makes the pair kernel's
+// stream-K share cover the last partial round and the two before it
+// whenever there are that many.
+int tc_sk_min_rounds() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_TC_SK_ROUNDS");
+    return s != nullptr && std::strcmp(s, "2") == 0 ? 2 : 1;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_TC_SPLIT=0 turns off the column split of
 // the last partial round of FP16/BF16 tiles.
 bool tc_split_disabled() {
@@ -507,7 +518,8 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
   // column parts when they fit it twice.
   const int sk_first = (tc_streamk_disabled() || !handover)
                            ? -1
-                           : dgemm::tc_pair_streamk_first(pair_tiles, pairs, nk_pair);
+                           : dgemm::tc_pair_streamk_first(pair_tiles, pairs, nk_pair,
+                                                          tc_sk_min_rounds());
   const auto pair_busy = [&]() {
     if (sk_first >= 0) return 2 * pairs;
     const dgemm::TcSplit sp = dgemm::tc_pair_split(pair_tiles, pairs);
@@ -585,7 +597,9 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
 void tc_schedule_params(const gemm_plan_t& plan, int M, int N, dgemm::TcParams* p) {
   p->tiles_m = ceil_div(M, plan.block_m);
   p->tiles_n = ceil_div(N, plan.block_n);
-  p->group_m = tc_group_override() > 0 ? tc_group_override() : dgemm::kTcGroupM;
+  p->group_m = tc_group_override() > 0    ? tc_group_override()
+               : plan.cluster_ctas == 2 ? dgemm::kTc2GroupM
+                                        : dgemm::kTcGroupM;
   p->full_tiles = plan.tiles - plan.split_tiles;
   p->split_tiles = plan.split_tiles;
   p->parts = plan.split_pieces;
