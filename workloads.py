@@ -58,6 +58,8 @@ WORKLOADS = {
         Workload("bf16_8192", "bf16", 8192, 8192, 8192, "normal", 3),
         Workload("f32_edge", "f32", 1000, 1030, 777, "uniform", 4),
         Workload("bf16_edge", "bf16", 4097, 3000, 1536, "uniform", 4),
+        # a skinny product (two output tiles, long K): single CTAs, split-K
+        Workload("f16_skinny", "f16", 256, 256, 65536, "normal", 5),
     ]
 }
 
