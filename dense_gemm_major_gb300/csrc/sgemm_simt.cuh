@@ -225,40 +225,78 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   // worth of k-tiles, or G = 2 tiles, so each range is half a tile: either
   // way a tile is cut into at most two pieces.  The ring's slot and phase
   // follow the k-tiles this CTA has consumed over all its units (g0 + kt).
+  //
+  // Within its range a CTA runs its whole tiles first, then the head of the
+  // last tile it touches (k-tiles from 0), then the tail of the first (up to
+  // nk): every CTA then works at k-tile tau or tau - (share mod nk) of its
+  // units at time tau, so the share's A and B panels are read in two fronts
+  // instead of at as many k offsets as there are CTAs, and L2 holds the
+  // slices in between (the two pieces of a cut tile add into C in either
+  // order, or combine from the workspace in a fixed one).  Measured on
+  // GB300 at 4096^3: DRAM traffic 435 -> 389 MB per launch, same time.
   const int nk_all = (p.K + BK - 1) / BK;
   const int b = blockIdx.x;
   int dp_next = b;
-  long long it, it_end;
+  int sk_units = 0, sk_next = 0;   // stream-K units of this CTA, the next one
+  int sk_t0 = 0, sk_kb0 = 0, sk_t1 = 0, sk_ke1 = 0, sk_w0 = 0, sk_nw = 0;
+  bool sk_head = false;
   if (p.slices > 1) {
     dp_next = 0x7fffffff;
-    it = 0;
-    it_end = 1;
+    sk_units = 1;
   } else {
     const long long total = (long long)(p.tiles_m * p.tiles_n - p.dp_tiles) * nk_all;
-    it = (long long)b * total / gridDim.x;
-    it_end = (long long)(b + 1) * total / gridDim.x;
+    const long long it0 = (long long)b * total / gridDim.x;
+    const long long it1 = (long long)(b + 1) * total / gridDim.x;
+    if (it1 > it0) {
+      sk_t0 = (int)(it0 / nk_all);
+      sk_kb0 = (int)(it0 % nk_all);
+      sk_t1 = (int)((it1 - 1) / nk_all);
+      sk_ke1 = (int)((it1 - 1) % nk_all) + 1;
+      if (sk_t0 == sk_t1) {
+        sk_units = 1;   // half a tile: one unit [kb0, ke1)
+      } else {
+        sk_head = sk_ke1 < nk_all;
+        sk_w0 = sk_t0 + (sk_kb0 > 0 ? 1 : 0);
+        sk_nw = sk_t1 - (sk_head ? 1 : 0) - sk_w0 + 1;
+        sk_units = sk_nw + (sk_head ? 1 : 0) + (sk_kb0 > 0 ? 1 : 0);
+      }
+    }
   }
   int g0 = 0;
-  while (dp_next < p.dp_tiles || it < it_end) {
+  while (dp_next < p.dp_tiles || sk_next < sk_units) {
     int tile, k_begin, k_end;
     if (p.slices > 1) {
       tile = b / p.slices;
       const int sl = b - tile * p.slices;
       k_begin = sl * nk_all / p.slices;
       k_end = (sl + 1) * nk_all / p.slices;
-      it = it_end;
+      ++sk_next;
     } else if (dp_next < p.dp_tiles) {
       tile = dp_next;
       k_begin = 0;
       k_end = nk_all;
       dp_next += gridDim.x;
     } else {
-      const int t = (int)(it / nk_all);
+      const int u = sk_next++;
+      int t;
+      if (sk_t0 == sk_t1) {
+        t = sk_t0;
+        k_begin = sk_kb0;
+        k_end = sk_ke1;
+      } else if (u < sk_nw) {
+        t = sk_w0 + u;
+        k_begin = 0;
+        k_end = nk_all;
+      } else if (sk_head && u == sk_nw) {
+        t = sk_t1;
+        k_begin = 0;
+        k_end = sk_ke1;
+      } else {
+        t = sk_t0;
+        k_begin = sk_kb0;
+        k_end = nk_all;
+      }
       tile = p.dp_tiles + t;
-      k_begin = (int)(it - (long long)t * nk_all);
-      const long long left = it_end - it;
-      k_end = left < nk_all - k_begin ? k_begin + (int)left : nk_all;
-      it += k_end - k_begin;
     }
     int tm, tn;
     grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);

@@ -97,19 +97,29 @@ def _streamk_cuts(tiles, nk, grid):
 
 
 def _streamk_units(tiles, nk, grid):
-    """The SGEMM kernel's unit loop, per CTA: (tile, k_begin, k_end)."""
+    """The SGEMM kernel's unit loop, per CTA: (tile, k_begin, k_end) -- its
+    whole tiles of the waves, then of its stream-K range the whole tiles,
+    the head of the last tile (k from 0) and the tail of the first (to nk)."""
     dp = _dp_tiles(tiles, grid)
     total = (tiles - dp) * nk
     out = []
     for b in range(grid):
         units = [(t, 0, nk) for t in range(b, dp, grid)]
-        it, end = b * total // grid, (b + 1) * total // grid
-        while it < end:
-            t = it // nk
-            kb = it - t * nk
-            ke = min(nk, kb + (end - it))
-            units.append((dp + t, kb, ke))
-            it += ke - kb
+        it0, it1 = b * total // grid, (b + 1) * total // grid
+        if it1 > it0:
+            t0, kb0 = divmod(it0, nk)
+            t1, ke1 = (it1 - 1) // nk, (it1 - 1) % nk + 1
+            if t0 == t1:
+                units.append((dp + t0, kb0, ke1))
+            else:
+                head = ke1 < nk
+                w0 = t0 + (1 if kb0 > 0 else 0)
+                w1 = t1 - (1 if head else 0)
+                units += [(dp + t, 0, nk) for t in range(w0, w1 + 1)]
+                if head:
+                    units.append((dp + t1, 0, ke1))
+                if kb0 > 0:
+                    units.append((dp + t0, kb0, nk))
         out.append(units)
     return out
 
