@@ -21,6 +21,10 @@ LIB = os.path.join(PKG, "libdense_gemm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+# Extra nvcc flags for measurement builds (for example
+# -DDENSE_GEMM_L2_HINT=1); a change of them rebuilds every unit.
+EXTRA_FLAGS = os.environ.get("DENSE_GEMM_NVCC_FLAGS", "").split()
+FLAGS_STAMP = os.path.join(OBJ_DIR, "flags.txt")
 
 
 def nvcc() -> str:
@@ -37,16 +41,23 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
     os.makedirs(OBJ_DIR, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest_header = max((os.path.getmtime(h) for h in _headers()), default=0.0)
+    flags_text = " ".join(EXTRA_FLAGS)
+    try:
+        with open(FLAGS_STAMP) as f:
+            flags_changed = f.read() != flags_text
+    except OSError:
+        flags_changed = bool(EXTRA_FLAGS)
     procs = []
     objs = []
     for src in sources:
         obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
         objs.append(obj)
-        stale = (not os.path.exists(obj) or os.path.getmtime(obj) < os.path.getmtime(src)
+        stale = (flags_changed or not os.path.exists(obj)
+                 or os.path.getmtime(obj) < os.path.getmtime(src)
                  or os.path.getmtime(obj) < newest_header)
         if not stale and not ptxas_verbose:
             continue
-        cmd = [nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + \
+        cmd = [nvcc()] + NVCC_FLAGS + EXTRA_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + \
             ["-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -62,6 +73,8 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{t}" for s, t in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
+    with open(FLAGS_STAMP, "w") as f:
+        f.write(flags_text)
     if procs or not os.path.exists(LIB) or any(os.path.getmtime(LIB) < os.path.getmtime(o) for o in objs):
         cmd = [nvcc()] + ARCH + ["-shared", "-o", LIB] + objs + ["-lcuda"]
         if verbose:

@@ -200,18 +200,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(fb, kABytes + boxes * kBBoxBytes);
           const uint32_t adst = smem_u32(sA + s * kABytes);
           if constexpr (!kAT) {
-            tma_load_2d(adst, &tmA, fb, kt * BK, tm * BM);
+            tma_load_operand<0>(adst, &tmA, fb, kt * BK, tm * BM);
           } else {   // A stored K x M: two 64-row (m) blocks, MN-major
             for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d(adst + j * kBBoxBytes, &tmA, fb, tm * BM + j * 64, kt * BK);
+              tma_load_operand<0>(adst + j * kBBoxBytes, &tmA, fb, tm * BM + j * 64, kt * BK);
           }
           const uint32_t bdst = smem_u32(sB + s * kBBytes);
           for (int j = 0; j < boxes; ++j) {
             const int n = tn * BN + w.n_off + j * 64;
             if constexpr (!kBT)
-              tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, n, kt * BK);
+              tma_load_operand<1>(bdst + j * kBBoxBytes, &tmB, fb, n, kt * BK);
             else   // B stored N x K: 64 rows (n) of 64 k each, K-major
-              tma_load_2d(bdst + j * kBBoxBytes, &tmB, fb, kt * BK, n);
+              tma_load_operand<1>(bdst + j * kBBoxBytes, &tmB, fb, kt * BK, n);
           }
           issued = it + 1;
         }

@@ -198,22 +198,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           for (int kb = 0; kb < kKBlocks; ++kb) {
             const int k = kt * BK + kb * 64;
             if constexpr (!kAT) {   // K-major: one 128-row box per k-block
-              tma_load_2d_pair(adst + kb * kAKBlock, &tmA, fb, k, m);
+              tma_load_operand_pair<0>(adst + kb * kAKBlock, &tmA, fb, k, m);
             } else {   // A stored K x M: two 64-row (m) blocks, MN-major
               for (int jj = 0; jj < BM / 64; ++jj)
-                tma_load_2d_pair(adst + jj * kMNBlock + kb * kBox64, &tmA, fb, m + jj * 64, k);
+                tma_load_operand_pair<0>(adst + jj * kMNBlock + kb * kBox64, &tmA, fb, m + jj * 64, k);
             }
             if constexpr (kBT) {   // B stored N x K: 64 rows (n) of 64 k per box, K-major
               for (int jj = 0; jj < boxes; ++jj) {
                 const int n = w.tn * BN + w.n_off + (int)rank * half + jj * 64;
-                tma_load_2d_pair(bdst + kb * kBKBlock + jj * kBox64, &tmB, fb, k, n);
+                tma_load_operand_pair<1>(bdst + kb * kBKBlock + jj * kBox64, &tmB, fb, k, n);
               }
             }
           }
           if constexpr (!kBT) {   // MN-major: one box per 64-column block, all BK rows
             for (int jj = 0; jj < boxes; ++jj) {
               const int n = w.tn * BN + w.n_off + (int)rank * half + jj * 64;
-              tma_load_2d_pair(bdst + jj * kMNBlock, &tmB, fb, n, kt * BK);
+              tma_load_operand_pair<1>(bdst + jj * kMNBlock, &tmB, fb, n, kt * BK);
             }
           }
           issued = it + 1;

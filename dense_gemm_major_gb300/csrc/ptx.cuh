@@ -179,6 +179,47 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* des
       : "memory");
 }
 
+// L2 cache hints on the operand loads, a compile-time switch for the
+// access-policy measurement (the GB300 GEMM roadmap, section 3.2, suggests
+// keeping reused data resident in L2; its section 6.1 warns that marking
+// data read once does the opposite).  DENSE_GEMM_L2_HINT: 0 (the default)
+// plain loads; 1 A evict-first, B evict-last; 2 A evict-last, B
+// evict-first.  Build with -DDENSE_GEMM_L2_HINT=n in DENSE_GEMM_NVCC_FLAGS.
+#ifndef DENSE_GEMM_L2_HINT
+#define DENSE_GEMM_L2_HINT 0
+#endif
+
+__device__ __forceinline__ uint64_t l2_policy(bool evict_first) {
+  uint64_t p;
+  if (evict_first)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache-policy operand.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* desc,
+                                                 uint32_t bar, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// The load of operand kOperand (0 = A, 1 = B) under DENSE_GEMM_L2_HINT.
+template <int kOperand>
+__device__ __forceinline__ void tma_load_operand(uint32_t dst, const CUtensorMap* desc,
+                                                 uint32_t bar, int32_t x, int32_t y) {
+#if DENSE_GEMM_L2_HINT == 0
+  tma_load_2d(dst, desc, bar, x, y);
+#else
+  tma_load_2d_hint(dst, desc, bar, x, y, l2_policy((DENSE_GEMM_L2_HINT == 1) == (kOperand == 0)));
+#endif
+}
+
 // 2-D tiled store shared -> global (out-of-range rows/columns are clipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* desc, uint32_t src, int32_t x,
                                              int32_t y) {

@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
         if (tid == 0) {
           mbar_arrive_expect_tx(bar, (kCpA ? 0u : kAStageFloats * 4u) +
                                          (kCpB ? 0u : (uint32_t)kBStageFloats * 4u));
-          if constexpr (!kCpA) tma_load_2d(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
-          if constexpr (!kCpB) tma_load_2d(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
+          if constexpr (!kCpA) tma_load_operand<0>(smem_u32(sA + s * kAStageFloats), &tmA, bar, k0, m0);
+          if constexpr (!kCpB) tma_load_operand<1>(smem_u32(sB + s * kBStageFloats), &tmB, bar, n0, k0);
         }
       }
       if constexpr (kAnyCp) {

@@ -9,6 +9,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include "ptx.cuh"
+
 namespace dgemm {
 
 // ------------------------------------------------------------ tcgen05 PTX
@@ -129,27 +131,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r0)[32], uint32_t (&r1)[
         "+r"(r1[30]), "+r"(r1[31])
       :
       : "memory");
-}
-
-// Writes 32 consecutive FP32 columns of this thread's TMEM lane (the inverse
-// of tmem_ld32).  Asynchronous: tmem_st_wait() completes it.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-// Waits until this thread's tcgen05.st writes have been performed.
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 template <typename T>
@@ -312,6 +293,29 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(desc)), "r"(cluster_bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// tma_load_2d_pair with an L2 cache-policy operand.
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* desc,
+                                                      uint32_t cluster_bar, int32_t x, int32_t y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(cluster_bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// The pair load of operand kOperand (0 = A, 1 = B) under DENSE_GEMM_L2_HINT.
+template <int kOperand>
+__device__ __forceinline__ void tma_load_operand_pair(uint32_t dst, const CUtensorMap* desc,
+                                                      uint32_t cluster_bar, int32_t x, int32_t y) {
+#if DENSE_GEMM_L2_HINT == 0
+  tma_load_2d_pair(dst, desc, cluster_bar, x, y);
+#else
+  tma_load_2d_pair_hint(dst, desc, cluster_bar, x, y,
+                        l2_policy((DENSE_GEMM_L2_HINT == 1) == (kOperand == 0)));
+#endif
 }
 
 }  // namespace dgemm
