@@ -338,7 +338,8 @@ def run_ours(args, ws, rank, local):
     scaled = args.alpha != 1.0 or args.beta != 0.0
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     # This library's kernel launches per step: one per GEMM, plus the
-    # zeroing launch of an FP32 GEMM whose last wave is split along K and
+    # re-pitch launch of an FP32 GEMM with an operand TMA cannot address
+    # (the step's operands are row-major: both copies are one launch) and
     # the reduction launch of a split-K GEMM.
     launches_per_step = 0
     for c in cases:
@@ -348,8 +349,7 @@ def run_ours(args, ws, rank, local):
                                   sms)
         if plan.path == dg.PATH_NOOP:
             continue
-        launches_per_step += 1 + (1 if (w.dtype == "f32" and plan.split_tiles) else 0) + (
-            1 if plan.splitk_slices > 1 else 0)
+        launches_per_step += 1 + (1 if plan.splitk_slices > 1 else 0) + (1 if plan.pack else 0)
 
     def launch(c, s=sptr):
         w = c["w"]

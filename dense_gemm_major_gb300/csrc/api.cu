@@ -110,6 +110,39 @@ constexpr long long kSplitkWorkspaceCap = 64ll << 20;   // bytes
 constexpr int kPackMinReuse = 256;
 constexpr long long kPackMinWork = 1ll << 30;
 constexpr long long kPackCapBytes = 1ll << 30;
+// Re-pitching row-major FP32 operands whose base or leading dimension is not
+// 16-byte aligned (so that TMA can stage them): minimum M * N * K.
+constexpr long long kRepitchMinWork = 1ll << 29;
+
+inline long long round4(long long x) { return (x + 3) / 4 * 4; }
+
+// FP32 split-K slice count: the s in [2, min(nk, 32)] that minimises
+// ceil(tiles * s / sms) * (nk / s + kSgemmSliceCost), the k-tiles on the
+// busiest SM (two co-resident CTAs share its FMA pipe, so they count twice)
+// plus a fixed cost per slice (pipeline fill, partial store, reduction)
+// worth kSgemmSliceCost k-tiles; the smallest such s; then bounded so the
+// workspace stays under the cap.  Measured on GB300 (us, s = 2/4/8/16):
+// 256^3 23.2/17.1/15.0/-, 384^3 29.3/21.2/19.1/17.0 (12), 512^3
+// 33.4/25.3/21.1/21.1, 768^3 47.7/31.4/33.4/41.6, 256 x 256 x 1024
+// 55.9/33.4/23.2/21.1; the rule picks 8, 12, 9, 4 and 32.
+constexpr double kSgemmSliceCost = 2.0;
+int sgemm_splitk_slices(int tiles, int sms, int nk, int M, int N) {
+  if (tiles <= 0 || sms <= 0) return 1;
+  const int smax = nk < 32 ? nk : 32;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int s = 2; s <= smax; ++s) {
+    const double waves = (double)(((long long)tiles * s + sms - 1) / sms);
+    const double cost = waves * ((double)nk / s + kSgemmSliceCost);
+    if (best == 1 || cost < best_cost - 1e-9) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  const long long slice_bytes = (long long)M * (((long long)N + 3) / 4 * 4) * 4;
+  while (best > 1 && best * slice_bytes > kSplitkWorkspaceCap) --best;
+  return best >= 2 ? best : 1;
+}
 
 // Slices for a split-K problem, bounded so the workspace stays under the cap.
 int splitk_slices_capped(int tiles, int slots, int nk, int M, int N) {
@@ -223,6 +256,19 @@ int forced_sgemm_pack() {
   return v;
 }
 
+// Measurement override: DENSE_GEMM_SGEMM_REPITCH=0 never re-pitches an
+// unaligned row-major FP32 operand, =1 always does (-1 = no override).
+int forced_sgemm_repitch() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_SGEMM_REPITCH");
+    if (s == nullptr) return -1;
+    if (std::strcmp(s, "0") == 0) return 0;
+    if (std::strcmp(s, "1") == 0) return 1;
+    return -1;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_TC_STREAMK=0 turns off the pair kernel's
 // stream-K share (its last partial round then runs as column parts, or as
 // it is).
@@ -274,6 +320,19 @@ int forced_tc_kernel() {
     if (std::strcmp(s, "single") == 0) return 1;
     if (std::strcmp(s, "pair") == 0) return 2;
     return 0;
+  }();
+  return v;
+}
+
+// Measurement override: DENSE_GEMM_SGEMM_SLICES=s (2..32) runs every FP32
+// product as split-K with s slices (capped at one k-tile per slice); 0 = no
+// override.
+int forced_sgemm_slices() {
+  static const int v = [] {
+    const char* s = std::getenv("DENSE_GEMM_SGEMM_SLICES");
+    if (s == nullptr) return 0;
+    const int x = std::atoi(s);
+    return x >= 2 && x <= 32 ? x : 0;
   }();
   return v;
 }
@@ -359,9 +418,14 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   // (k-slices of narrow tiles into a workspace, then a reduction).
   double best_score = 1.0;
   sgemm_pick_tn(M, N, K, sms, &best_score);
-  const int slices = forced_sgemm_tn() || best_score >= kSgemmSplitkBelowScore
-                         ? 1
-                         : splitk_slices_capped(narrow_tiles, 2 * sms, nk_all, M, N);
+  int slices = forced_sgemm_tn() || best_score >= kSgemmSplitkBelowScore
+                   ? 1
+                   : sgemm_splitk_slices(narrow_tiles, sms, nk_all, M, N);
+  if (const int fs = forced_sgemm_slices()) {
+    const long long slice_bytes = (long long)M * (((long long)N + 3) / 4 * 4) * 4;
+    slices = fs < nk_all ? fs : nk_all;
+    while (slices > 1 && slices * slice_bytes > kSplitkWorkspaceCap) --slices;
+  }
   if (slices > 1) {
     plan->block_m = dgemm::kSgemmBM;
     plan->block_n = dgemm::sgemm_bn(8);
@@ -389,9 +453,10 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   // one CTA per slot; all full waves but the last one or two run as whole
   // tiles, and each CTA takes an equal share of the remaining tiles'
   // (tile, k-tile) iteration space (hybrid stream-K); a range boundary
-  // inside a tile cuts it into two pieces.  With beta == 0 the pieces add
-  // into zeroed C; with beta != 0 they store FP32 partials to a workspace
-  // (two tiles per boundary) that a fixup kernel combines.
+  // inside a tile cuts it into two pieces, which meet through a pair of
+  // flag words per boundary.  With beta == 0 the second piece to finish
+  // adds into the first one's C; with beta != 0 the first leaves FP32
+  // partial sums in a workspace (one tile per boundary) for the second.
   const int slots = (tn == 8 ? 2 : 1) * sms;
   const int nk = ceil_div(K, dgemm::kSgemmBK);
   // (A single wave of at most half the slots runs as two CTAs per tile:
@@ -405,16 +470,18 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   plan->splitk_slices = 1;
   if (plan->split_tiles && beta != 0.f)
     plan->workspace_bytes =
-        (long long)(grid - 1) * 2 * dgemm::kSgemmBM * plan->block_n * 4;
+        (long long)(grid - 1) * dgemm::kSgemmBM * plan->block_n * 4;
   plan->ctas = grid;
   return GEMM_OK;
 }
 
 // pair_clusters: CTA pairs of the pair kernel that can be resident at once
-// (0: num_sms / 2, every SM).
+// (0: num_sms / 2, every SM).  allow_copy false: no FP32 operand is copied
+// into scratch (transposed or re-pitched) whatever the product's size.
 gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
                         const void* A, int lda, const void* B, int ldb, float beta, const void* C,
-                        int ldc, int num_sms, int pair_clusters, gemm_plan_t* plan) {
+                        int ldc, int num_sms, int pair_clusters, gemm_plan_t* plan,
+                        bool allow_copy = true) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
@@ -462,7 +529,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     // (measured on GB300: 4096^3 TN +15.6 % staged, +1.3 % packed; 2048^3
     // +32 % / +3.5 %; 1024^3 +16 % / +10 %; 512^3 +17 % / +25 %;
     // 4096 x 128 x 4096 TN +23 % / +30 %).
-    if (op_a || op_b) {
+    if ((op_a || op_b) && allow_copy) {
       const long long rows = op_a ? M : K, cols = op_a ? K : N;
       const long long bytes = rows * ((cols + 3) / 4 * 4) * 4;
       const int reuse = op_a ? N : M;
@@ -471,9 +538,35 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
                                         (long long)M * N * K >= kPackMinWork &&
                                         bytes <= kPackCapBytes);
       if (pack) {
+        // The other (row-major) operand is re-pitched as well when TMA
+        // cannot address it (the product is far above kRepitchMinWork) and
+        // both copies fit under the cap.
+        const bool other16 = op_a ? b16 : a16;
+        const long long other =
+            (op_a ? (long long)K * round4(N) : (long long)M * round4(K)) * 4;
+        const long long total = (bytes + 255) / 256 * 256 + (other + 255) / 256 * 256;
+        const bool both = !other16 && total <= kPackCapBytes;
         const gemm_status_t st =
-            plan_sgemm(M, N, K, 0, 0, op_a ? true : a16, op_b ? true : b16, beta, sms, plan);
-        plan->pack = op_a ? 1 : 2;
+            plan_sgemm(M, N, K, 0, 0, true, both || other16, beta, sms, plan);
+        plan->pack = (op_a ? 1 : 2) | (both ? (op_a ? 2 : 1) : 0);
+        plan->pack_bytes = both ? total : bytes;
+        return st;
+      }
+    }
+    // Row-major operands whose base or leading dimension is not 16-byte
+    // aligned cannot be staged by TMA; 4-byte cp.async staging costs the
+    // product ~35 % (FMA pipe 57 % busy against 82 %).  Large enough
+    // products first copy such an operand into scratch with 16-byte rows
+    // (HBM-bound, every element read and written once) and run with TMA.
+    if (!op_a && !op_b && (!a16 || !b16) && allow_copy) {
+      const long long bytes_a = a16 ? 0 : (long long)M * round4(K) * 4;
+      const long long bytes_b = b16 ? 0 : (long long)K * round4(N) * 4;
+      const long long bytes = (bytes_a + 255) / 256 * 256 + bytes_b;
+      const int forced = forced_sgemm_repitch();
+      if (forced == 1 || (forced == -1 && (long long)M * N * K >= kRepitchMinWork &&
+                          bytes <= kPackCapBytes)) {
+        const gemm_status_t st = plan_sgemm(M, N, K, 0, 0, true, true, beta, sms, plan);
+        plan->pack = (a16 ? 0 : 1) | (b16 ? 0 : 2);
         plan->pack_bytes = bytes;
         return st;
       }
@@ -615,12 +708,15 @@ void tc_schedule_params(const gemm_plan_t& plan, int M, int N, dgemm::TcParams* 
   }
 }
 
+// fixed_flags: flag words for the FP32 stream-K hand-over supplied by the
+// caller (gemm_f32_noalloc) instead of the stream's library-owned array.
 gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alpha, const void* A,
                   int lda, const void* B, int ldb, float beta, void* C, int ldc,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool allow_copy = true,
+                  const dgemm::FixedFlags* fixed_flags = nullptr) {
   gemm_plan_t plan;
-  gemm_status_t st =
-      plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 1, 0, &plan);
+  gemm_status_t st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                               1, 0, &plan, allow_copy);
   if (st != GEMM_OK) return st;
   if (plan.path == GEMM_PATH_NOOP) return GEMM_OK;
   DeviceInfo* dev = nullptr;
@@ -628,7 +724,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
   if (st != GEMM_OK) return st;
   // Re-plan with the device's SM count (validation above needs no device).
   st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms,
-                 dev->pair_clusters, &plan);
+                 dev->pair_clusters, &plan, allow_copy);
   if (st != GEMM_OK) return st;
   cudaError_t e = cudaSuccess;
 
@@ -644,27 +740,44 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     int klda = swap ? ldb : lda, kldb = swap ? lda : ldb;
     int kop_a = swap ? 0 : op_a, kop_b = swap ? 0 : op_b;
     if (plan.pack) {
-      // A stored K x M becomes M x K; B stored N x K becomes K x N.
+      // Each copied operand becomes row-major with 16-byte rows in scratch:
+      // A stored K x M is transposed into M x K, B stored N x K into K x N;
+      // row-major operands are re-pitched, both in one launch.  A's copy
+      // comes first.
       float* packed = nullptr;
       st = get_workspace(stream, (size_t)plan.pack_bytes, &packed, kWsPack);
       if (st != GEMM_OK) return st;
-      const bool pa = plan.pack == 1;
-      const long long rows = pa ? K : N, cols = pa ? M : K;
-      const long long ldp = (rows + 3) / 4 * 4;
-      e = dgemm::launch_transpose_f32(static_cast<const float*>(pa ? A : B), rows, cols,
-                                      pa ? lda : ldb, packed, ldp, dev->sms, stream);
+      float* dst = packed;
+      dgemm::RepitchJob jobs[2];
+      int njobs = 0;
+      for (int which = 0; which < 2 && e == cudaSuccess; ++which) {
+        if (!(plan.pack & (1 << which))) continue;
+        const bool is_a = which == 0;
+        const bool trans = is_a ? op_a != 0 : op_b != 0;
+        const long long rows = is_a ? M : K, cols = is_a ? K : N;   // of the copy
+        const long long ldp = round4(cols);
+        const float* src = static_cast<const float*>(is_a ? A : B);
+        const long long lds = is_a ? lda : ldb;
+        if (trans)
+          e = dgemm::launch_transpose_f32(src, cols, rows, lds, dst, ldp, dev->sms, stream);
+        else
+          jobs[njobs++] = dgemm::RepitchJob{src, rows, cols, lds, dst, ldp};
+        if (is_a) {
+          kA = dst;
+          klda = (int)ldp;
+          kop_a = 0;
+        } else {
+          kB = dst;
+          kldb = (int)ldp;
+          kop_b = 0;
+        }
+        dst += (rows * ldp + 63) / 64 * 64;
+      }
+      if (e == cudaSuccess && njobs > 0)
+        e = dgemm::launch_repitch_f32(jobs, njobs, dev->sms, stream);
       if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
-      }
-      if (pa) {
-        kA = packed;
-        klda = (int)ldp;
-        kop_a = 0;
-      } else {
-        kB = packed;
-        kldb = (int)ldp;
-        kop_b = 0;
       }
     }
     dgemm::SgemmParams p;
@@ -693,9 +806,23 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
       if (st != GEMM_OK) return st;
     }
-    if (p.slices == 1 && plan.split_tiles > 0 && plan.workspace_bytes > 0) {
-      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.tail_ws);
-      if (st != GEMM_OK) return st;
+    if (p.slices == 1 && plan.split_tiles > 0) {
+      if (plan.workspace_bytes > 0) {
+        st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.tail_ws);
+        if (st != GEMM_OK) return st;
+      }
+      const long long words = 2ll * (plan.ctas - 1);
+      if (fixed_flags != nullptr) {
+        if (words > fixed_flags->words) return GEMM_ERR_SCRATCH_LIMIT;
+        p.sk_flags = fixed_flags->flags;
+        p.epoch = fixed_flags->epoch;
+      } else {
+        float* flags = nullptr;
+        st = get_workspace(stream, (size_t)words * 4, &flags, kWsFlags);
+        if (st != GEMM_OK) return st;
+        p.sk_flags = reinterpret_cast<unsigned*>(flags);
+        p.epoch = next_epoch(stream);
+      }
     }
     p.alpha = alpha;
     p.beta = beta;
@@ -797,6 +924,19 @@ unsigned* current_fault_word() {
   return current_device(&dev) == GEMM_OK ? dev->fault : nullptr;
 }
 unsigned long long wait_bound_ns() { return wait_timeout_ns(); }
+
+gemm_status_t plan_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
+                               int ldb, const float* C, int ldc, int num_sms, gemm_plan_t* plan) {
+  return plan_impl(0, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, num_sms, 0,
+                   plan, false);
+}
+
+gemm_status_t run_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
+                              int ldb, float* C, int ldc, cudaStream_t stream,
+                              const FixedFlags& flags) {
+  return run(0, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream, false,
+             &flags);
+}
 
 bool pdl_enabled() {
   static const bool v = [] {

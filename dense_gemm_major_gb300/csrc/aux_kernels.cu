@@ -1,7 +1,7 @@
 // Small kernels around the GEMM path: the K == 0 / alpha == 0 product
 // (C := beta * C), the split-K slice reduction, the FP32 operand transpose
-// that packs a transposed operand into row-major scratch, and the self-test
-// of the bounded mbarrier wait.
+// that packs a transposed operand into row-major scratch, the re-pitch of
+// an operand with unaligned rows, and the self-tests of the bounded waits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -132,7 +132,43 @@ __global__ void __launch_bounds__(kTrThreads)
   }
 }
 
+// Copies each job's S (lds) into D (ldd, 16-byte rows): item i of the
+// grid-stride loop over both jobs' quads takes the 4 columns 4q .. 4q + 3
+// of one row, reads them as scalars (a warp reads 512 contiguous bytes) and
+// writes one 16-byte store; columns from cols on are written as zeros.
+__global__ void __launch_bounds__(256)
+    repitch_f32_kernel(RepitchJob j0, RepitchJob j1, int njobs) {
+  const long long q0 = j0.rows * (j0.ldd / 4);
+  const long long total = q0 + (njobs > 1 ? j1.rows * (j1.ldd / 4) : 0);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const bool second = i >= q0;
+    const RepitchJob& j = second ? j1 : j0;
+    const long long k = second ? i - q0 : i;
+    const long long quads = j.ldd / 4;
+    const long long r = k / quads, c = (k - r * quads) * 4;
+    const float* src = j.S + r * j.lds + c;
+    float4 v;
+    v.x = c < j.cols ? __ldcs(src) : 0.f;
+    v.y = c + 1 < j.cols ? __ldcs(src + 1) : 0.f;
+    v.z = c + 2 < j.cols ? __ldcs(src + 2) : 0.f;
+    v.w = c + 3 < j.cols ? __ldcs(src + 3) : 0.f;
+    *reinterpret_cast<float4*>(j.D + r * j.ldd + c) = v;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_repitch_f32(const RepitchJob* jobs, int njobs, int sms, cudaStream_t stream) {
+  if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+  long long total = 0;
+  for (int i = 0; i < njobs; ++i) total += jobs[i].rows * (jobs[i].ldd / 4);
+  long long blocks = (long long)(sms > 0 ? sms : 1) * 8;
+  if (blocks * 256 > total) blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  repitch_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(jobs[0], jobs[njobs - 1], njobs);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long long ldw,
                                  void* C, long long ldc, int elem, float alpha, float beta,

@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "dense_gemm.h"
+
 namespace dgemm {
 
 // ---------------------------------------------------------------- FP32 SIMT
@@ -43,18 +45,23 @@ struct SgemmParams {
   // [c * total / G, (c + 1) * total / G) of the iteration space of the
   // remaining tiles, total = (tiles - dp_tiles) * nk (G <= tiles - dp_tiles,
   // or G = 2 tiles with dp_tiles = 0), one unit per tile it touches.
-  // split_tiles tiles are cut by a range boundary into two pieces.  With
-  // tail_ws == nullptr (only when beta = 0) both pieces add alpha times
-  // their FP32 partial sums into C, which is zeroed first; with exactly two
-  // addends the result does not depend on their order.  Otherwise the
-  // pieces of the tile cut by boundary c store their partial sums at
-  // tail_ws + (2 (c - 1) + piece) * BM * BN (row-major, leading dimension
-  // BN) and a fixup kernel writes alpha * (piece 0 + piece 1) + beta * C, in
-  // that order, so the result is again independent of scheduling.
+  // split_tiles tiles are cut by a range boundary into two pieces, which
+  // meet through boundary c's words sk_flags[2 (c - 1)] (arrival: the
+  // first piece to finish finds a value other than epoch there) and
+  // sk_flags[2 (c - 1) + 1] (done: set to epoch once the first piece's
+  // result is visible).  With tail_ws == nullptr (only when beta = 0) the
+  // first piece stores alpha times its FP32 sums to C and the second adds
+  // alpha times its own into it; otherwise the first stores its unscaled
+  // sums at tail_ws + (c - 1) * BM * BN (row-major, leading dimension BN)
+  // and the second writes alpha * (sum + sum) + beta * C.  With exactly two
+  // addends the result does not depend on which piece came first.  The
+  // flags need no reset between launches: each launch brings a new epoch.
   int grid;
   int dp_tiles = 0;
   int split_tiles;
   float* tail_ws = nullptr;
+  unsigned* sk_flags = nullptr;   // 2 (grid - 1) words when split_tiles > 0
+  unsigned epoch = 0;             // non-zero, new for every launch
   // Split-K mode (slices > 1): CTA u computes k-slice u % slices of tile
   // u / slices (k-tiles [s*nk/slices, (s+1)*nk/slices)) and stores its FP32
   // partial tile at ws + s * M * ldw (row-major, leading dimension ldw);
@@ -93,9 +100,7 @@ __host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, in
 
 // tn: 8 (narrow) or 16 (wide).  use_tma: A and B are staged by TMA
 // (16-byte aligned bases and strides); otherwise by 4-byte cp.async with
-// zero fill.  When p.split_tiles > 0, first zeroes C on the cut tiles
-// (tail_ws == nullptr) or afterwards combines their pieces (one extra launch
-// either way).  Returns the launch error.
+// zero fill.  Returns the launch error.
 cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUtensorMap* tmA,
                          const CUtensorMap* tmB, cudaStream_t stream);
 
@@ -420,6 +425,18 @@ cudaError_t launch_splitk_reduce(const float* ws, int slices, int M, int N, long
 cudaError_t launch_transpose_f32(const float* S, long long rows, long long cols, long long lds,
                                  float* D, long long ldd, int sms, cudaStream_t stream);
 
+// One re-pitch copy: D (rows x cols, row pitch ldd, a multiple of 4,
+// 16-byte aligned) := S (row pitch lds, any 4-byte alignment), FP32; the
+// padding columns of D are zeroed.  D must not overlap S.
+struct RepitchJob {
+  const float* S;
+  long long rows, cols, lds;
+  float* D;
+  long long ldd;
+};
+
+// Re-pitches 1 or 2 operands whose rows TMA cannot address, in one launch.
+cudaError_t launch_repitch_f32(const RepitchJob* jobs, int njobs, int sms, cudaStream_t stream);
 // C := beta * C on an M x N block (C is not read when beta == 0): the
 // product when K == 0 or alpha == 0.
 cudaError_t launch_scale_c(void* C, int M, int N, long long ldc, int elem, float beta,
@@ -442,6 +459,26 @@ inline int splitk_slices(int tiles, int slots, int nk) {
 // every device-side wait, from the C-ABI translation unit.
 unsigned* current_fault_word();
 unsigned long long wait_bound_ns();
+
+// Caller-owned flag words for the FP32 stream-K hand-over (SgemmParams::
+// sk_flags): `words` of them, written by nothing but the GEMM kernels, and
+// the launch's epoch (non-zero, new for every launch that uses them).
+struct FixedFlags {
+  unsigned* flags;
+  long long words;
+  unsigned epoch;
+};
+
+// gemm_plan / gemm_f32 (beta = 0) that never copy an operand into library
+// scratch (an unaligned row-major operand is then staged by 4-byte
+// cp.async) and take the stream-K flags from `flags`
+// (GEMM_ERR_SCRATCH_LIMIT if too few); run_f32_no_copy allocates nothing
+// unless the plan is split-K.
+gemm_status_t plan_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
+                               int ldb, const float* C, int ldc, int num_sms, gemm_plan_t* plan);
+gemm_status_t run_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
+                              int ldb, float* C, int ldc, cudaStream_t stream,
+                              const FixedFlags& flags);
 
 // Whether the GEMM kernels are launched as programmatic dependents of the
 // kernel before them (DENSE_GEMM_PDL=0 turns it off, for measurement).

@@ -1,8 +1,10 @@
 // gemm_f32_noalloc: the FP32 GEMM for callers that cannot allocate device
 // memory (see include/dense_gemm.h).  Split-K problems keep their FP32
 // partial tiles in the fixed array below instead of a library-allocated
-// workspace; everything else goes to gemm_f32, which allocates nothing for
-// those problems.
+// workspace; everything else runs as gemm_f32 with operand copies turned
+// off (an unaligned operand is staged by cp.async, never re-pitched into
+// scratch) and the stream-K hand-over flags taken from a fixed array too.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -18,13 +20,19 @@ namespace {
 // the symbol as a pointer; it only names the array for cudaGetSymbolAddress.
 constexpr size_t kScratchBytes = 16u << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchBytes / sizeof(float)];
+// The stream-K hand-over flags of the calls that are not split-K (two words
+// per CTA boundary; zero at load, then only ever set to a call's epoch).
+constexpr long long kFlagWords = 8192;
+static __device__ unsigned g_noalloc_flags[kFlagWords];
 
 constexpr int kMaxDevices = 64;
 
 struct ScratchDevice {
   bool ready = false;
   float* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+  unsigned* flags = nullptr;  // device address of g_noalloc_flags
   int sms = 0;
+  std::atomic<unsigned> epoch{0};
 };
 
 std::mutex g_mu;
@@ -42,7 +50,9 @@ gemm_status_t scratch_device(ScratchDevice** out) {
   ScratchDevice& d = g_dev[dev];
   if (!d.ready) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+    void* fptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&fptr, g_noalloc_flags) != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_UNSUPPORTED_DEVICE;
     }
@@ -53,6 +63,7 @@ gemm_status_t scratch_device(ScratchDevice** out) {
       return GEMM_ERR_UNSUPPORTED_DEVICE;
     }
     d.scratch = static_cast<float*>(ptr);
+    d.flags = static_cast<unsigned*>(fptr);
     d.sms = sms;
     d.ready = true;
   }
@@ -69,16 +80,21 @@ extern "C" gemm_status_t gemm_f32_noalloc(int M, int N, int K, const float* A, i
                                           cudaStream_t stream) {
   // Argument checks first (no device needed), as for gemm_f32.
   gemm_plan_t plan;
-  gemm_status_t st = gemm_plan(0, M, N, K, A, lda, B, ldb, C, ldc, 1, &plan);
+  gemm_status_t st = dgemm::plan_f32_no_copy(M, N, K, A, lda, B, ldb, C, ldc, 1, &plan);
   if (st != GEMM_OK || plan.path == GEMM_PATH_NOOP) return st;
   ScratchDevice* dev = nullptr;
   st = scratch_device(&dev);
   if (st != GEMM_OK) return st;
   unsigned* fault = dgemm::current_fault_word();
   if (fault == nullptr) return GEMM_ERR_UNSUPPORTED_DEVICE;
-  st = gemm_plan(0, M, N, K, A, lda, B, ldb, C, ldc, dev->sms, &plan);
+  st = dgemm::plan_f32_no_copy(M, N, K, A, lda, B, ldb, C, ldc, dev->sms, &plan);
   if (st != GEMM_OK) return st;
-  if (plan.splitk_slices <= 1) return gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream);
+  if (plan.splitk_slices <= 1) {
+    unsigned e = ++dev->epoch;
+    if (e == 0) e = ++dev->epoch;
+    const dgemm::FixedFlags flags{dev->flags, kFlagWords, e};
+    return dgemm::run_f32_no_copy(M, N, K, A, lda, B, ldb, C, ldc, stream, flags);
+  }
   if (plan.workspace_bytes > (long long)kScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
 
   // Split-K with the static scratch: the narrow SIMT tile, tiles staged by

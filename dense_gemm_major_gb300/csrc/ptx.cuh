@@ -296,6 +296,7 @@ enum FaultCode : unsigned {
   kFaultDrainWait = 1u << 5,
   kFaultTcPairTmem = 1u << 6,   // the two CTAs of a pair got different TMEM bases
   kFaultTcPartialWait = 1u << 7,   // a K-split piece's partial never arrived
+  kFaultSgemmPieceWait = 1u << 8,  // an SGEMM stream-K piece's partner never published
 };
 
 __device__ __forceinline__ void raise_fault(unsigned* fault, unsigned code) {

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
 
   extern __shared__ unsigned char smem_raw[];
   __shared__ int s_abort;
+  __shared__ int s_second;   // this CTA's cut piece got to its tile second
   unsigned char* const base = align_smem_1024(smem_raw);
   float* sA = reinterpret_cast<float*>(base);
   float* sB = sA + S * kAStageFloats;
@@ -231,9 +232,9 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   // nk): every CTA then works at k-tile tau or tau - (share mod nk) of its
   // units at time tau, so the share's A and B panels are read in two fronts
   // instead of at as many k offsets as there are CTAs, and L2 holds the
-  // slices in between (the two pieces of a cut tile add into C in either
-  // order, or combine from the workspace in a fixed one).  Measured on
-  // GB300 at 4096^3: DRAM traffic 435 -> 389 MB per launch, same time.
+  // slices in between (the two pieces of a cut tile combine in whichever
+  // order they finish, see below).  Measured on GB300 at 4096^3: DRAM
+  // traffic 435 -> 389 MB per launch, same time.
   const int nk_all = (p.K + BK - 1) / BK;
   const int b = blockIdx.x;
   int dp_next = b;
@@ -478,23 +479,67 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     long long part_ld = 0;
     int part_m0 = 0, part_n0 = 0;
     bool add_into_c = false;
+    unsigned* done_flag = nullptr;   // set to p.epoch once this unit's stores are visible
     if (p.slices > 1) {
       part = p.ws + (long long)(b % p.slices) * p.M * p.ldw;
       part_ld = p.ldw;
     } else if (k_begin != 0 || k_end != nk_all) {
       // One of the two pieces of a tile cut by boundary cb (the first k-tile
-      // of CTA cb): piece 0 ends this CTA's range, piece 1 starts it.
-      if (p.tail_ws != nullptr) {
-        const int piece = k_begin == 0 ? 0 : 1;
-        const int cb = piece == 0 ? b + 1 : b;
-        part = p.tail_ws + ((long long)(cb - 1) * 2 + piece) * (BM * BN);
-        part_ld = BN;
-        part_m0 = m0;
-        part_n0 = n0;
+      // of CTA cb): piece 0 ends CTA cb - 1's range, piece 1 starts CTA cb's.
+      // Whichever piece finishes first publishes its sums and raises the
+      // boundary's done flag; the second waits for that flag (the first has
+      // already finished its k-loop, so the wait is short and needs no
+      // co-residency) and completes the tile.  With beta == 0 the first
+      // stores alpha * sums to C and the second adds alpha * its sums into
+      // it; otherwise the first leaves its unscaled sums in the boundary's
+      // workspace tile and the second adds them to its accumulators and
+      // writes alpha * total + beta * C.  Two addends give the same sum in
+      // either order, so the result does not depend on which came first.
+      const int cb = k_begin == 0 ? b + 1 : b;
+      unsigned* arrive = p.sk_flags + 2 * (cb - 1);
+      if (tid == 0) {
+        const bool second = atomicExch(arrive, p.epoch) == p.epoch;
+        if (second && !flag_wait_equal(arrive + 1, p.epoch, p.timeout_ns, nullptr))
+          raise_fault(p.fault, kFaultSgemmPieceWait);
+        s_second = second ? 1 : 0;
+      }
+      __syncthreads();
+      float* const slot =
+          p.tail_ws != nullptr ? p.tail_ws + (long long)(cb - 1) * (BM * BN) : nullptr;
+      if (!s_second) {
+        done_flag = arrive + 1;
+        if (slot != nullptr) {
+          part = slot;
+          part_ld = BN;
+          part_m0 = m0;
+          part_n0 = n0;
+        }
+      } else if (slot != nullptr) {
+        // (The slot holds the first piece's sums at every element of the
+        // tile inside C; the others are never stored.)
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+  #pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(
+                slot + (a_row0 + 4 * i) * BN + b_col0 + 32 * h));
+            const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+            const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+            acc[i][2 * h + 0] = pack_pair(lo.x + o.x, lo.y + o.y);
+            acc[i][2 * h + 1] = pack_pair(hi.x + o.z, hi.y + o.w);
+          }
+        }
       } else {
         add_into_c = true;
       }
     }
+    // After the first piece's stores: make them visible, then raise the flag.
+    const auto publish = [&]() {
+      if (done_flag == nullptr) return;
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) flag_store_release(done_flag, p.epoch);
+    };
 
     // Scaling pass, C := alpha * (A.B) + beta * C, applied to the
     // accumulators in place before any store (partial sums for a workspace
@@ -593,6 +638,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           }
         }
       }
+      publish();
       g0 += nk;
       continue;
     }
@@ -640,89 +686,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
         }
       }
     }
+    publish();
     g0 += nk;
-  }
-}
-
-// Boundary c (0 < c < G) of the stream-K split is the first k-tile of CTA c
-// in the stream-K tiles' iteration space, c * total / G.  When it is not a
-// multiple of nk it cuts tile dp_tiles + boundary / nk into two pieces: CTA
-// c-1's last unit and CTA c's first.  Returns that tile, or -1.  The host
-// counts the same boundaries.
-__device__ __forceinline__ int cut_tile(const SgemmParams& p, int c, int G) {
-  const int nk = (p.K + BK - 1) / BK;
-  const long long total = (long long)(p.tiles_m * p.tiles_n - p.dp_tiles) * nk;
-  const long long bnd = (long long)c * total / G;
-  return bnd % nk != 0 ? p.dp_tiles + (int)(bnd / nk) : -1;
-}
-
-// Writes C := alpha * (piece 0 + piece 1) + beta * C on the tile cut by
-// boundary c = blockIdx.x + 1 from its two partial sums in tail_ws (slots
-// 2 (c - 1) and 2 (c - 1) + 1).  Block (c - 1, y) takes 2048 consecutive
-// elements (2048 / bn rows) of that tile, 8 per thread at a stride of 256;
-// every thread issues all its loads before its first store, so the loads
-// overlap.
-constexpr int kFixupElems = 2048;
-__global__ void __launch_bounds__(256) sgemm_tail_fixup(const SgemmParams p, int bn, int G) {
-  const int c = (int)blockIdx.x + 1;
-  const int tile = cut_tile(p, c, G);
-  if (tile < 0) return;
-  int tm, tn;
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int rows = min(BM, p.M - tm * BM);
-  const int cols = min(bn, p.N - tn * bn);
-  const float* __restrict__ p0 = p.tail_ws + (long long)(2 * (c - 1)) * (BM * bn);
-  const float* __restrict__ p1 = p0 + BM * bn;
-  const int r0 = tm * BM, cl0 = tn * bn;
-  const int first = (int)blockIdx.y * kFixupElems;
-  constexpr int kPer = kFixupElems / 256;
-  float v[kPer], old[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = first + (int)threadIdx.x + 256 * q;
-    const int r = idx / bn;
-    const int cc = idx - r * bn;
-    v[q] = 0.f;
-    old[q] = 0.f;
-    if (r < rows && cc < cols) {
-      v[q] = p0[idx] + p1[idx];
-      if (p.beta != 0.f) old[q] = p.C[c_index(p, r0 + r, cl0 + cc)];
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int idx = first + (int)threadIdx.x + 256 * q;
-    const int r = idx / bn;
-    const int cc = idx - r * bn;
-    if (r < rows && cc < cols) {
-      const float a = p.alpha * v[q];
-      p.C[c_index(p, r0 + r, cl0 + cc)] = p.beta != 0.f ? fmaf(p.beta, old[q], a) : a;
-    }
-  }
-}
-
-// Zeroes C on the tile cut by boundary blockIdx.x + 1 (if any) before its
-// two pieces add into it; block y takes rows y, y + gridDim.y, ... of the
-// tile, with 16-byte stores when C's rows allow them.
-constexpr int kZeroRowSplit = 16;
-__global__ void __launch_bounds__(256) sgemm_zero_split_tiles(const SgemmParams p, int bn,
-                                                              int G) {
-  const int tile = cut_tile(p, (int)blockIdx.x + 1, G);
-  if (tile < 0) return;
-  int tm, tn;
-  grouped_tile(tile, p.tiles_m, p.tiles_n, kSgemmGroupM, tm, tn);
-  const int rows = min(BM, p.M - tm * BM);
-  const int cols = min(bn, p.N - tn * bn);
-  const bool vec = p.c_vec4 != 0 && !p.c_trans && cols % 4 == 0;
-  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
-    if (vec) {
-      float4* row = reinterpret_cast<float4*>(p.C + (long long)(tm * BM + r) * p.ldc + tn * bn);
-      for (int c = threadIdx.x; c < cols / 4; c += blockDim.x)
-        row[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      for (int c = threadIdx.x; c < cols; c += blockDim.x)
-        p.C[c_index(p, tm * BM + r, tn * bn + c)] = 0.f;
-    }
   }
 }
 
@@ -738,19 +703,8 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
   const int tiles = p.tiles_m * p.tiles_n;
   // Stream-K: G = p.grid CTAs (<= tiles); p.split_tiles tiles are cut in two.
   const int G = p.slices > 1 ? tiles * p.slices : p.grid;
-  const bool cuts = p.slices == 1 && p.split_tiles > 0;
-  if (cuts && p.tail_ws == nullptr) {
-    sgemm_zero_split_tiles<<<dim3((unsigned)(G - 1), kZeroRowSplit), 256, 0, stream>>>(
-        p, sgemm_bn(TN), G);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  e = launch_gemm_kernel(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>, dim3(G),
-                         dim3(kSgemmThreads), sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
-  if (e != cudaSuccess || !cuts || p.tail_ws == nullptr) return e;
-  const dim3 fixup_grid((unsigned)(G - 1), (unsigned)(BM * sgemm_bn(TN) / kFixupElems));
-  sgemm_tail_fixup<<<fixup_grid, 256, 0, stream>>>(p, sgemm_bn(TN), G);
-  return cudaGetLastError();
+  return launch_gemm_kernel(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>, dim3(G),
+                            dim3(kSgemmThreads), sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
 }
 
 }  // namespace

@@ -26,16 +26,20 @@
  *    never written.
  *  - Every pointer is caller-owned DEVICE memory of the current device.  The
  *    work is queued on `stream` and the call returns without synchronising.
- *  - Device memory: a call whose output has too few tiles to fill the GPU
- *    and a long K runs as split-K and needs an FP32 workspace (at most
- *    64 MiB, see gemm_plan_t.workspace_bytes; FP32 scaled calls also keep
- *    stream-K partial tiles there).  gemm_f32_op with exactly one operand
- *    transposed may copy it, transposed, into a second scratch array
- *    (gemm_plan_t.pack_bytes, at most 1 GiB).  The library owns one of
- *    each per (device, stream): it is allocated by the first call that
- *    needs it and grown, after synchronising that stream, when a later call
- *    needs more; it lives until the process exits.  Calls on different
- *    streams never share one.  All other calls allocate nothing.
+ *  - Device memory: the library owns up to three arrays per (device,
+ *    stream), each allocated by the first call that needs it and grown,
+ *    after synchronising that stream, when a later call needs more; they
+ *    live until the process exits and calls on different streams never
+ *    share one.  (1) An FP32 workspace (gemm_plan_t.workspace_bytes, at most
+ *    64 MiB): split-K slices, the FP16/BF16 pair kernel's stream-K partial
+ *    tiles, and the FP32 stream-K partial tiles of scaled calls with
+ *    beta != 0.  (2) An operand copy (gemm_plan_t.pack_bytes, at most
+ *    1 GiB): FP32 calls with exactly one operand stored transposed, or with
+ *    a row-major operand whose base or leading dimension is not 16-byte
+ *    aligned (gemm_plan_t.pack).  (3) A flag array of at most 16 bytes per
+ *    CTA: the hand-over flags of any grid whose tiles are cut into two
+ *    pieces (gemm_plan_t.split_tiles with CTA pairs or FP32 stream-K).
+ *    Calls whose plan needs none of these allocate nothing.
  *  - Accumulation is FP32 in every type.  FP16 / BF16 results are rounded to
  *    nearest-even once, from the FP32 accumulator.
  *  - Errors: argument problems are reported synchronously, before anything
@@ -79,7 +83,9 @@ typedef enum gemm_status_t {
  * for sm_103a with a TMA-fed multi-stage ring and an 8x8 or 8x16 per-thread
  * tile chosen by problem size.
  * Any alignment is accepted: when a base pointer or lda/ldb is not 16-byte
- * aligned the tiles are staged with 4-byte cp.async instead of TMA.
+ * aligned the operand is either copied into library scratch with 16-byte
+ * rows (products of at least 2^28 multiply-adds, gemm_plan_t.pack) or its
+ * tiles are staged with 4-byte cp.async instead of TMA.
  */
 gemm_status_t gemm_f32(int M, int N, int K,
                        const float *A, int lda,
@@ -111,13 +117,15 @@ gemm_status_t gemm_bf16(int M, int N, int K,
  * counterpart: this entry point exists for callers that cannot call
  * cudaMalloc, for example a serving process that reserves its whole memory
  * budget at start-up and may not allocate afterwards, or code whose latency
- * path cannot afford cudaMalloc's implicit synchronisation.  gemm_f32 needs a
- * library-allocated workspace only for split-K problems (few output tiles,
- * long K); this variant runs those with the same kernels but keeps the FP32
- * partial tiles in one fixed, library-wide device array of 16 MiB instead.
+ * path cannot afford cudaMalloc's implicit synchronisation.  gemm_f32 needs
+ * library-allocated memory only for split-K problems (few output tiles, long
+ * K) and for large products with an operand TMA cannot address (re-pitched
+ * into scratch); this variant runs split-K with the same kernels but keeps
+ * the FP32 partial tiles in one fixed, library-wide device array of 16 MiB
+ * instead, and stages an unaligned operand with cp.async in place.
  *
  * Same arguments, conventions and results as gemm_f32.  Problems that are
- * not split-K go to gemm_f32 unchanged (it allocates nothing for them).
+ * not split-K run as gemm_f32 without operand copies (nothing allocated).
  * A split-K problem whose partial tiles need more than 16 MiB
  * (gemm_plan_t.workspace_bytes) is refused with GEMM_ERR_SCRATCH_LIMIT
  * before anything is queued.
@@ -305,12 +313,16 @@ typedef struct gemm_plan_t {
                         tiles go to a workspace, summed in slice order by a
                         second kernel                                     */
   long long workspace_bytes; /* device workspace that split-K needs        */
-  int pack;          /* FP32 with exactly one operand stored transposed:
-                        1 (A) or 2 (B) when that operand is first copied,
-                        transposed, into a row-major scratch array of
-                        pack_bytes by an HBM-bound kernel, and the product
-                        then runs as the row-major one (path and tiles
-                        above describe that run); 0 when nothing is packed */
+  int pack;          /* FP32: bit 0 (A) and bit 1 (B) mark an operand
+                        that is first copied by an HBM-bound kernel into
+                        row-major scratch with 16-byte aligned rows (A's
+                        copy first, 256-byte aligned, then B's; pack_bytes
+                        in all): an operand stored transposed (exactly one
+                        of the two) is transposed, a row-major one whose
+                        base or leading dimension is not 16-byte aligned
+                        is re-pitched.  The product then runs as the
+                        row-major TMA one (path and tiles above describe
+                        that run); 0 when nothing is copied               */
   long long pack_bytes;
   int split_in_k;    /* FP16/BF16 CTA pairs: 1 when the tiles from
                         streamk_first_tile on (the last partial round and

@@ -221,18 +221,20 @@ def test_op_splitk_scaled(dg, dtype, shape, op_a, op_b):
 
 
 @pytest.mark.parametrize("op_a,op_b,shape,pad,packed", [
-    ("T", "N", (2000, 200, 600), 0, False),    # N = 200 reuses A too little: cp.async
-    ("N", "T", (200, 2000, 600), 0, False),    # M = 200: B staged transposed
-    ("T", "N", (700, 300, 333), 13, False),    # too small a product to pack
-    ("T", "N", (1024, 2048, 1025), 13, True),  # A packed, K ragged (packed rows padded)
-    ("N", "T", (1000, 2051, 1100), 5, True),   # B packed, N ragged
-    ("T", "N", (2048, 2048, 1200), 0, True),   # stream-K grid on packed A
+    ("T", "N", (2000, 200, 600), 0, 0),     # N = 200 reuses A too little: cp.async
+    ("N", "T", (200, 2000, 600), 0, 0),     # M = 200: B staged transposed
+    ("T", "N", (700, 300, 333), 13, 0),     # too small a product to pack
+    ("T", "N", (1024, 2048, 1025), 13, 3),  # A packed, K ragged; B (ldb 2061) re-pitched
+    ("N", "T", (1000, 2051, 1100), 5, 3),   # B packed, N ragged; A (lda 1105) re-pitched
+    ("T", "N", (2048, 2048, 1200), 0, 1),   # stream-K grid on packed A
 ])
 def test_sgemm_packed_and_transposed_staging(dg, op_a, op_b, shape, pad, packed):
     # One FP32 operand stored transposed: either packed into row-major
-    # scratch first (an HBM-bound transpose) or staged by the transposing
-    # cp.async loaders; the plan says which, the result matches the oracle
-    # either way, from stored arrays with padded, unaligned rows.
+    # scratch first (an HBM-bound transpose; a row-major partner whose rows
+    # are not 16-byte pitched is re-pitched in the same scratch) or staged
+    # by the transposing cp.async loaders; the plan says which, the result
+    # matches the oracle either way, from stored arrays with padded,
+    # unaligned rows.
     M, N, K = shape
     A, B = _inputs("f32", M, N, K, 121 + M)
     S_a, S_b = (A.t() if op_a == "T" else A), (B.t() if op_b == "T" else B)
@@ -244,9 +246,9 @@ def test_sgemm_packed_and_transposed_staging(dg, op_a, op_b, shape, pad, packed)
     st, plan = dg.gemm_plan_op("f32", op_a, op_b, M, N, K, 1.0, A_st.data_ptr(), Abuf.stride(0),
                                B_st.data_ptr(), Bbuf.stride(0), 0.0, 1 << 44, N,
                                torch.cuda.get_device_properties(0).multi_processor_count)
-    assert st == dg.GEMM_OK and (plan.pack != 0) == packed
+    assert st == dg.GEMM_OK and plan.pack == packed
     if packed:
-        assert plan.pack == (1 if op_a == "T" else 2) and plan.path != dg.PATH_SIMT_MIXED
+        assert plan.path == dg.PATH_SIMT_TMA
     C = torch.full((M, N), float("nan"), device="cuda")
     _call(dg, "f32", op_a, op_b, A_st, B_st, C, M, N, K)
     _check("f32", op_a, op_b, A_st, B_st, C,

@@ -47,8 +47,41 @@ def test_f32_4096_sampled_rows(dg):
 
 
 def test_f32_edge_full(dg):
-    # 1000 x 1030 x 777, lda = 777: not 16-byte pitched -> cp.async staging
+    # 1000 x 1030 x 777, lda = 777, ldb = 1030: not 16-byte pitched -> both
+    # operands re-pitched into scratch, then TMA staging
     _run_workload(dg, workloads.WORKLOADS["f32_edge"])
+
+
+@pytest.mark.parametrize("shape,pad_a,pad_b,offset,pack", [
+    ((1024, 1024, 1024), 1, 0, False, 1),     # A's rows 4-byte pitched
+    ((1024, 1030, 600), 0, 0, False, 2),      # B's rows (1030 floats) not 16-byte pitched
+    ((1100, 900, 555), 0, 3, False, 3),       # both, K and N ragged
+    ((1024, 1024, 1024), 0, 0, True, 3),      # both bases 4 bytes past a 16-byte boundary
+    ((700, 300, 333), 1, 1, False, 0),        # too small a product: cp.async in place
+])
+def test_f32_repitched_operands(dg, shape, pad_a, pad_b, offset, pack):
+    # Row-major operands that TMA cannot address are copied into scratch
+    # with 16-byte rows first when the product is large enough (the plan
+    # says which operands); the result matches the oracle either way, and a
+    # second call (reusing the scratch) gives the same bits.
+    M, N, K = shape
+    w = workloads.Workload(f"rp{M}x{N}x{K}", "f32", M, N, K, "uniform", 131 + pad_a + pad_b)
+    A, B = workloads.make(w)
+    o = 1 if offset else 0
+    abuf = torch.full((M * (K + pad_a) + o,), float("nan"), device="cuda")
+    bbuf = torch.full((K * (N + pad_b) + o,), float("nan"), device="cuda")
+    Ad = abuf[o:].view(M, K + pad_a)[:, :K]
+    Bd = bbuf[o:].view(K, N + pad_b)[:, :N]
+    Ad.copy_(A)
+    Bd.copy_(B)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = dg.gemm_plan("f32", M, N, K, Ad.data_ptr(), K + pad_a, Bd.data_ptr(), N + pad_b,
+                            1 << 44, N, sms)
+    assert st == dg.GEMM_OK and plan.pack == pack
+    assert plan.path == (dg.PATH_SIMT_TMA if pack else dg.PATH_SIMT_CPASYNC)
+    C = run_gemm(dg, Ad, Bd)
+    compare("f32", A, B, C, rows=workloads.sample_rows(M, 96, seed=M + N))
+    assert torch.equal(C, run_gemm(dg, Ad, Bd))
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (2, 3, 1), (2, 3, 4), (1, 300, 7), (300, 1, 9),
@@ -115,7 +148,8 @@ def test_f32_empty_output_leaves_memory_untouched(dg):
 
 
 def test_f32_repeat_is_deterministic(dg):
-    # The edge shape splits every tile into two k-pieces added into C.
+    # The edge shape splits every tile into two k-pieces, which finish in
+    # either order; the sum of two addends does not depend on it.
     w = workloads.WORKLOADS["f32_edge"]
     A, B = workloads.make(w)
     Ad, Bd = A.cuda(), B.cuda()
@@ -147,11 +181,11 @@ def test_bounded_flag_wait_self_test_reports_timeout(dg):
 
 
 # Hybrid stream-K schedules: whole-tile waves, then equal k-tile ranges per
-# CTA; a range boundary inside a tile cuts it into two pieces that add into
-# zeroed C (beta = 0) or meet in the tail workspace (beta != 0).  C starts as
-# NaN, so a tile the zeroing kernel or a piece misses shows up; integer
-# entries make every sum exact, so a k-range counted twice or skipped
-# breaks bit-exactness.
+# CTA; a range boundary inside a tile cuts it into two pieces: the first to
+# finish stores to C (beta = 0) or leaves its sums in the boundary's
+# workspace tile (beta != 0), the second adds its own.  C starts as NaN, so
+# a tile or element a piece misses shows up; integer entries make every sum
+# exact, so a k-range counted twice or skipped breaks bit-exactness.
 STREAMK_SHAPES = [
     (2176, 2304, 96),    # 153 wide tiles on 152 CTAs, 3 k-tiles each: a cut almost everywhere
     (4096, 4096, 64),    # 512 tiles, 2 k-tiles: whole-tile waves + cuts at half tiles

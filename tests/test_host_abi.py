@@ -130,8 +130,9 @@ def _streamk_units(tiles, nk, grid):
 def test_streamk_schedule_covers_every_k_tile_once(tiles, nk, slots):
     # The plan's grid rule, then the kernel's unit loop: every (tile, k-tile)
     # is computed exactly once, no tile has more than two pieces, the cut
-    # count is what the plan reports, and the two pieces of a cut tile map
-    # to the two workspace slots of its boundary.
+    # count is what the plan reports, and the two pieces of a cut tile meet
+    # at one boundary (its flag words and workspace tile), a different one
+    # for every cut tile.
     grid = slots if tiles > slots else (2 * tiles if (2 * tiles <= slots and nk >= 2) else tiles)
     units = _streamk_units(tiles, nk, grid)
     seen = {}
@@ -195,20 +196,36 @@ def test_plan_paths():
     ok, p = dg.gemm_plan("f32", 1024, 1024, 512, FAKE, 512, FAKE + (1 << 30), 1024,
                          FAKE + (2 << 30), 1024, num_sms=152)
     assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles) == (128, 3, 64)
-    # lda = 777 floats is not a 16-byte pitch: cp.async staging
+    # lda = 777 and ldb = 1030 floats are not 16-byte pitches: with
+    # 8.0e8 >= 2^29 multiply-adds both operands are first re-pitched into
+    # scratch (A's copy, 1000 x 780 floats, rounded up to 256 bytes, then
+    # B's, 777 x 1032) and the product runs with TMA staging
     ok, p = dg.gemm_plan("f32", 1000, 1030, 777, FAKE, 777, FAKE + (1 << 30), 1030,
                          FAKE + (2 << 30), 1030)
-    assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_CPASYNC
+    assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_TMA
+    assert p.pack == 3 and p.pack_bytes == (1000 * 780 * 4 + 255) // 256 * 256 + 777 * 1032 * 4
     # 72 narrow tiles as two k-halves each keep 144 of the 152 SMs busy
     # (score 0.91): no split-K; every tile is cut once, no workspace
     assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 72
     assert (p.splitk_slices, p.ctas, p.workspace_bytes) == (1, 144, 0)
-    # 36 narrow tiles over K = 4096 (best whole-K score 0.45): split-K, 8
-    # slices of 16 k-tiles into an 8 x 768 x 768 FP32 workspace
+    # a smaller product with an unaligned pitch: staged in place by cp.async
+    ok, p = dg.gemm_plan("f32", 700, 300, 333, FAKE, 333, FAKE + (1 << 30), 300,
+                         FAKE + (2 << 30), 300)
+    assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_CPASYNC and p.pack == 0
+    # 36 narrow tiles over K = 4096 (best whole-K score 0.45): split-K, 4
+    # slices of 32 k-tiles (one CTA per SM; 8 slices would put two on each
+    # SM for the same k-tiles per SM) into a 4 x 768 x 768 FP32 workspace
     ok, p = dg.gemm_plan("f32", 768, 768, 4096, FAKE, 4096, FAKE + (1 << 30), 768,
                          FAKE + (2 << 30), 768)
-    assert (p.tiles, p.splitk_slices, p.ctas) == (36, 8, 288)
-    assert p.workspace_bytes == 8 * 768 * 768 * 4
+    assert (p.tiles, p.splitk_slices, p.ctas) == (36, 4, 144)
+    assert p.workspace_bytes == 4 * 768 * 768 * 4
+    # tiny products: one k-tile per slice when the SMs allow (256^3: 4 tiles
+    # x 8 slices), the split that minimises the busiest SM's k-tiles plus a
+    # fixed cost per slice (512^3: 16 tiles x 9 slices)
+    for (m, n, k), want in [((256, 256, 256), (4, 8)), ((512, 512, 512), (16, 9)),
+                            ((384, 384, 384), (9, 12))]:
+        ok, p = dg.gemm_plan("f32", m, n, k, FAKE, k, FAKE + (1 << 30), n, FAKE + (2 << 30), n)
+        assert (p.tiles, p.splitk_slices) == want
     # misaligned base pointer (4-byte aligned only)
     ok, p = dg.gemm_plan("f32", 64, 64, 64, FAKE + 4, 64, FAKE + (1 << 30), 64,
                          FAKE + (2 << 30), 64)
@@ -403,14 +420,15 @@ def test_scaled_plans():
     assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
     ok, p = dg.gemm_plan_ex("bf16", 64, 64, 0, 1.0, 0, 0, 0, 64, 0.5, FAKE, 64, 152)
     assert ok == dg.GEMM_OK and p.path == dg.PATH_ZERO_FILL
-    # The SGEMM's stream-K pieces either way; with beta != 0 they go through
-    # a workspace of two FP32 tiles per range boundary (151 x 2 x 128 x 256
-    # x 4 bytes), with beta == 0 they add into C.
+    # The SGEMM's stream-K pieces either way; with beta != 0 the first of a
+    # cut tile's pieces leaves its sums in a workspace of one FP32 tile per
+    # range boundary (151 x 128 x 256 x 4 bytes), with beta == 0 it stores
+    # them to C and the second piece adds into C.
     args = (4096, 4096, 4096, 1.0, FAKE, 4096, FAKE + (1 << 30), 4096)
     ok, p0 = dg.gemm_plan_ex("f32", *args, 0.0, FAKE + (2 << 30), 4096, 152)
     ok, p1 = dg.gemm_plan_ex("f32", *args, 0.5, FAKE + (2 << 30), 4096, 152)
     assert p0.split_tiles == 144 and p1.split_tiles == 144 and p1.ctas == 152
-    assert p0.workspace_bytes == 0 and p1.workspace_bytes == 151 * 2 * 128 * 256 * 4
+    assert p0.workspace_bytes == 0 and p1.workspace_bytes == 151 * 128 * 256 * 4
     # FP16/BF16 plans do not depend on alpha and beta
     for dt in ("f16", "bf16"):
         ok, q0 = dg.gemm_plan(dt, 4096, 4096, 4096, FAKE, 4096, FAKE + (1 << 30), 4096,

@@ -4,9 +4,10 @@ budget, or a latency path that cannot take cudaMalloc's synchronisation).
 It keeps split-K partial tiles in the library's fixed 16 MiB device array
 instead of an allocated workspace.
 
-Every shape below is one the planner runs as split-K within 16 MiB of
-partials (asserted from the plan first), so each call really goes through
-the static array.  The tests call the entry through the C ABI, twice in a
+The split-K shapes below are ones the planner runs as split-K within 16 MiB
+of partials (asserted from the plan first), so each call really goes
+through the static array; the stream-K shapes cut tiles whose pieces meet
+through the entry's fixed flag array.  The tests call the entry through the C ABI, twice in a
 row (the array keeps the previous call's contents), and check its output
 against the CPU oracle at the FP32 tolerance and bit for bit against
 gemm_f32 (the same slices summed in the same order; only the staging of the
@@ -54,10 +55,35 @@ def test_noalloc_matches_oracle_and_gemm_f32_on_two_calls(shape):
         assert torch.equal(C, ref)
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch():
-    # 36 tiles -> 8 k-slices of 768 x 768 FP32 = 18.9 MB > 16 MiB
+@pytest.mark.parametrize("shape", [(1000, 1030, 777), (2048, 2048, 2048)])
+def test_noalloc_stream_k_pieces_meet_through_fixed_flags(shape):
+    # Not split-K: the stream-K share cuts tiles in two, and the pieces meet
+    # through the entry's fixed flag array (the edge shape's unaligned rows
+    # are staged in place, never re-pitched into scratch).  Same bits as
+    # gemm_f32, which re-pitches them, on two calls; the oracle agrees.
     dg = gpu_lib()
-    M, N, K = 768, 768, 4096
+    M, N, K = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)
+    assert st == dg.GEMM_OK and plan.splitk_slices == 1 and plan.split_tiles > 0
+    w = workloads.Workload(f"noalloc_sk{M}x{N}x{K}", "f32", M, N, K, "uniform", 98)
+    A_cpu, B_cpu = workloads.make(w)
+    A, B = A_cpu.cuda(), B_cpu.cuda()
+    ref = torch.full((M, N), float("nan"), device="cuda")
+    assert _run(dg, dg.gemm_f32, A, B, ref) == dg.GEMM_OK
+    check_device(dg)
+    for _ in range(2):
+        C = torch.full((M, N), float("nan"), device="cuda")
+        assert _run(dg, dg.gemm_f32_noalloc, A, B, C) == dg.GEMM_OK
+        check_device(dg)
+        assert torch.equal(C, ref)
+    compare("f32", A_cpu, B_cpu, C, rows=workloads.sample_rows(M, 64, seed=98))
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    # 16 tiles, K = 16384 -> 19 k-slices of 448 x 512 FP32 = 17.4 MB > 16 MiB
+    dg = gpu_lib()
+    M, N, K = 448, 512, 16384
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     _, plan = dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)
     assert plan.splitk_slices > 1 and plan.workspace_bytes > SCRATCH_BYTES
