@@ -402,7 +402,7 @@ constexpr double kSgemmSplitkBelowScore = 0.6;
 // B with storage ops op_a / op_b, a16 / b16: base and leading dimension
 // 16-byte aligned).  The arguments are already validated.
 gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool b16, float beta,
-                         int sms, gemm_plan_t* plan) {
+                         int sms, gemm_plan_t* plan, bool c_trans = false) {
   // TMA cannot transpose 4-byte elements: a transposed operand is staged
   // by the transposing cp.async loaders; with exactly one transposed, the
   // other comes by TMA when it is 16-byte aligned.
@@ -468,7 +468,10 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles - dp_tiles, nk, grid);
   plan->split_pieces = plan->split_tiles ? 2 : 1;
   plan->splitk_slices = 1;
-  if (plan->split_tiles && beta != 0.f)
+  // (The grid of two CTAs per tile over row-major operands combines each
+  // tile's halves in distributed shared memory: no workspace, no flags.)
+  const bool pair_k = dgemm::sgemm_pair_k(plan->tiles, grid, 1) && !op_a && !op_b && !c_trans;
+  if (plan->split_tiles && beta != 0.f && !pair_k)
     plan->workspace_bytes =
         (long long)(grid - 1) * dgemm::kSgemmBM * plan->block_n * 4;
   plan->ctas = grid;
@@ -519,7 +522,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     // Both operands stored transposed: C^T = B_st . A_st is a product of two
     // row-major arrays, which the kernel computes with TMA staging and
     // stores transposed (SgemmParams::c_trans).
-    if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan);
+    if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan, true);
     // Exactly one stored transposed: pack it (A into M x K, B into K x N,
     // rows padded to 16 bytes) and run the row-major product, when each
     // packed element is used by at least kPackMinReuse output columns
@@ -806,7 +809,9 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
       st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
       if (st != GEMM_OK) return st;
     }
-    if (p.slices == 1 && plan.split_tiles > 0) {
+    const bool pair_k = dgemm::sgemm_pair_k(plan.tiles, plan.ctas, p.slices) && !kop_a &&
+                        !kop_b && !swap;
+    if (p.slices == 1 && plan.split_tiles > 0 && !pair_k) {
       if (plan.workspace_bytes > 0) {
         st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.tail_ws);
         if (st != GEMM_OK) return st;

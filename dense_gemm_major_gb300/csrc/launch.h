@@ -85,6 +85,15 @@ struct SgemmParams {
   unsigned long long timeout_ns;
 };
 
+// Whether an FP32 grid of row-major operands (no transposed storage) runs
+// as CTA pairs that split K: the single-wave grid of two CTAs per tile
+// (grid = 2 tiles, not split-K).  The two CTAs of a tile form a cluster
+// and combine their halves of the sum through distributed shared memory,
+// so they need neither flags nor workspace.
+__host__ __device__ inline bool sgemm_pair_k(int tiles, int grid, int slices) {
+  return slices == 1 && tiles > 0 && grid == 2 * tiles;
+}
+
 // Tile (tm, tn) of linear tile index t under grouped rasterisation: tiles
 // walk down a group of `group` tile rows before moving one tile column right.
 __host__ __device__ inline void grouped_tile(int t, int tiles_m, int tiles_n, int group, int& tm,
@@ -489,21 +498,42 @@ bool pdl_enabled();
 // with programmatic stream serialization: its CTAs can be scheduled, and
 // run their prologue (barriers, TMEM, descriptor prefetch), while the
 // previous kernel in the stream finishes.  Measured on GB300, back-to-back
-// FP16 GEMMs: 2048^3 18.5 -> 15.9 us, 4096^3 86.7 -> 84.4 us.
+// FP16 GEMMs: 2048^3 18.5 -> 15.9 us, 4096^3 86.7 -> 84.4 us.  cluster_x > 1
+// groups consecutive CTAs into clusters of that many (a kernel compiled
+// with __cluster_dims__ takes 1 here).
 template <typename... Params, typename... Args>
-cudaError_t launch_gemm_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
-                               cudaStream_t stream, Args&&... args) {
+cudaError_t launch_gemm_kernel_clusters(unsigned cluster_x, void (*kernel)(Params...), dim3 grid,
+                                        dim3 block, size_t smem, cudaStream_t stream,
+                                        Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_gemm_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, Args&&... args) {
+  return launch_gemm_kernel_clusters(1, kernel, grid, block, smem, stream,
+                                     std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------- self test

@@ -145,6 +145,30 @@ __device__ __forceinline__ bool flag_wait_equal(const unsigned* f, unsigned v, u
   }
 }
 
+// ---------------------------------------------------------------- clusters
+
+// Shared::cluster address of the object at shared offset `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// All threads of every CTA of the cluster: release this CTA's earlier
+// memory operations, acquire the others'.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16-byte store to the shared memory of a CTA of the cluster (address from
+// mapa_shared).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // Programmatic dependent launch: a kernel launched with the

@@ -9,6 +9,16 @@ cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUten
   CUtensorMap none{};
   if (!use_tma) tmA = tmB = &none;
   if (p.op_a || p.op_b || p.c_trans) return launch_sgemm_op(p, tn, use_tma, tmA, tmB, stream);
+  if (sgemm_pair_k(p.tiles_m * p.tiles_n, p.grid, p.slices)) {
+    if (tn == 16)
+      return use_tma ? launch_cfg<true, 16, 1, false, false, false, true>(p, tmA, tmB, stream)
+                     : launch_cfg<false, 16, 1, false, false, false, true>(p, tmA, tmB, stream);
+    if (tn == 9)
+      return use_tma ? launch_cfg<true, 8, 1, false, false, false, true>(p, tmA, tmB, stream)
+                     : launch_cfg<false, 8, 1, false, false, false, true>(p, tmA, tmB, stream);
+    return use_tma ? launch_cfg<true, 8, 2, false, false, false, true>(p, tmA, tmB, stream)
+                   : launch_cfg<false, 8, 2, false, false, false, true>(p, tmA, tmB, stream);
+  }
   if (tn == 16)
     return use_tma ? launch_cfg<true, 16, 1>(p, tmA, tmB, stream)
                    : launch_cfg<false, 16, 1>(p, tmA, tmB, stream);

@@ -163,12 +163,15 @@ __device__ __forceinline__ void transpose4_lanes(float (&x)[4], int tr) {
 // (all others by cp.async); with one operand transposed the two kinds of
 // copy complete on the same mbarrier (1 TMA arrival + 256 cp.async ones).
 // kCT: C is stored transposed (p.c_trans), a compile-time choice so that the
-// row-major instances carry no trace of it.
-template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false>
+// row-major instances carry no trace of it.  kPairK: the grid of two CTAs
+// per tile (sgemm_pair_k), launched as clusters of two.
+template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false,
+          bool kPairK = false>
 __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     sgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const SgemmParams p) {
   static_assert(!(kTma && kTA && kTB), "with both operands transposed nothing is TMA-staged");
+  static_assert(!(kPairK && (kTA || kTB || kCT)), "CTA pairs over K take row-major operands");
   constexpr bool kCpA = !kTma || kTA;   // A staged by cp.async
   constexpr bool kCpB = !kTma || kTB;   // B staged by cp.async
   constexpr bool kAnyCp = kCpA || kCpB;
@@ -264,6 +267,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     }
   }
   int g0 = 0;
+  bool pair_synced = false;   // kPairK: this CTA passed the exchange's two cluster barriers
   while (dp_next < p.dp_tiles || sk_next < sk_units) {
     int tile, k_begin, k_end;
     if (p.slices > 1) {
@@ -469,7 +473,57 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
         }
       }
       __syncthreads();
+      // (The partner CTA of a pair waits at two cluster barriers: pass them.)
+      if constexpr (kPairK) {
+        cluster_sync_all();
+        cluster_sync_all();
+      }
       return;
+    }
+
+    if constexpr (kPairK) {
+      // The two CTAs of this tile's cluster hold the sums over the two
+      // halves of K (rank 0 the first).  Rank 0 keeps rows 0..63 (warps
+      // 0..3) and rank 1 rows 64..127 (warps 4..7); each warp of the other
+      // half sends its accumulators into the partner's (now idle) ring,
+      // where the warp with the same rows adds them to its own and the
+      // tile's C is written half by each CTA.  Thread t (mod 128) puts its
+      // j-th 16-byte group at ring + 16 (128 j + t): a warp's stores and
+      // loads are contiguous, free of bank conflicts.  a + b == b + a, so
+      // the result does not depend on which half is whose.
+      const uint32_t rank = (uint32_t)b & 1u;
+      const bool keep = (warp_m < 2) == (rank == 0);
+      const int t = tid & 127;
+      cluster_sync_all();   // both CTAs are done with their rings
+      if (!keep) {
+        const uint32_t dst = mapa_shared(smem_u32(sA), rank ^ 1u);
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+  #pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+            const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+            st_cluster_v4(dst + 16u * (uint32_t)(128 * (i * NH + h) + t), lo.x, lo.y, hi.x, hi.y);
+          }
+        }
+      }
+      cluster_sync_all();   // the partner's half is in this CTA's ring
+      pair_synced = true;
+      if (!keep) {
+        g0 += nk;
+        continue;
+      }
+  #pragma unroll
+      for (int i = 0; i < 8; ++i) {
+  #pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const float4 o = *reinterpret_cast<const float4*>(sA + 4 * (128 * (i * NH + h) + t));
+          const float2 lo = unpack_pair(acc[i][2 * h + 0]);
+          const float2 hi = unpack_pair(acc[i][2 * h + 1]);
+          acc[i][2 * h + 0] = pack_pair(lo.x + o.x, lo.y + o.y);
+          acc[i][2 * h + 1] = pack_pair(hi.x + o.z, hi.y + o.w);
+        }
+      }
     }
 
     // Destination: unscaled FP32 partial sums go to
@@ -483,7 +537,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     if (p.slices > 1) {
       part = p.ws + (long long)(b % p.slices) * p.M * p.ldw;
       part_ld = p.ldw;
-    } else if (k_begin != 0 || k_end != nk_all) {
+    } else if (!kPairK && (k_begin != 0 || k_end != nk_all)) {
       // One of the two pieces of a tile cut by boundary cb (the first k-tile
       // of CTA cb): piece 0 ends CTA cb - 1's range, piece 1 starts CTA cb's.
       // Whichever piece finishes first publishes its sums and raises the
@@ -689,22 +743,31 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
     publish();
     g0 += nk;
   }
+  // A CTA of a pair with no unit (never planned) still meets its partner's
+  // two cluster barriers.
+  if constexpr (kPairK) {
+    if (!pair_synced) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+  }
 }
 
-template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false>
+template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false,
+          bool kPairK = false>
 cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
                        cudaStream_t stream) {
   // The attribute is per function; setting it on every call is cheap and
   // keeps this correct for every device of the process.
-  cudaError_t e = cudaFuncSetAttribute(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto kernel = sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT, kPairK>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        sgemm_smem_bytes(TN));
   if (e != cudaSuccess) return e;
   const int tiles = p.tiles_m * p.tiles_n;
   // Stream-K: G = p.grid CTAs (<= tiles); p.split_tiles tiles are cut in two.
   const int G = p.slices > 1 ? tiles * p.slices : p.grid;
-  return launch_gemm_kernel(sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT>, dim3(G),
-                            dim3(kSgemmThreads), sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
+  return launch_gemm_kernel_clusters(kPairK ? 2u : 1u, kernel, dim3(G), dim3(kSgemmThreads),
+                                     sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
 }
 
 }  // namespace

@@ -265,23 +265,10 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Shared::cluster address of the object at shared offset `addr` in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
 // Arrive on an mbarrier given by its shared::cluster address (any CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-
-// All threads of both CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 2-D TMA load into this CTA's shared memory whose completion is counted on

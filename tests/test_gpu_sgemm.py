@@ -237,6 +237,39 @@ def test_f32_streamk_integer_exact(dg, shape, alpha, beta):
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024),   # narrow tiles, TMA
+                                   (640, 2560, 1000),    # wide tiles
+                                   (384, 2048, 4096),    # long K
+                                   (1000, 777, 555),     # ragged; ldb = 777 staged by cp.async
+                                   (1000, 1030, 777)])   # re-pitched operands
+def test_f32_pair_k_halves(dg, shape):
+    # A single wave of at most half the SMs' worth of tiles runs as two CTAs
+    # per tile, each over half of K, launched as a cluster; the halves meet
+    # in distributed shared memory (no workspace even with beta != 0).
+    # Integer entries make every sum exact; C starts as NaN, so an element
+    # neither CTA writes shows up; repeated calls give the same bits.
+    M, N, K = shape
+    plan = _plan32_ex(dg, M, N, K, 0.5)
+    assert plan.splitk_slices == 1 and plan.ctas == 2 * plan.tiles and plan.split_tiles > 0
+    assert plan.workspace_bytes == 0
+    w = workloads.Workload(f"pk{M}x{N}x{K}", "f32", M, N, K, "int", 65, -2, 2)
+    A, B = workloads.make(w)
+    Ad, Bd = A.cuda(), B.cuda()
+    C = run_gemm(dg, Ad, Bd)
+    compare("f32", A, B, C, exact=True, rows=workloads.sample_rows(M, 64, seed=65))
+    assert torch.equal(C, run_gemm(dg, Ad, Bd))
+    C_in = torch.randint(-3, 4, (M, N), generator=torch.Generator().manual_seed(66)).float()
+    C2 = C_in.cuda()
+    st = dg.gemm_ex("f32", M, N, K, 2.0, Ad.data_ptr(), K, Bd.data_ptr(), N, 0.5,
+                    C2.data_ptr(), N, torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK, dg.status_string(st)
+    check_device(dg)
+    rows = workloads.sample_rows(M, 64, seed=67)
+    ref, _ = oracle.gemm_scaled("f32", 2.0, workloads.to_numpy_bits(A), workloads.to_numpy_bits(B),
+                                0.5, workloads.to_numpy_bits(C_in), rows=rows)
+    assert np.array_equal(C2.cpu().numpy().astype(np.float64)[rows], ref)
+
+
 def _plan32(dg, M, N, K):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return dg.gemm_plan("f32", M, N, K, 1 << 40, K, 2 << 40, N, 3 << 40, N, sms)[1]
