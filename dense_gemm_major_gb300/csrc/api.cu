@@ -53,8 +53,9 @@ struct Workspace {
   size_t bytes = 0;
   unsigned epoch = 0;   // kWsFlags: the last epoch handed to a launch
 };
-// kWsFlags holds the hand-over flags of the pair kernel's K split: zeroed
-// when (re)allocated, then only ever set to a launch's epoch and cleared.
+// kWsFlags holds the hand-over flags of cut tiles (the pair kernel's K
+// split, the SGEMM's stream-K pieces): zeroed when (re)allocated, then only
+// ever set to a launch's epoch (or cleared).
 constexpr int kWsPartials = 0, kWsPack = 1, kWsFlags = 2;
 std::map<std::tuple<int, cudaStream_t, int>, Workspace> g_workspaces;   // guarded by g_mu
 

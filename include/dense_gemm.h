@@ -300,9 +300,12 @@ typedef struct gemm_plan_t {
                         of the last partial round (or of a small grid)
                         run as split_pieces column parts, or, with
                         split_in_k, the tiles the stream-K share cuts    */
-  int split_pieces;  /* 1 when nothing is split.  FP32: 2, the pieces'
-                        FP32 partials are added into zeroed C (or, with
-                        beta != 0, combined from a workspace).  FP16/BF16:
+  int split_pieces;  /* 1 when nothing is split.  FP32: 2; the piece that
+                        finishes first stores its sums to C (or, with
+                        beta != 0, to a workspace tile) and the second
+                        adds its own; in a grid of two CTAs per tile
+                        (ctas == 2 * tiles) the two form a cluster and
+                        combine in shared memory instead.  FP16/BF16:
                         2 or 4 column parts of the output tile, each over
                         the full K range; with split_in_k, 2 (the head
                         and the tail of a cut tile)                       */
