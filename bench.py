@@ -340,7 +340,8 @@ def run_ours(args, ws, rank, local):
     # This library's kernel launches per step: one per GEMM, plus the
     # re-pitch launch of an FP32 GEMM with an operand TMA cannot address
     # (the step's operands are row-major: both copies are one launch) and
-    # the reduction launch of a split-K GEMM.
+    # the reduction launch of a split-K GEMM (none when an FP32 tile's
+    # k-slices combine within a cluster).
     launches_per_step = 0
     for c in cases:
         w = c["w"]
@@ -349,7 +350,8 @@ def run_ours(args, ws, rank, local):
                                   sms)
         if plan.path == dg.PATH_NOOP:
             continue
-        launches_per_step += 1 + (1 if plan.splitk_slices > 1 else 0) + (1 if plan.pack else 0)
+        reduce = plan.splitk_slices > 1 and not (w.dtype == "f32" and plan.cluster_ctas > 1)
+        launches_per_step += 1 + (1 if reduce else 0) + (1 if plan.pack else 0)
 
     def launch(c, s=sptr):
         w = c["w"]

@@ -33,7 +33,8 @@ EXPORTED = ("gemm_f32", "gemm_f16", "gemm_bf16", "gemm_status_string", "gemm_dev
             "gemm_f32_ex", "gemm_f16_ex", "gemm_bf16_ex", "gemm_plan_ex",
             "gemm_f32_op", "gemm_f16_op", "gemm_bf16_op", "gemm_plan_op", "gemm_host",
             "gemm_host_blocks", "gemm_host_k_blocks", "gemm_selftest_flag_timeout",
-            "gemm_plan_resident", "gemm_pair_clusters", "gemm_pair_units", "gemm_probe_ffma",
+            "gemm_plan_resident", "gemm_pair_clusters", "gemm_sgemm_clusters", "gemm_pair_units",
+            "gemm_probe_ffma",
             "gemm_probe_ffma_threads")
 
 # Operand storage (gemm_op_t): N = as stored row-major, T = stored transposed
@@ -104,6 +105,8 @@ def load() -> ctypes.CDLL:
     lib.gemm_probe_ffma_threads.argtypes = []
     lib.gemm_pair_clusters.restype = i
     lib.gemm_pair_clusters.argtypes = []
+    lib.gemm_sgemm_clusters.restype = i
+    lib.gemm_sgemm_clusters.argtypes = [i, i]
     lib.gemm_host.restype = i
     lib.gemm_host.argtypes = [i, i, i, i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     lib.gemm_host_blocks.restype = i
@@ -245,6 +248,10 @@ def gemm_probe_ffma_threads() -> int:
 
 def gemm_pair_clusters() -> int:
     return load().gemm_pair_clusters()
+
+
+def gemm_sgemm_clusters(config, cluster_size) -> int:
+    return load().gemm_sgemm_clusters(config, cluster_size)
 
 
 def gemm_f32_op(op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0) -> int:

@@ -38,6 +38,8 @@ struct DeviceInfo {
   // 2-CTA clusters of the pair kernel that fit on the device at once
   // (cudaOccupancyMaxActiveClusters; 0 if the query failed).
   int pair_clusters = 0;
+  // Clusters of the SGEMM kernel over K that fit at once (the same query).
+  dgemm::SgemmClusterCaps sgemm_caps{};
   unsigned* fault = nullptr;  // device address of g_fault_word
 };
 
@@ -190,7 +192,10 @@ gemm_status_t current_device(DeviceInfo** out) {
       d.supported = false;
     }
     d.fault = static_cast<unsigned*>(addr);
-    if (d.supported) d.pair_clusters = dgemm::tc_pair_resident_clusters();
+    if (d.supported) {
+      d.pair_clusters = dgemm::tc_pair_resident_clusters();
+      d.sgemm_caps = dgemm::sgemm_cluster_caps();
+    }
   }
   if (!d.supported) return GEMM_ERR_UNSUPPORTED_DEVICE;
   *out = &d;
@@ -338,6 +343,17 @@ int forced_sgemm_slices() {
   return v;
 }
 
+// Measurement override: DENSE_GEMM_SGEMM_CLUSTER=0 runs the FP32 grid of
+// two CTAs per tile as stream-K pieces meeting through flags instead of
+// 2-CTA clusters.
+bool sgemm_clusters_off() {
+  static const bool v = [] {
+    const char* s = std::getenv("DENSE_GEMM_SGEMM_CLUSTER");
+    return s != nullptr && std::strcmp(s, "0") == 0;
+  }();
+  return v;
+}
+
 // Measurement override: DENSE_GEMM_SGEMM_TILE=narrow|wide forces the FP32
 // tile configuration (0 = no override).
 int forced_sgemm_tn() {
@@ -399,11 +415,23 @@ int sgemm_pick_tn(int M, int N, int K, int sms, double* score_out = nullptr) {
 // 178 us.
 constexpr double kSgemmSplitkBelowScore = 0.6;
 
+// Clusters of s CTAs (2, 4, 8) of SGEMM configuration cfg (0 narrow/1,
+// 1 narrow/2, 2 wide) that fit at once: the device's answer, else the
+// SM count's.
+long long sgemm_cluster_cap(const dgemm::SgemmClusterCaps* caps, int sms, int cfg, int s) {
+  const int idx = s == 2 ? 0 : (s == 4 ? 1 : 2);
+  if (caps != nullptr) return caps->n[cfg][idx];
+  return (long long)(cfg == 1 ? 2 : 1) * sms / s;
+}
+
 // FP32 plan of the problem as the SGEMM kernel sees it (M x N output, A and
 // B with storage ops op_a / op_b, a16 / b16: base and leading dimension
-// 16-byte aligned).  The arguments are already validated.
+// 16-byte aligned; c_trans: C is stored transposed); the arguments are
+// already validated.  caps: the device's cluster capacities (nullptr:
+// derived from sms).
 gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool b16, float beta,
-                         int sms, gemm_plan_t* plan, bool c_trans = false) {
+                         int sms, gemm_plan_t* plan, bool c_trans = false,
+                         const dgemm::SgemmClusterCaps* caps = nullptr) {
   // TMA cannot transpose 4-byte elements: a transposed operand is staged
   // by the transposing cp.async loaders; with exactly one transposed, the
   // other comes by TMA when it is 16-byte aligned.
@@ -413,10 +441,16 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
     plan->path = GEMM_PATH_SIMT_MIXED;
   else
     plan->path = GEMM_PATH_SIMT_CPASYNC;
+  // The two k-halves of a tile can form a cluster (combining in
+  // distributed shared memory) only in the row-major kernels.
+  const bool row_major = !op_a && !op_b && !c_trans;
   const int narrow_tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, dgemm::sgemm_bn(8));
   const int nk_all = ceil_div(K, dgemm::kSgemmBK);
   // A grid that no whole-K configuration keeps busy enough runs as split-K
-  // (k-slices of narrow tiles into a workspace, then a reduction).
+  // (k-slices of narrow tiles into a workspace, then a reduction).  (Eight
+  // or four k-slices of a tile as a cluster that adds them in distributed
+  // shared memory instead were measured no faster: 256^3 17.0 against
+  // 15.0 us, 768^3 31.4 against 31.4 us.)
   double best_score = 1.0;
   sgemm_pick_tn(M, N, K, sms, &best_score);
   int slices = forced_sgemm_tn() || best_score >= kSgemmSplitkBelowScore
@@ -460,19 +494,28 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   // partial sums in a workspace (one tile per boundary) for the second.
   const int slots = (tn == 8 ? 2 : 1) * sms;
   const int nk = ceil_div(K, dgemm::kSgemmBK);
-  // (A single wave of at most half the slots runs as two CTAs per tile:
-  // grid = 2 tiles puts every boundary in the middle of a tile.)
+  // A single wave of at most half the slots runs as two CTAs per tile, over
+  // the two halves of K: as 2-CTA clusters (two k-slices combining in
+  // shared memory) for row-major operands when they all fit at once, else
+  // as the stream-K grid of 2 tiles (every boundary in the middle of a
+  // tile).
   const int grid = plan->tiles > slots        ? slots
                    : (2 * plan->tiles <= slots && nk >= 2) ? 2 * plan->tiles
                                                            : plan->tiles;
+  const int cfg = tn == 9 ? 0 : (tn == 8 ? 1 : 2);
+  if (grid == 2 * plan->tiles && row_major && !sgemm_clusters_off() &&
+      plan->tiles <= sgemm_cluster_cap(caps, sms, cfg, 2)) {
+    plan->split_pieces = 1;
+    plan->splitk_slices = 2;
+    plan->cluster_ctas = 2;
+    plan->ctas = grid;
+    return GEMM_OK;
+  }
   const int dp_tiles = dgemm::sgemm_dp_tiles(plan->tiles, grid);
   plan->split_tiles = dgemm::sgemm_streamk_cuts(plan->tiles - dp_tiles, nk, grid);
   plan->split_pieces = plan->split_tiles ? 2 : 1;
   plan->splitk_slices = 1;
-  // (The grid of two CTAs per tile over row-major operands combines each
-  // tile's halves in distributed shared memory: no workspace, no flags.)
-  const bool pair_k = dgemm::sgemm_pair_k(plan->tiles, grid, 1) && !op_a && !op_b && !c_trans;
-  if (plan->split_tiles && beta != 0.f && !pair_k)
+  if (plan->split_tiles && beta != 0.f)
     plan->workspace_bytes =
         (long long)(grid - 1) * dgemm::kSgemmBM * plan->block_n * 4;
   plan->ctas = grid;
@@ -485,7 +528,8 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
 gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, float alpha,
                         const void* A, int lda, const void* B, int ldb, float beta, const void* C,
                         int ldc, int num_sms, int pair_clusters, gemm_plan_t* plan,
-                        bool allow_copy = true) {
+                        bool allow_copy = true,
+                        const dgemm::SgemmClusterCaps* caps = nullptr) {
   if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   if (dtype < 0 || dtype > 2) return GEMM_ERR_INVALID_ARG;
@@ -523,7 +567,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
     // Both operands stored transposed: C^T = B_st . A_st is a product of two
     // row-major arrays, which the kernel computes with TMA staging and
     // stores transposed (SgemmParams::c_trans).
-    if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan, true);
+    if (op_a && op_b) return plan_sgemm(N, M, K, 0, 0, b16, a16, beta, sms, plan, true, caps);
     // Exactly one stored transposed: pack it (A into M x K, B into K x N,
     // rows padded to 16 bytes) and run the row-major product, when each
     // packed element is used by at least kPackMinReuse output columns
@@ -551,7 +595,7 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
         const long long total = (bytes + 255) / 256 * 256 + (other + 255) / 256 * 256;
         const bool both = !other16 && total <= kPackCapBytes;
         const gemm_status_t st =
-            plan_sgemm(M, N, K, 0, 0, true, both || other16, beta, sms, plan);
+            plan_sgemm(M, N, K, 0, 0, true, both || other16, beta, sms, plan, false, caps);
         plan->pack = (op_a ? 1 : 2) | (both ? (op_a ? 2 : 1) : 0);
         plan->pack_bytes = both ? total : bytes;
         return st;
@@ -569,13 +613,14 @@ gemm_status_t plan_impl(int dtype, int op_a, int op_b, int M, int N, int K, floa
       const int forced = forced_sgemm_repitch();
       if (forced == 1 || (forced == -1 && (long long)M * N * K >= kRepitchMinWork &&
                           bytes <= kPackCapBytes)) {
-        const gemm_status_t st = plan_sgemm(M, N, K, 0, 0, true, true, beta, sms, plan);
+        const gemm_status_t st =
+            plan_sgemm(M, N, K, 0, 0, true, true, beta, sms, plan, false, caps);
         plan->pack = (a16 ? 0 : 1) | (b16 ? 0 : 2);
         plan->pack_bytes = bytes;
         return st;
       }
     }
-    return plan_sgemm(M, N, K, op_a, op_b, a16, b16, beta, sms, plan);
+    return plan_sgemm(M, N, K, op_a, op_b, a16, b16, beta, sms, plan, false, caps);
   }
   // FP16 / BF16: TMA in and out needs 16-byte aligned bases and pitches.
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda % 8) || (ldb % 8) || (ldc % 8))
@@ -712,12 +757,12 @@ void tc_schedule_params(const gemm_plan_t& plan, int M, int N, dgemm::TcParams* 
   }
 }
 
-// fixed_flags: flag words for the FP32 stream-K hand-over supplied by the
-// caller (gemm_f32_noalloc) instead of the stream's library-owned array.
+// fixed: flag words and split-K workspace supplied by the caller
+// (gemm_f32_noalloc) instead of the stream's library-owned arrays.
 gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alpha, const void* A,
                   int lda, const void* B, int ldb, float beta, void* C, int ldc,
                   cudaStream_t stream, bool allow_copy = true,
-                  const dgemm::FixedFlags* fixed_flags = nullptr) {
+                  const dgemm::FixedScratch* fixed = nullptr) {
   gemm_plan_t plan;
   gemm_status_t st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                1, 0, &plan, allow_copy);
@@ -728,7 +773,7 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
   if (st != GEMM_OK) return st;
   // Re-plan with the device's SM count (validation above needs no device).
   st = plan_impl(dtype, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dev->sms,
-                 dev->pair_clusters, &plan, allow_copy);
+                 dev->pair_clusters, &plan, allow_copy, &dev->sgemm_caps);
   if (st != GEMM_OK) return st;
   cudaError_t e = cudaSuccess;
 
@@ -797,31 +842,40 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.ldb = kldb;
     p.C = static_cast<float*>(C);
     p.ldc = ldc;
-    const int tn = plan.splitk_slices > 1 ? 8 : sgemm_pick_tn(kM, kN, K, dev->sms);
+    // CTA pairs over K (a plan of 2 k-slices in 2-CTA clusters) run the
+    // stream-K schedule of a grid of 2 tiles (each CTA one half of a tile)
+    // with the cluster exchange, on the plan's tile configuration.
+    const bool cluster = plan.cluster_ctas > 1;
+    const int tn = plan.splitk_slices > 1 && !cluster ? 8 : sgemm_pick_tn(kM, kN, K, dev->sms);
     p.tiles_m = ceil_div(kM, dgemm::kSgemmBM);
     p.tiles_n = ceil_div(kN, plan.block_n);
     p.grid = plan.ctas;
     p.dp_tiles = plan.splitk_slices > 1 ? 0 : dgemm::sgemm_dp_tiles(plan.tiles, plan.ctas);
     p.split_tiles = plan.split_tiles;
-    p.slices = plan.splitk_slices;
+    p.slices = cluster ? 1 : plan.splitk_slices;
+    p.cluster_k = cluster ? 1 : 0;
     p.ws = nullptr;
     p.ldw = ((long long)kN + 3) / 4 * 4;
     if (p.slices > 1) {
-      st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
-      if (st != GEMM_OK) return st;
+      if (fixed != nullptr) {
+        if (plan.workspace_bytes > fixed->ws_bytes) return GEMM_ERR_SCRATCH_LIMIT;
+        p.ws = fixed->ws;
+      } else {
+        st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.ws);
+        if (st != GEMM_OK) return st;
+      }
     }
-    const bool pair_k = dgemm::sgemm_pair_k(plan.tiles, plan.ctas, p.slices) && !kop_a &&
-                        !kop_b && !swap;
-    if (p.slices == 1 && plan.split_tiles > 0 && !pair_k) {
+    if (p.slices == 1 && plan.split_tiles > 0) {
       if (plan.workspace_bytes > 0) {
+        if (fixed != nullptr) return GEMM_ERR_SCRATCH_LIMIT;   // (beta != 0: never planned)
         st = get_workspace(stream, (size_t)plan.workspace_bytes, &p.tail_ws);
         if (st != GEMM_OK) return st;
       }
       const long long words = 2ll * (plan.ctas - 1);
-      if (fixed_flags != nullptr) {
-        if (words > fixed_flags->words) return GEMM_ERR_SCRATCH_LIMIT;
-        p.sk_flags = fixed_flags->flags;
-        p.epoch = fixed_flags->epoch;
+      if (fixed != nullptr) {
+        if (words > fixed->flag_words) return GEMM_ERR_SCRATCH_LIMIT;
+        p.sk_flags = fixed->flags;
+        p.epoch = fixed->epoch;
       } else {
         float* flags = nullptr;
         st = get_workspace(stream, (size_t)words * 4, &flags, kWsFlags);
@@ -931,17 +985,11 @@ unsigned* current_fault_word() {
 }
 unsigned long long wait_bound_ns() { return wait_timeout_ns(); }
 
-gemm_status_t plan_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
-                               int ldb, const float* C, int ldc, int num_sms, gemm_plan_t* plan) {
-  return plan_impl(0, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, num_sms, 0,
-                   plan, false);
-}
-
 gemm_status_t run_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
                               int ldb, float* C, int ldc, cudaStream_t stream,
-                              const FixedFlags& flags) {
+                              const FixedScratch& scratch) {
   return run(0, GEMM_OP_N, GEMM_OP_N, M, N, K, 1.f, A, lda, B, ldb, 0.f, C, ldc, stream, false,
-             &flags);
+             &scratch);
 }
 
 bool pdl_enabled() {
@@ -1096,6 +1144,14 @@ int gemm_pair_clusters(void) {
   DeviceInfo* dev = nullptr;
   if (current_device(&dev) != GEMM_OK) return -1;
   return dev->pair_clusters;
+}
+
+int gemm_sgemm_clusters(int config, int cluster_size) {
+  if (config < 0 || config > 2 || (cluster_size != 2 && cluster_size != 4 && cluster_size != 8))
+    return -1;
+  DeviceInfo* dev = nullptr;
+  if (current_device(&dev) != GEMM_OK) return -1;
+  return dev->sgemm_caps.n[config][cluster_size == 2 ? 0 : (cluster_size == 4 ? 1 : 2)];
 }
 
 int gemm_smem_layout_offset(int layout, int row, int col) {

@@ -70,6 +70,10 @@ struct SgemmParams {
   int slices;
   float* ws;
   long long ldw;
+  // cluster_k = 1 (slices == 1, grid = 2 tiles, dp_tiles = 0): CTAs 2t and
+  // 2t + 1 compute tile t over the two halves of K as a cluster of two and
+  // add their halves in distributed shared memory; no flags, no workspace.
+  int cluster_k = 0;
   // C := alpha * (A.B) + beta * C; the old C is read only when beta != 0
   // (in split-K mode splitk_reduce applies alpha and beta; for split tiles
   // with tail_ws the fixup kernel does).
@@ -84,15 +88,6 @@ struct SgemmParams {
   unsigned* fault;   // device fault word
   unsigned long long timeout_ns;
 };
-
-// Whether an FP32 grid of row-major operands (no transposed storage) runs
-// as CTA pairs that split K: the single-wave grid of two CTAs per tile
-// (grid = 2 tiles, not split-K).  The two CTAs of a tile form a cluster
-// and combine their halves of the sum through distributed shared memory,
-// so they need neither flags nor workspace.
-__host__ __device__ inline bool sgemm_pair_k(int tiles, int grid, int slices) {
-  return slices == 1 && tiles > 0 && grid == 2 * tiles;
-}
 
 // Tile (tm, tn) of linear tile index t under grouped rasterisation: tiles
 // walk down a group of `group` tile rows before moving one tile column right.
@@ -175,6 +170,10 @@ struct TcParams {
   int slices;
   float* ws;
   long long ldw;
+  // cluster_k = 1 (slices == 1, grid = 2 tiles, dp_tiles = 0): CTAs 2t and
+  // 2t + 1 compute tile t over the two halves of K as a cluster of two and
+  // add their halves in distributed shared memory; no flags, no workspace.
+  int cluster_k = 0;
   // C := alpha * (A.B) + beta * C: the epilogue reads the old C (c_in,
   // leading dimension ldc, elements of the output type) when beta != 0.
   // Split-K units leave both to splitk_reduce.
@@ -469,25 +468,35 @@ inline int splitk_slices(int tiles, int slots, int nk) {
 unsigned* current_fault_word();
 unsigned long long wait_bound_ns();
 
-// Caller-owned flag words for the FP32 stream-K hand-over (SgemmParams::
-// sk_flags): `words` of them, written by nothing but the GEMM kernels, and
-// the launch's epoch (non-zero, new for every launch that uses them).
-struct FixedFlags {
+// Caller-owned device scratch for an FP32 call that must not allocate:
+// `flag_words` flag words for the stream-K hand-over (SgemmParams::
+// sk_flags; written by nothing but the GEMM kernels), the launch's epoch
+// (non-zero, new for every launch that uses them), and `ws_bytes` of FP32
+// split-K workspace.
+struct FixedScratch {
   unsigned* flags;
-  long long words;
+  long long flag_words;
   unsigned epoch;
+  float* ws;
+  long long ws_bytes;
 };
 
-// gemm_plan / gemm_f32 (beta = 0) that never copy an operand into library
-// scratch (an unaligned row-major operand is then staged by 4-byte
-// cp.async) and take the stream-K flags from `flags`
-// (GEMM_ERR_SCRATCH_LIMIT if too few); run_f32_no_copy allocates nothing
-// unless the plan is split-K.
-gemm_status_t plan_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
-                               int ldb, const float* C, int ldc, int num_sms, gemm_plan_t* plan);
+// gemm_f32 that allocates nothing: no operand is copied into scratch (an
+// unaligned row-major operand is staged by 4-byte cp.async) and the flags
+// and workspace come from `scratch` (GEMM_ERR_SCRATCH_LIMIT, before
+// anything is queued, if they are too small).
 gemm_status_t run_f32_no_copy(int M, int N, int K, const float* A, int lda, const float* B,
                               int ldb, float* C, int ldc, cudaStream_t stream,
-                              const FixedFlags& flags);
+                              const FixedScratch& scratch);
+
+// 2-, 4- and 8-CTA clusters of the SGEMM kernel that fit on the current
+// device at once, n[cfg][0 / 1 / 2] for s = 2 / 4 / 8, cfg 0 = narrow
+// tiles with one CTA per SM, 1 = narrow with two, 2 = wide
+// (cudaOccupancyMaxActiveClusters; 0 where the query failed).
+struct SgemmClusterCaps {
+  int n[3][3];
+};
+SgemmClusterCaps sgemm_cluster_caps();
 
 // Whether the GEMM kernels are launched as programmatic dependents of the
 // kernel before them (DENSE_GEMM_PDL=0 turns it off, for measurement).

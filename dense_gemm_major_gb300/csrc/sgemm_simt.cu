@@ -9,7 +9,7 @@ cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUten
   CUtensorMap none{};
   if (!use_tma) tmA = tmB = &none;
   if (p.op_a || p.op_b || p.c_trans) return launch_sgemm_op(p, tn, use_tma, tmA, tmB, stream);
-  if (sgemm_pair_k(p.tiles_m * p.tiles_n, p.grid, p.slices)) {
+  if (p.cluster_k) {
     if (tn == 16)
       return use_tma ? launch_cfg<true, 16, 1, false, false, false, true>(p, tmA, tmB, stream)
                      : launch_cfg<false, 16, 1, false, false, false, true>(p, tmA, tmB, stream);
@@ -27,6 +27,50 @@ cudaError_t launch_sgemm(const SgemmParams& p, int tn, bool use_tma, const CUten
                    : launch_cfg<false, 8, 1>(p, tmA, tmB, stream);
   return use_tma ? launch_cfg<true, 8, 2>(p, tmA, tmB, stream)
                  : launch_cfg<false, 8, 2>(p, tmA, tmB, stream);
+}
+
+namespace {
+
+template <bool kTma, int TN, int kMinBlocks>
+int cluster_capacity(int s) {
+  const auto kernel = sgemm_kernel<kTma, TN, kMinBlocks, false, false, false, true>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           sgemm_smem_bytes(TN)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)s);
+  cfg.blockDim = dim3(kSgemmThreads);
+  cfg.dynamicSmemBytes = sgemm_smem_bytes(TN);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)s;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
+
+}  // namespace
+
+SgemmClusterCaps sgemm_cluster_caps() {
+  // The TMA instances stand for the cp.async ones: same block and shared
+  // memory, and both keep the CTAs per SM that their launch bounds name.
+  SgemmClusterCaps c{};
+  const int sizes[3] = {2, 4, 8};
+  for (int i = 0; i < 3; ++i) {
+    c.n[0][i] = cluster_capacity<true, 8, 1>(sizes[i]);
+    c.n[1][i] = cluster_capacity<true, 8, 2>(sizes[i]);
+    c.n[2][i] = cluster_capacity<true, 16, 1>(sizes[i]);
+  }
+  return c;
 }
 
 // Host-visible copy of the A / B stage layouts, for layout checks on the CPU.

@@ -164,7 +164,8 @@ __device__ __forceinline__ void transpose4_lanes(float (&x)[4], int tr) {
 // copy complete on the same mbarrier (1 TMA arrival + 256 cp.async ones).
 // kCT: C is stored transposed (p.c_trans), a compile-time choice so that the
 // row-major instances carry no trace of it.  kPairK: the grid of two CTAs
-// per tile (sgemm_pair_k), launched as clusters of two.
+// per tile over the two halves of K (SgemmParams::cluster_k), launched as
+// clusters of two.
 template <bool kTma, int TN, int kMinBlocks, bool kTA = false, bool kTB = false, bool kCT = false,
           bool kPairK = false>
 __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)

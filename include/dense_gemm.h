@@ -119,26 +119,28 @@ gemm_status_t gemm_bf16(int M, int N, int K,
  * budget at start-up and may not allocate afterwards, or code whose latency
  * path cannot afford cudaMalloc's implicit synchronisation.  gemm_f32 needs
  * library-allocated memory only for split-K problems (few output tiles, long
- * K) and for large products with an operand TMA cannot address (re-pitched
- * into scratch); this variant runs split-K with the same kernels but keeps
- * the FP32 partial tiles in one fixed, library-wide device array of 16 MiB
- * instead, and stages an unaligned operand with cp.async in place.
+ * K) whose slices are summed through a workspace, for stream-K grids (a
+ * small array of hand-over flags) and for large products with an operand
+ * TMA cannot address (re-pitched into scratch).  This variant runs the
+ * same kernels but keeps the FP32 partial tiles in one fixed,
+ * library-wide device array of 16 MiB and the flags in another fixed
+ * array, and stages an unaligned operand with cp.async in place.
  *
- * Same arguments, conventions and results as gemm_f32.  Problems that are
- * not split-K run as gemm_f32 without operand copies (nothing allocated).
- * A split-K problem whose partial tiles need more than 16 MiB
- * (gemm_plan_t.workspace_bytes) is refused with GEMM_ERR_SCRATCH_LIMIT
- * before anything is queued.
- *  - Set-up: the first call on a device looks up the device address of the
- *    array (cudaGetSymbolAddress) and that device's SM count, with the
- *    device current; make that first call before any stream capture.
- *  - Every call on a device shares the one array and it keeps whatever the
- *    last call wrote; nothing in it needs to start at zero (each slice is
- *    fully written before it is read).  Calls whose work overlaps on the GPU
- *    (different streams, no ordering between them) race on the array:
- *    order them, e.g. keep them on one stream.
- *  - The array stays allocated on every device that has loaded it until the
- *    process exits.
+ * Same arguments, conventions and results (bit for bit: the same tiles
+ * and slices, summed in the same order) as gemm_f32.  A split-K problem
+ * whose partial tiles need more than 16 MiB (gemm_plan_t.workspace_bytes)
+ * is refused with GEMM_ERR_SCRATCH_LIMIT before anything is queued.
+ *  - Set-up: the first call on a device looks up the device addresses of
+ *    the arrays (cudaGetSymbolAddress), with the device current; make that
+ *    first call before any stream capture.
+ *  - Every call on a device shares the arrays and they keep whatever the
+ *    last call wrote; nothing in them needs to start at zero (each slice
+ *    is fully written before it is read; each call brings a new flag
+ *    value).  Calls whose work overlaps on the GPU (different streams, no
+ *    ordering between them) race on the arrays: order them, e.g. keep them
+ *    on one stream.
+ *  - The arrays stay allocated on every device that has loaded them until
+ *    the process exits.
  */
 gemm_status_t gemm_f32_noalloc(int M, int N, int K,
                                const float *A, int lda,
@@ -303,18 +305,21 @@ typedef struct gemm_plan_t {
   int split_pieces;  /* 1 when nothing is split.  FP32: 2; the piece that
                         finishes first stores its sums to C (or, with
                         beta != 0, to a workspace tile) and the second
-                        adds its own; in a grid of two CTAs per tile
-                        (ctas == 2 * tiles) the two form a cluster and
-                        combine in shared memory instead.  FP16/BF16:
+                        adds its own.  FP16/BF16:
                         2 or 4 column parts of the output tile, each over
                         the full K range; with split_in_k, 2 (the head
                         and the tail of a cut tile)                       */
   int cluster_ctas;  /* FP16/BF16: 2 when CTA pairs (tcgen05 cta_group::2)
-                        compute 256 x 256 tiles, else 1                   */
+                        compute 256 x 256 tiles, else 1.  FP32: 2 when the
+                        two k-halves of each tile (splitk_slices = 2) run
+                        as a 2-CTA cluster and add their partial tiles in
+                        distributed shared memory, else 0                 */
   int splitk_slices; /* > 1: the grid is too small for the GPU, so each tile
                         is computed as this many k-slices whose FP32 partial
                         tiles go to a workspace, summed in slice order by a
-                        second kernel                                     */
+                        second kernel (FP32 with cluster_ctas = 2: added
+                        within the cluster, no workspace and no second
+                        kernel)                                           */
   long long workspace_bytes; /* device workspace that split-K needs        */
   int pack;          /* FP32: bit 0 (A) and bit 1 (B) mark an operand
                         that is first copied by an HBM-bound kernel into
@@ -384,6 +389,11 @@ int gemm_pair_units(const gemm_plan_t *plan, int M, int N, int K, int pair, int 
  * first call on a device queries it), 0 if the query failed, -1 if there is
  * no supported device. */
 int gemm_pair_clusters(void);
+/* The same for the FP32 kernel's clusters over K: how many clusters of
+ * `cluster_size` (2, 4 or 8) CTAs of tile configuration `config` (0 narrow
+ * tiles one CTA per SM, 1 narrow two per SM, 2 wide) fit at once on the
+ * current device; -1 for bad arguments or no supported device. */
+int gemm_sgemm_clusters(int config, int cluster_size);
 
 /*
  * Shared-memory layout of the kernels' operand tiles, as an element offset

@@ -191,7 +191,6 @@ STREAMK_SHAPES = [
     (4096, 4096, 64),    # 512 tiles, 2 k-tiles: whole-tile waves + cuts at half tiles
     (4096, 4096, 32),    # 1 k-tile per tile: uneven whole-tile counts, no cuts
     (5000, 3000, 300),   # ragged in M, N and K
-    (1000, 1030, 65),    # 72 narrow tiles as 144 half-tile CTAs (grid = 2 tiles)
 ]
 
 
@@ -239,24 +238,29 @@ def test_f32_streamk_integer_exact(dg, shape, alpha, beta):
 
 @pytest.mark.parametrize("shape", [(1024, 1024, 1024),   # narrow tiles, TMA
                                    (640, 2560, 1000),    # wide tiles
-                                   (384, 2048, 4096),    # long K
+                                   (1000, 1030, 65),     # 3 k-tiles
                                    (1000, 777, 555),     # ragged; ldb = 777 staged by cp.async
                                    (1000, 1030, 777)])   # re-pitched operands
-def test_f32_pair_k_halves(dg, shape):
+def test_f32_cta_pairs_over_k(dg, shape):
     # A single wave of at most half the SMs' worth of tiles runs as two CTAs
-    # per tile, each over half of K, launched as a cluster; the halves meet
-    # in distributed shared memory (no workspace even with beta != 0).
+    # per tile, each over half of K, launched as 2-CTA clusters; the halves
+    # meet in distributed shared memory (no workspace even with beta != 0).
     # Integer entries make every sum exact; C starts as NaN, so an element
-    # neither CTA writes shows up; repeated calls give the same bits.
+    # neither CTA writes shows up; repeated calls give the same bits; a
+    # padded C keeps its padding.
     M, N, K = shape
     plan = _plan32_ex(dg, M, N, K, 0.5)
-    assert plan.splitk_slices == 1 and plan.ctas == 2 * plan.tiles and plan.split_tiles > 0
-    assert plan.workspace_bytes == 0
+    assert (plan.cluster_ctas, plan.splitk_slices) == (2, 2)
+    assert plan.ctas == 2 * plan.tiles and plan.workspace_bytes == 0
     w = workloads.Workload(f"pk{M}x{N}x{K}", "f32", M, N, K, "int", 65, -2, 2)
     A, B = workloads.make(w)
     Ad, Bd = A.cuda(), B.cuda()
-    C = run_gemm(dg, Ad, Bd)
+    Cbuf = torch.full((M, N + 3), -7.0, device="cuda")
+    C = Cbuf[:, :N]
+    C.fill_(float("nan"))
+    run_gemm(dg, Ad, Bd, C)
     compare("f32", A, B, C, exact=True, rows=workloads.sample_rows(M, 64, seed=65))
+    assert torch.all(Cbuf[:, N:] == -7.0)
     assert torch.equal(C, run_gemm(dg, Ad, Bd))
     C_in = torch.randint(-3, 4, (M, N), generator=torch.Generator().manual_seed(66)).float()
     C2 = C_in.cuda()

@@ -205,9 +205,10 @@ def test_plan_paths():
     assert ok == dg.GEMM_OK and p.path == dg.PATH_SIMT_TMA
     assert p.pack == 3 and p.pack_bytes == (1000 * 780 * 4 + 255) // 256 * 256 + 777 * 1032 * 4
     # 72 narrow tiles as two k-halves each keep 144 of the 152 SMs busy
-    # (score 0.91): no split-K; every tile is cut once, no workspace
-    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 72
-    assert (p.splitk_slices, p.ctas, p.workspace_bytes) == (1, 144, 0)
+    # (score 0.91): the halves of a tile run as a 2-CTA cluster and add in
+    # distributed shared memory (two k-slices, no workspace, no cut tiles)
+    assert p.tiles == 8 * 9 and p.block_n == 128 and p.split_tiles == 0
+    assert (p.splitk_slices, p.cluster_ctas, p.ctas, p.workspace_bytes) == (2, 2, 144, 0)
     # a smaller product with an unaligned pitch: staged in place by cp.async
     ok, p = dg.gemm_plan("f32", 700, 300, 333, FAKE, 333, FAKE + (1 << 30), 300,
                          FAKE + (2 << 30), 300)
@@ -217,15 +218,15 @@ def test_plan_paths():
     # SM for the same k-tiles per SM) into a 4 x 768 x 768 FP32 workspace
     ok, p = dg.gemm_plan("f32", 768, 768, 4096, FAKE, 4096, FAKE + (1 << 30), 768,
                          FAKE + (2 << 30), 768)
-    assert (p.tiles, p.splitk_slices, p.ctas) == (36, 4, 144)
+    assert (p.tiles, p.splitk_slices, p.cluster_ctas, p.ctas) == (36, 4, 0, 144)
     assert p.workspace_bytes == 4 * 768 * 768 * 4
     # tiny products: one k-tile per slice when the SMs allow (256^3: 4 tiles
     # x 8 slices), the split that minimises the busiest SM's k-tiles plus a
     # fixed cost per slice (512^3: 16 tiles x 9 slices)
     for (m, n, k), want in [((256, 256, 256), (4, 8)), ((512, 512, 512), (16, 9)),
-                            ((384, 384, 384), (9, 12))]:
+                            ((384, 384, 384), (9, 12)), ((256, 256, 1024), (4, 32))]:
         ok, p = dg.gemm_plan("f32", m, n, k, FAKE, k, FAKE + (1 << 30), n, FAKE + (2 << 30), n)
-        assert (p.tiles, p.splitk_slices) == want
+        assert (p.tiles, p.splitk_slices, p.cluster_ctas) == want + (0,)
     # misaligned base pointer (4-byte aligned only)
     ok, p = dg.gemm_plan("f32", 64, 64, 64, FAKE + 4, 64, FAKE + (1 << 30), 64,
                          FAKE + (2 << 30), 64)
