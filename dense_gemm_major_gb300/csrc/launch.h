@@ -54,8 +54,9 @@ struct SgemmParams {
   // alpha times its own into it; otherwise the first stores its unscaled
   // sums at tail_ws + (c - 1) * BM * BN (row-major, leading dimension BN)
   // and the second writes alpha * (sum + sum) + beta * C.  With exactly two
-  // addends the result does not depend on which piece came first.  The
-  // flags need no reset between launches: each launch brings a new epoch.
+  // addends the result does not depend on which piece came first.  Each
+  // launch brings a new epoch, and the second piece clears both words once
+  // it has seen the first's, so a replayed launch (same epoch) works too.
   int grid;
   int dp_tiles = 0;
   int split_tiles;

@@ -554,8 +554,14 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       unsigned* arrive = p.sk_flags + 2 * (cb - 1);
       if (tid == 0) {
         const bool second = atomicExch(arrive, p.epoch) == p.epoch;
-        if (second && !flag_wait_equal(arrive + 1, p.epoch, p.timeout_ns, nullptr))
-          raise_fault(p.fault, kFaultSgemmPieceWait);
+        if (second) {
+          if (!flag_wait_equal(arrive + 1, p.epoch, p.timeout_ns, nullptr))
+            raise_fault(p.fault, kFaultSgemmPieceWait);
+          // The first piece is done with both words: clear them, so that a
+          // replay of this launch (a CUDA graph, same epoch) starts afresh.
+          arrive[0] = 0u;
+          arrive[1] = 0u;
+        }
         s_second = second ? 1 : 0;
       }
       __syncthreads();
