@@ -76,8 +76,8 @@ struct SgemmParams {
   // add their halves in distributed shared memory; no flags, no workspace.
   int cluster_k = 0;
   // C := alpha * (A.B) + beta * C; the old C is read only when beta != 0
-  // (in split-K mode splitk_reduce applies alpha and beta; for split tiles
-  // with tail_ws the fixup kernel does).
+  // (in split-K mode splitk_reduce applies alpha and beta; for a cut tile
+  // the piece that completes it does).
   float alpha = 1.f, beta = 0.f;
   int c_vec4;        // C rows may be written with 16-byte stores (C and ldc
                      // 16-byte aligned; row-major C also needs N % 4 == 0,
