@@ -607,6 +607,50 @@ def test_sgemm_pack_decisions():
     assert st == dg.GEMM_OK and p.pack == 0 and p.path == dg.PATH_SIMT_MIXED
 
 
+def test_sgemm_repitch_decisions():
+    # Row-major FP32 operands whose base or leading dimension is not 16-byte
+    # aligned are copied into 16-byte-pitched scratch (plan.pack bit 0 for
+    # A, bit 1 for B; A's copy first, rounded up to 256 bytes) when
+    # M * N * K >= 2^29, and the product then runs with TMA staging; below
+    # that they are staged in place by cp.async.
+    def plan(M, N, K, lda, ldb, a_off=0, b_off=0):
+        return dg.gemm_plan("f32", M, N, K, FAKE + a_off, lda, FAKE + (1 << 36) + b_off, ldb,
+                            FAKE + (1 << 38), N, 152)[1]
+    r256 = lambda x: (x + 255) // 256 * 256
+    p = plan(1024, 1024, 1024, 1025, 1024)
+    assert (p.pack, p.path, p.pack_bytes) == (1, dg.PATH_SIMT_TMA, 1024 * 1024 * 4)   # M x K
+    p = plan(1024, 1030, 600, 600, 1030)
+    assert (p.pack, p.path, p.pack_bytes) == (2, dg.PATH_SIMT_TMA, 600 * 1032 * 4)
+    p = plan(1100, 900, 555, 555, 903)
+    assert (p.pack, p.path) == (3, dg.PATH_SIMT_TMA)
+    assert p.pack_bytes == r256(1100 * 556 * 4) + 555 * 900 * 4
+    # a base 4 bytes past a 16-byte boundary counts as unaligned as well
+    p = plan(1024, 1024, 1024, 1024, 1024, a_off=4, b_off=4)
+    assert (p.pack, p.pack_bytes) == (3, r256(1024 * 1024 * 4) + 1024 * 1024 * 4)
+    # 2^29 is the threshold: 512 x 1024 x 1024 copies, 512 x 1024 x 1020 does not
+    assert plan(512, 1024, 1024, 1025, 1024).pack == 1
+    p = plan(512, 1024, 1020, 1021, 1024)
+    assert (p.pack, p.path) == (0, dg.PATH_SIMT_CPASYNC)
+    # aligned operands are never copied
+    assert plan(4096, 4096, 4096, 4096, 4096).pack == 0
+    # a transposed operand that is packed takes its unaligned row-major
+    # partner along: A stored K x M transposed, B (ldb 2061) re-pitched
+    st, p = dg.gemm_plan_op("f32", "T", "N", 1024, 2048, 1025, 1.0, FAKE, 1024,
+                            FAKE + (1 << 36), 2061, 0.0, FAKE + (1 << 38), 2048, 152)
+    assert st == dg.GEMM_OK and (p.pack, p.path) == (3, dg.PATH_SIMT_TMA)
+    assert p.pack_bytes == r256(1024 * 1028 * 4) + r256(1025 * 2048 * 4)
+
+
+def test_sgemm_cluster_query_without_a_device():
+    # The device's cluster capacities are only known on a device: -1 here,
+    # and -1 for sizes or configurations that do not exist.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert dg.gemm_sgemm_clusters(0, 2) == -1
+    assert dg.gemm_sgemm_clusters(3, 2) == -1 and dg.gemm_sgemm_clusters(0, 3) == -1
+
+
 def test_host_entry_blocks_and_validation():
     # Row blocks: FP32 two while each block keeps a full grid of 128 x 256
     # tiles, else one; FP16 / BF16 up to four blocks of whole 256-row units.
