@@ -171,10 +171,6 @@ struct TcParams {
   int slices;
   float* ws;
   long long ldw;
-  // cluster_k = 1 (slices == 1, grid = 2 tiles, dp_tiles = 0): CTAs 2t and
-  // 2t + 1 compute tile t over the two halves of K as a cluster of two and
-  // add their halves in distributed shared memory; no flags, no workspace.
-  int cluster_k = 0;
   // C := alpha * (A.B) + beta * C: the epilogue reads the old C (c_in,
   // leading dimension ldc, elements of the output type) when beta != 0.
   // Split-K units leave both to splitk_reduce.
