@@ -1,7 +1,7 @@
 // gemm_host: the product on operands and result in host memory.  The
 // library copies them to device staging buffers it owns and overlaps the
 // copies with the computation: C is cut into row blocks, and a large FP32
-// product also into two ranges of K; while the GEMM of one block runs on
+// product also into ranges of K; while the GEMM of one block runs on
 // the caller's stream, the operands of the next go up on one side stream
 // and the finished rows of C come back on another.  Each block is an
 // ordinary gemm_*_op call on device memory (a later K range with beta = 1
@@ -20,7 +20,16 @@
 namespace {
 
 constexpr int kMaxBlocks = 4;    // row blocks
-constexpr int kMaxKBlocks = 2;   // ranges of K (FP32)
+constexpr int kMaxKBlocks = 3;   // ranges of K (FP32)
+// Ends of the ranges of K, in percent of K (rounded up to 128): a short
+// first range, so that the first kernel waits for little of A and B, each
+// later range long enough for the kernel before it to outlast its upload.
+// Measured on GB300, 4096^3 FP32 through gemm_host alone / with the FP16
+// 4096^3 problem on a second stream: ranges ending at 35 % and 100 %
+// 2.51 / 2.77 ms; 25 / 100 2.47 / 2.69; 20 / 100 2.52 / 2.77; 15 / 100
+// 2.61 / 2.83; 15 / 45 / 100 2.46 / 2.69; 10 / 35 / 100 2.44 / 2.66.
+constexpr int kKEndPct[kMaxKBlocks] = {10, 35, 100};
+constexpr int kKRanges = 3;
 constexpr int kRowAlign = 256;   // row blocks are whole CTA-pair tile rows
 
 struct HostStaging {
@@ -138,11 +147,12 @@ extern "C" int gemm_host_blocks(int dtype, int M, int N, int num_sms) {
 
 extern "C" int gemm_host_k_blocks(int dtype, int M, int N, int K) {
   // FP32 only: the partial C between ranges stays FP32, where FP16 / BF16
-  // would round it to 16 bits once more.  Two ranges (the first ~35 % of
-  // K) when the product is large enough (>= 2^36 FLOPs) for the shorter
-  // first upload to matter against the extra launches and smaller grids.
+  // would round it to 16 bits once more.  kKRanges ranges of K (ending at
+  // kKEndPct percent of K) when the product is large enough (>= 2^36
+  // FLOPs) for the shorter first upload to matter against the extra
+  // launches and smaller grids.
   if (dtype != 0 || K < 2048 || M <= 0 || N <= 0) return 1;
-  return 2.0 * M * N * K >= 68719476736.0 ? kMaxKBlocks : 1;
+  return 2.0 * M * N * K >= 68719476736.0 ? kKRanges : 1;
 }
 
 extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N,
@@ -206,11 +216,12 @@ extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, in
     return r < M ? (int)r : M;
   };
   const int nkb = reads_ab ? gemm_host_k_blocks(dtype, M, N, K) : 1;
-  // The first range of K is the shorter one: only its share of A and B
-  // has to arrive before the first kernel, and the first kernel still
-  // outlasts the upload of the rest (~0.35 K at 200 GB/s against
-  // ~64 TFLOP/s).
-  const int kfirst = nkb == 1 ? K : (int)round_up((long long)K * 35 / 100, 128);
+  // Range j of K is [kend(j - 1), kend(j)).
+  const auto kend = [&](int j) {
+    if (j >= nkb - 1) return K;
+    const long long e = round_up((long long)K * kKEndPct[j] / 100, 128);
+    return e < K ? (int)e : K;
+  };
   unsigned char* const da = static_cast<unsigned char*>(h->a);
   unsigned char* const db = static_cast<unsigned char*>(h->b);
   unsigned char* const dc = static_cast<unsigned char*>(h->c);
@@ -234,8 +245,9 @@ extern "C" gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, in
     unsigned char* c_dev = dc + (size_t)r0 * dlc * es;
     unsigned char* c_host = hc + (size_t)r0 * ldc * es;
     for (int j = 0; j < nkb; ++j) {
-      const int k0 = j == 0 ? 0 : kfirst;
-      const int kk = j == 0 ? kfirst : K - kfirst;
+      const int k0 = j == 0 ? 0 : kend(j - 1);
+      const int kk = kend(j) - k0;
+      if (j > 0 && kk <= 0) continue;   // (a range that rounding left empty)
       // B's rows k0.. (stored K x N) or columns k0.. (stored N x K), once.
       unsigned char* b_blk = op_b ? db + (size_t)k0 * es : db + (size_t)k0 * dlb * es;
       if (reads_ab && i == 0) {

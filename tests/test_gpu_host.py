@@ -199,9 +199,10 @@ def test_matmul_on_cpu_tensors_reports_a_device_fault(dg):
 
 def test_host_k_blocks_scaled_transposed(dg):
     # FP32, both operands stored transposed, alpha / beta: two row blocks x
-    # two ranges of K, the second range adding onto the first's C.
+    # three ranges of K, each later range adding onto the C the one before
+    # left.
     M, N, K = 4096, 2304, 4096
-    assert dg.gemm_host_k_blocks("f32", M, N, K) == 2
+    assert dg.gemm_host_k_blocks("f32", M, N, K) == 3
     A, B = workloads.make(workloads.Workload("host_kb", "f32", M, N, K, "uniform", 141, -2, 2))
     C_in = torch.rand((M, N), generator=torch.Generator().manual_seed(142)) * 2 - 1
     A_st, B_st = _host(A.t().contiguous(), 3), _host(B.t().contiguous(), 1)

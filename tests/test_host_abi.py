@@ -662,10 +662,10 @@ def test_host_entry_blocks_and_validation():
     assert dg.gemm_host_blocks("f16", 300, 4096, 152) == 2
     assert dg.gemm_host_blocks("f16", 256, 4096, 152) == 1
     assert dg.gemm_host_blocks("bf16", 0, 4096, 152) == 1
-    # FP32 products of >= 2^36 FLOPs with K >= 2048 also run as two ranges
-    # of K (never FP16 / BF16, whose partial C would be rounded)
-    assert dg.gemm_host_k_blocks("f32", 4096, 4096, 4096) == 2
-    assert dg.gemm_host_k_blocks("f32", 4096, 4096, 2048) == 2
+    # FP32 products of >= 2^36 FLOPs with K >= 2048 also run as three
+    # ranges of K (never FP16 / BF16, whose partial C would be rounded)
+    assert dg.gemm_host_k_blocks("f32", 4096, 4096, 4096) == 3
+    assert dg.gemm_host_k_blocks("f32", 4096, 4096, 2048) == 3
     assert dg.gemm_host_k_blocks("f32", 4096, 4096, 1024) == 1
     assert dg.gemm_host_k_blocks("f32", 2048, 2048, 2048) == 1
     assert dg.gemm_host_k_blocks("f16", 8192, 8192, 8192) == 1
