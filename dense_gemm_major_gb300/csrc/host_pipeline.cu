@@ -27,8 +27,10 @@ constexpr int kMaxKBlocks = 3;   // ranges of K (FP32)
 // Measured on GB300, 4096^3 FP32 through gemm_host alone / with the FP16
 // 4096^3 problem on a second stream: ranges ending at 35 % and 100 %
 // 2.51 / 2.77 ms; 25 / 100 2.47 / 2.69; 20 / 100 2.52 / 2.77; 15 / 100
-// 2.61 / 2.83; 15 / 45 / 100 2.46 / 2.69; 10 / 35 / 100 2.44 / 2.66.
-constexpr int kKEndPct[kMaxKBlocks] = {10, 35, 100};
+// 2.61 / 2.83; 15 / 45 / 100 2.46 / 2.69; 10 / 35 / 100 2.44 / 2.66-2.69;
+// 8 / 30 / 100 2.43 / 2.62-2.67; 10 / 30 / 100 2.45 / 2.65-2.67;
+// 12 / 40 / 100 2.43 / 2.61-2.63.
+constexpr int kKEndPct[kMaxKBlocks] = {12, 40, 100};
 constexpr int kKRanges = 3;
 constexpr int kRowAlign = 256;   // row blocks are whole CTA-pair tile rows
 

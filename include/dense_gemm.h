@@ -258,9 +258,9 @@ gemm_status_t gemm_host(int dtype, gemm_op_t op_a, gemm_op_t op_b, int M, int N,
  * (1, 2 or 4; blocks are multiples of 256 rows). */
 int gemm_host_blocks(int dtype, int M, int N, int num_sms);
 /* Ranges of K each row block of an FP32 gemm_host product runs as (1 or 3;
- * ending at ~10 % and ~35 % of K, multiples of 128, and at K): each later
+ * ending at ~12 % and ~40 % of K, multiples of 128, and at K): each later
  * range is a gemm_f32_op call with beta = 1 on the C the one before left,
- * so the upload before the first kernel is about a tenth as large. */
+ * so the upload before the first kernel is about an eighth as large. */
 int gemm_host_k_blocks(int dtype, int M, int N, int K);
 
 /* Static, never-null description of a status code. */
