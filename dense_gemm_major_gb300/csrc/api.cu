@@ -924,9 +924,12 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
              : encode_2d(&tmB, dt, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb * 2, 64,
                          plan.cluster_ctas == 2 ? dgemm::kTc2BK : dgemm::kTcBK,
                          CU_TENSOR_MAP_SWIZZLE_128B);
+    // C up to the last whole 16-byte granule of a row; the kernels write the
+    // ragged tail (N % 8 columns) with plain stores.
+    const int n_tma = N & ~7;
     if (!enc_a || !enc_b ||
-        !encode_2d(&tmC, dt, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * 2, dgemm::kTcEpiCols,
-                   32, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_2d(&tmC, dt, C, (uint64_t)(n_tma > 0 ? n_tma : N), (uint64_t)M,
+                   (uint64_t)ldc * 2, dgemm::kTcEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_128B))
       return GEMM_ERR_LAUNCH;
     dgemm::TcParams p;
     p.M = M;
@@ -944,7 +947,9 @@ gemm_status_t run(int dtype, int op_a, int op_b, int M, int N, int K, float alph
     p.alpha = alpha;
     p.beta = beta;
     p.c_in = C;
+    p.c_out = C;
     p.ldc = ldc;
+    p.n_tma = n_tma;
     p.fault = dev->fault;
     p.timeout_ns = wait_timeout_ns();
     if (plan.cluster_ctas == 2 && plan.split_in_k) {

@@ -289,9 +289,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
                                   ((ch ^ (lane & 7)) << 4)) = v;
       }
+      store_tail_row(reinterpret_cast<const unsigned char*>(row), lane, p.c_out, p.ldc, p.M, p.N,
+                     p.n_tma, tm * BM + q * 32 + lane, tn * BN + col);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && p.n_tma > 0) {
         tma_store_2d(&tmC, smem_u32(buf), tn * BN + col, tm * BM + q * 32);
         tma_store_commit();
       }

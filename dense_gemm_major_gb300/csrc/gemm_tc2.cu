@@ -406,9 +406,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(row) +
                                     ((ch ^ (lane & 7)) << 4)) = v;
         }
+        store_tail_row(reinterpret_cast<const unsigned char*>(row), lane, p.c_out, p.ldc, p.M,
+                       p.N, p.n_tma, row0 + lane, w.tn * BN + w.n_off + c * kTcEpiCols);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && p.n_tma > 0) {
           tma_store_2d(&tmC, smem_u32(buf), w.tn * BN + w.n_off + c * kTcEpiCols, row0);
           tma_store_commit();
         }

@@ -177,6 +177,13 @@ struct TcParams {
   float alpha = 1.f, beta = 0.f;
   const void* c_in = nullptr;
   long long ldc;
+  // C's columns [0, n_tma) go out through TMA stores (tmC's inner extent is
+  // n_tma: N rounded down to a multiple of 8 elements, since a TMA store
+  // whose clipped edge falls inside a 16-byte granule writes the whole
+  // granule); the ragged tail [n_tma, N) through plain 2-byte stores to
+  // c_out.  n_tma == 0 (N < 8): no TMA stores at all.
+  int n_tma = 0;
+  void* c_out = nullptr;
   // Work units: tiles [0, full_tiles) whole (128 x 256); each later tile
   // as `parts` consecutive units of 128 x (256 / parts) columns, each over
   // the full K range.

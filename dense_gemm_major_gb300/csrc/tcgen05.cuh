@@ -220,6 +220,25 @@ __device__ __forceinline__ void scale_row64(uint32_t (&r0)[32], uint32_t (&r1)[3
   }
 }
 
+// The ragged tail of C, columns [n_tma, N) (fewer than 8; n_tma a multiple
+// of 8), that the TMA store of a 64-column box leaves out: read back from
+// this lane's staged row (128-byte swizzled, 16-byte chunk ch at
+// (ch ^ (lane & 7)) * 16) and written with 2-byte stores.  `col` is the
+// box's first global column (a multiple of 64); only the box holding
+// column n_tma, and rows below M, write anything.
+__device__ __forceinline__ void store_tail_row(const unsigned char* staged_row, int lane,
+                                               void* c_out, long long ldc, int M, int N,
+                                               int n_tma, int row, int col) {
+  if (n_tma == N || n_tma < col || n_tma >= col + 64 || row >= M) return;
+  const int ch = (n_tma - col) >> 3;
+  const uint4 v = *reinterpret_cast<const uint4*>(staged_row + ((ch ^ (lane & 7)) << 4));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unsigned short* dst = static_cast<unsigned short*>(c_out) + (long long)row * ldc + n_tma;
+#pragma unroll
+  for (int e = 0; e < 7; ++e)
+    if (n_tma + e < N) dst[e] = (unsigned short)(w[e >> 1] >> (16 * (e & 1)));
+}
+
 // ------------------------------------------------------------ CTA pairs
 
 // 2-CTA (cta_group::2) forms: one thread of the even CTA of a cluster pair

@@ -90,6 +90,47 @@ def test_tc_padded_leading_dimensions(dg, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("shape,cluster", [((300, 263, 200), 1), ((52, 49, 191), 2),
+                                           ((315, 37, 9), 1), ((128, 2, 12), 2),
+                                           ((2095, 6, 329), 1), ((1300, 1201, 1500), 2),
+                                           ((3000, 2999, 4096), 2)])
+@pytest.mark.parametrize("beta", [0.0, -0.5])
+def test_tc_ragged_n_leaves_c_padding(dg, dtype, shape, cluster, beta):
+    """N % 8 != 0: the last 16-byte granule of each C row is only partly
+    inside N, so the columns past N (up to the padded row's end) must come
+    through untouched, by either kernel and with or without beta."""
+    M, N, K = shape
+    ldc = (N + 7) // 8 * 8 + 8
+    ldb = (N + 7) // 8 * 8
+    plan = dg.gemm_plan_op(dtype, "N", "N", M, N, K, 1.5, 1 << 40, (K + 7) // 8 * 8, 2 << 40,
+                           ldb, beta, 3 << 40, ldc,
+                           torch.cuda.get_device_properties(0).multi_processor_count)[1]
+    assert plan.cluster_ctas == cluster and plan.splitk_slices == 1
+    w = workloads.Workload("ragged_n", dtype, M, N, K, "int", 88, -2, 2)
+    A, B = workloads.make(w)
+    Ad = padded(A, (K + 7) // 8 * 8 - K)
+    Bd = padded(B, ldb - N)
+    Cbuf = torch.full((M, ldc), -3.0, dtype=A.dtype, device="cuda")
+    C = Cbuf[:, :N]
+    C_in = torch.randint(-3, 4, (M, N), generator=torch.Generator().manual_seed(7)).to(A.dtype)
+    C.copy_(C_in.cuda())
+    st = dg.gemm_op(dtype, "N", "N", M, N, K, 1.5, Ad.data_ptr(), Ad.stride(0), Bd.data_ptr(),
+                    ldb, beta, C.data_ptr(), ldc, torch.cuda.current_stream().cuda_stream)
+    assert st == dg.GEMM_OK, dg.status_string(st)
+    check_device(dg)
+    assert torch.all(Cbuf[:, N:] == -3.0), "padding columns of C were written"
+    rows = None if M * N * K <= 2e8 else workloads.sample_rows(M, 48, seed=3)
+    ref, _ = oracle.gemm_scaled(dtype, 1.5, workloads.to_numpy_bits(A), workloads.to_numpy_bits(B),
+                                beta, workloads.to_numpy_bits(C_in), rows=rows)
+    got = C.float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[np.asarray(rows)]
+    # integer inputs: sums exact in FP32, 1.5 and -0.5 exact scalings, so the
+    # one rounding (FP32 -> the output type) is the oracle's too
+    np.testing.assert_array_equal(got, oracle.decode(dtype, oracle.round_rn(dtype, ref)))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_tc_misaligned_is_refused(dg, dtype):
     td = workloads.TORCH_DTYPES[dtype]
     A = torch.zeros(64, 60, dtype=td, device="cuda")     # lda = 60: 120-byte pitch
