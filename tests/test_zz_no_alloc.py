@@ -96,3 +96,68 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     assert _run(dg, dg.gemm_f32_noalloc, A, B, C) == dg.GEMM_ERR_SCRATCH_LIMIT
     check_device(dg)
     assert torch.all(C == 5.0)
+
+
+def _stored(X, pad, offset):
+    """X on the GPU as a row-padded view, optionally one element past a
+    16-byte boundary (so TMA cannot stage it and gemm_f32 may re-pitch)."""
+    rows, cols = X.shape
+    ld = cols + pad
+    o = 1 if offset else 0
+    buf = torch.full((rows * ld + o,), float("nan"), device="cuda")
+    view = buf[o:].view(rows, ld)[:, :cols]
+    view.copy_(X.cuda())
+    return view, ld
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_noalloc_random_shapes_match_gemm_f32(seed):
+    # Seeded shapes, paddings and base offsets: gemm_f32 re-pitches large
+    # unaligned operands into scratch and stages the rest by TMA, the entry
+    # always stages them in place; the tiles, slices and summation order are
+    # the same, so the bits are too.  Split-K beyond the fixed array is
+    # refused before anything is queued.
+    import numpy as np
+    import oracle
+    dg = gpu_lib()
+    rng = np.random.default_rng(7000 + seed)
+    size = lambda: int(rng.choice([rng.integers(1, 64), rng.integers(64, 900),
+                                   rng.integers(900, 3000)]))
+    M, N, K = size(), size(), size()
+    if seed % 4 == 0:
+        K = int(rng.integers(4000, 30000))          # long K: split-K candidates
+        M, N = int(rng.integers(1, 600)), int(rng.integers(1, 600))
+    pad_a, pad_b, pad_c = (int(x) for x in rng.integers(0, 4, 3))
+    off_a, off_b = bool(rng.random() < 0.5), bool(rng.random() < 0.5)
+    w = workloads.Workload(f"noalloc_rand{seed}", "f32", M, N, K, "uniform", 7100 + seed)
+    A_cpu, B_cpu = workloads.make(w)
+    A, lda = _stored(A_cpu, pad_a, off_a)
+    B, ldb = _stored(B_cpu, pad_b, off_b)
+    ldc = N + pad_c
+    ref_buf = torch.full((M, ldc), -7.0, device="cuda")
+    out_buf = torch.full((M, ldc), -7.0, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert dg.gemm_f32(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, ref_buf.data_ptr(), ldc,
+                       s) == dg.GEMM_OK
+    check_device(dg)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, plan = dg.gemm_plan("f32", M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb,
+                           out_buf.data_ptr(), ldc, sms)
+    st = dg.gemm_f32_noalloc(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out_buf.data_ptr(),
+                             ldc, s)
+    if plan.splitk_slices > 1 and plan.cluster_ctas <= 1 and plan.workspace_bytes > SCRATCH_BYTES:
+        assert st == dg.GEMM_ERR_SCRATCH_LIMIT
+        assert torch.all(out_buf == -7.0)
+        return
+    assert st == dg.GEMM_OK, (dg.status_string(st), M, N, K)
+    check_device(dg)
+    assert torch.equal(out_buf, ref_buf), (M, N, K, lda, ldb, ldc, plan.pack)
+    assert torch.all(out_buf[:, N:] == -7.0)
+    rows = None if M * N * K <= 2e8 else workloads.sample_rows(M, 48, seed=seed)
+    ref, S = oracle.gemm("f32", workloads.to_numpy_bits(A_cpu), workloads.to_numpy_bits(B_cpu),
+                         rows=rows)
+    got = out_buf[:, :N].cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[np.asarray(rows)]
+    err, idx, bad_zero = oracle.normalized_error(got, ref, S)
+    assert bad_zero == 0 and err <= 1e-5, (err, idx, M, N, K)
