@@ -35,8 +35,8 @@
 //    TMA).  Here: a 3- or 4-stage ring filled by TMA (one thread issues both
 //    tile copies, completion on an mbarrier) or, when a base or leading
 //    dimension is not 16-byte aligned, by 4-byte cp.async with zero fill
-//    completing on the same mbarrier.  One __syncthreads per 32-deep k-tile
-//    releases a slot.
+//    completing on the same mbarrier.  One __syncthreads per two 32-deep
+//    k-tiles releases two slots.
 //  * Hybrid stream-K tile scheduling (see the unit loop below) instead of one
 //    tile per CTA: full waves of whole tiles, then an equal share of the
 //    remaining (tile, k-tile) iterations per CTA.
@@ -451,9 +451,15 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           }
         }
       }
-      // Every thread is done with slot s (or some thread gave up).
-      if (__syncthreads_or(!ok)) break;
-      if (kt + S < nk) issue(kt + S, s);
+      // Slots are released two k-tiles at a time (one barrier per 64 of
+      // K): after an odd k-tile every thread is done with this slot and the
+      // one before it, whose k-tiles + S are staged now; the last k-tile
+      // ends with a barrier too (or some thread gave up).
+      if ((kt & 1) || kt + 1 == nk) {
+        if (__syncthreads_or(!ok || *(volatile int*)&s_abort)) break;
+        if ((kt & 1) && kt - 1 + S < nk) issue(kt - 1 + S, (g0 + kt - 1) % S);
+        if ((kt & 1) && kt + S < nk) issue(kt + S, s);
+      }
     }
 
     if (kt < nk) {
@@ -463,8 +469,11 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       if constexpr (kAnyCp) cp_async_wait_all();
       if constexpr (kTma) {
         if (tid == 0) {
-          const int issued = (kt + S < nk) ? kt + S : nk;
-          for (int t = kt; t < issued; ++t) {
+          // The last release point followed k-tile kt - 1 - (kt & 1) and
+          // staged up to that + S; every k-tile from kt & ~1 on may still be
+          // in flight.
+          const int issued = kt - (kt & 1) + S < nk ? kt - (kt & 1) + S : nk;
+          for (int t = kt & ~1; t < issued; ++t) {
             if (!mbar_wait_bounded(smem_u32(&full[(g0 + t) % S]), (uint32_t)(((g0 + t) / S) & 1),
                                    p.timeout_ns, nullptr)) {
               raise_fault(p.fault, kFaultDrainWait);
