@@ -35,8 +35,9 @@
 //    TMA).  Here: a 3- or 4-stage ring filled by TMA (one thread issues both
 //    tile copies, completion on an mbarrier) or, when a base or leading
 //    dimension is not 16-byte aligned, by 4-byte cp.async with zero fill
-//    completing on the same mbarrier.  One __syncthreads per two 32-deep
-//    k-tiles releases two slots.
+//    completing on the same mbarrier.  One __syncthreads per S - 1 32-deep
+//    k-tiles releases S - 1 slots (three of the wide tile's four, two of the
+//    narrow tile's three).
 //  * Hybrid stream-K tile scheduling (see the unit loop below) instead of one
 //    tile per CTA: full waves of whole tiles, then an equal share of the
 //    remaining (tile, k-tile) iterations per CTA.
@@ -179,6 +180,8 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   constexpr uint32_t kBarCount = (kTma ? 1u : 0u) + (kAnyCp ? (uint32_t)kSgemmThreads : 0u);
   constexpr int BN = sgemm_bn(TN);
   constexpr int S = sgemm_stages(TN);
+  constexpr int kRelease = S - 1;   // k-tiles per ring release (see the k-loop)
+  static_assert(kRelease >= 2, "the ring has at least three stages");
   constexpr int kBStageFloats = BK * BN;
   constexpr int NH = TN / 4;   // 16-byte column groups per thread
 
@@ -451,14 +454,19 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
           }
         }
       }
-      // Slots are released two k-tiles at a time (one barrier per 64 of
-      // K): after an odd k-tile every thread is done with this slot and the
-      // one before it, whose k-tiles + S are staged now; the last k-tile
-      // ends with a barrier too (or some thread gave up).
-      if ((kt & 1) || kt + 1 == nk) {
+      // Slots are released kRelease = S - 1 k-tiles at a time (one
+      // barrier per kRelease k-tiles, at least one k-tile always in flight):
+      // at the end of each group every thread is done with the group's
+      // slots, whose k-tiles + S are staged now; the last k-tile ends with
+      // a barrier too (or some thread gave up).
+      const bool group_end = (kt + 1) % kRelease == 0;
+      if (group_end || kt + 1 == nk) {
         if (__syncthreads_or(!ok || *(volatile int*)&s_abort)) break;
-        if ((kt & 1) && kt - 1 + S < nk) issue(kt - 1 + S, (g0 + kt - 1) % S);
-        if ((kt & 1) && kt + S < nk) issue(kt + S, s);
+        if (group_end) {
+  #pragma unroll
+          for (int r = kRelease - 1; r >= 0; --r)
+            if (kt - r + S < nk) issue(kt - r + S, (g0 + kt - r) % S);
+        }
       }
     }
 
@@ -469,11 +477,12 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
       if constexpr (kAnyCp) cp_async_wait_all();
       if constexpr (kTma) {
         if (tid == 0) {
-          // The last release point followed k-tile kt - 1 - (kt & 1) and
-          // staged up to that + S; every k-tile from kt & ~1 on may still be
-          // in flight.
-          const int issued = kt - (kt & 1) + S < nk ? kt - (kt & 1) + S : nk;
-          for (int t = kt & ~1; t < issued; ++t) {
+          // The last release point followed k-tile `from` - 1 (the start
+          // of kt's group) and staged up to that + S; every k-tile from
+          // `from` on may still be in flight.
+          const int from = kt / kRelease * kRelease;
+          const int issued = from + S < nk ? from + S : nk;
+          for (int t = from; t < issued; ++t) {
             if (!mbar_wait_bounded(smem_u32(&full[(g0 + t) % S]), (uint32_t)(((g0 + t) / S) & 1),
                                    p.timeout_ns, nullptr)) {
               raise_fault(p.fault, kFaultDrainWait);
