@@ -480,10 +480,10 @@ gemm_status_t plan_sgemm(int M, int N, int K, int op_a, int op_b, bool a16, bool
   plan->block_m = dgemm::kSgemmBM;
   plan->block_n = dgemm::sgemm_bn(tcfg);
   plan->block_k = dgemm::kSgemmBK;
-  plan->stages = dgemm::sgemm_stages(tcfg);
+  plan->stages = dgemm::sgemm_stages(tn);
   plan->threads = dgemm::kSgemmThreads;
   plan->tiles = ceil_div(M, dgemm::kSgemmBM) * ceil_div(N, plan->block_n);
-  plan->smem_bytes = dgemm::sgemm_smem_bytes(tcfg);
+  plan->smem_bytes = dgemm::sgemm_smem_bytes(tn);
   // Wave quantisation: with more tiles than resident CTAs the grid is
   // one CTA per slot; all full waves but the last one or two run as whole
   // tiles, and each CTA takes an equal share of the remaining tiles'

@@ -22,11 +22,17 @@ constexpr int kSgemmBK = 32;
 constexpr int kSgemmThreads = 256;
 constexpr int kSgemmGroupM = 16;   // tile rows per rasterisation group (L2 reuse)
 constexpr int sgemm_bn(int tn) { return 16 * tn; }
-constexpr int sgemm_stages(int tn) { return tn == 8 ? 3 : 4; }
+// Ring stages of tile configuration tn: 16 = wide (one CTA per SM), 8 =
+// narrow with two CTAs per SM, 9 = narrow with one, which has the wide
+// configuration's shared memory and so twice the stages of 8.
+constexpr int sgemm_stages(int tn) { return tn == 8 ? 3 : (tn == 9 ? 6 : 4); }
 constexpr int sgemm_smem_bytes(int tn) {
-  return sgemm_stages(tn) * (kSgemmBM * kSgemmBK + kSgemmBK * sgemm_bn(tn)) * 4 + 1024 /*align*/ +
-         64 /*barriers*/;
+  return sgemm_stages(tn) * (kSgemmBM * kSgemmBK + kSgemmBK * sgemm_bn(tn == 9 ? 8 : tn)) * 4 +
+         1024 /*align*/ + 64 /*barriers*/;
 }
+// The tile configuration of a kernel instance: TN outputs per thread row,
+// kMinBlocks CTAs per SM.
+constexpr int sgemm_cfg(int tn, int min_blocks) { return tn == 8 && min_blocks == 1 ? 9 : tn; }
 
 struct SgemmParams {
   int M, N, K;

@@ -34,15 +34,16 @@ namespace {
 template <bool kTma, int TN, int kMinBlocks>
 int cluster_capacity(int s) {
   const auto kernel = sgemm_kernel<kTma, TN, kMinBlocks, false, false, false, true>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           sgemm_smem_bytes(TN)) != cudaSuccess) {
+  constexpr int kSmem = sgemm_smem_bytes(sgemm_cfg(TN, kMinBlocks));
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)s);
   cfg.blockDim = dim3(kSgemmThreads);
-  cfg.dynamicSmemBytes = sgemm_smem_bytes(TN);
+  cfg.dynamicSmemBytes = kSmem;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = (unsigned)s;

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kSgemmThreads, kMinBlocks)
   constexpr bool kAnyCp = kCpA || kCpB;
   constexpr uint32_t kBarCount = (kTma ? 1u : 0u) + (kAnyCp ? (uint32_t)kSgemmThreads : 0u);
   constexpr int BN = sgemm_bn(TN);
-  constexpr int S = sgemm_stages(TN);
+  constexpr int S = sgemm_stages(sgemm_cfg(TN, kMinBlocks));
   constexpr int kRelease = S - 1;   // k-tiles per ring release (see the k-loop)
   static_assert(kRelease >= 2, "the ring has at least three stages");
   constexpr int kBStageFloats = BK * BN;
@@ -785,14 +785,14 @@ cudaError_t launch_cfg(const SgemmParams& p, const CUtensorMap* tmA, const CUten
   // The attribute is per function; setting it on every call is cheap and
   // keeps this correct for every device of the process.
   const auto kernel = sgemm_kernel<kTma, TN, kMinBlocks, kTA, kTB, kCT, kPairK>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       sgemm_smem_bytes(TN));
+  constexpr int kSmem = sgemm_smem_bytes(sgemm_cfg(TN, kMinBlocks));
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int tiles = p.tiles_m * p.tiles_n;
   // Stream-K: G = p.grid CTAs (<= tiles); p.split_tiles tiles are cut in two.
   const int G = p.slices > 1 ? tiles * p.slices : p.grid;
   return launch_gemm_kernel_clusters(kPairK ? 2u : 1u, kernel, dim3(G), dim3(kSgemmThreads),
-                                     sgemm_smem_bytes(TN), stream, *tmA, *tmB, p);
+                                     kSmem, stream, *tmA, *tmB, p);
 }
 
 }  // namespace

@@ -190,12 +190,13 @@ def test_plan_paths():
     # beats 1.00 x 128/152)
     ok, p = dg.gemm_plan("f32", 2048, 2048, 2048, FAKE, 2048, FAKE + (1 << 30), 2048,
                          FAKE + (2 << 30), 2048, num_sms=152)
-    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles, p.ctas) == (128, 3, 256, 152)
+    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles, p.ctas) == (128, 6, 256, 152)
     assert p.split_tiles == _streamk_cuts(256, 64, 152)
     # at most one narrow tile per SM: the narrow 128 x 128 configuration
+    # with one CTA per SM (six stages)
     ok, p = dg.gemm_plan("f32", 1024, 1024, 512, FAKE, 512, FAKE + (1 << 30), 1024,
                          FAKE + (2 << 30), 1024, num_sms=152)
-    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles) == (128, 3, 64)
+    assert ok == dg.GEMM_OK and (p.block_n, p.stages, p.tiles) == (128, 6, 64)
     # lda = 777 and ldb = 1030 floats are not 16-byte pitches: with
     # 8.0e8 >= 2^29 multiply-adds both operands are first re-pitched into
     # scratch (A's copy, 1000 x 780 floats, rounded up to 256 bytes, then
