@@ -105,7 +105,6 @@ __device__ __forceinline__ Unit unit_of(int u, const TcParams& p, int nk) {
   return w;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
 // A single thread's bounded wait (the MMA issuer's): spins on the barrier;
 // on giving up records the fault (once per CTA) and raises the abort flag.
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const TcParams& p,
@@ -116,6 +115,7 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, const
   return false;
 }
 
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcParams& p,
                                           Barriers* bars, unsigned fault_code) {
   const int lane = threadIdx.x & 31;

@@ -32,12 +32,12 @@
 //    every issue slot of an SM sub-partition to reach the FFMA peak.
 //  * A multi-stage pipeline (wingedge777 section 6 double buffer; m.lqnn.cn v4
 //    cp.async double buffer; m.nxbn.cn section 3.1-3.2 three or four stages and
-//    TMA).  Here: a 3- or 4-stage ring filled by TMA (one thread issues both
+//    TMA).  Here: a 3-, 4- or 6-stage ring filled by TMA (one thread issues both
 //    tile copies, completion on an mbarrier) or, when a base or leading
 //    dimension is not 16-byte aligned, by 4-byte cp.async with zero fill
 //    completing on the same mbarrier.  One __syncthreads per S - 1 32-deep
-//    k-tiles releases S - 1 slots (three of the wide tile's four, two of the
-//    narrow tile's three).
+//    k-tiles releases S - 1 slots (three of the wide tile's four; five of
+//    six, or two of three, for the narrow tile at one or two CTAs per SM).
 //  * Hybrid stream-K tile scheduling (see the unit loop below) instead of one
 //    tile per CTA: full waves of whole tiles, then an equal share of the
 //    remaining (tile, k-tile) iterations per CTA.
