@@ -373,8 +373,9 @@ int forced_sgemm_tn() {
 // with two.  Picks the largest (speed relative to wide) x (share of the CTA
 // slots busy): a grid of more tiles than slots is balanced by stream-K
 // (share 1), a smaller one fills tiles / slots (twice that when it runs as
-// two k-halves per tile).  Relative speeds measured on GB300 at 4096^3 and
-// 8192 x 8192 x 4096: wide 1.00, narrow/1 0.96, narrow/2 0.95.
+// two k-halves per tile).  Relative speeds measured on GB300 at 4096^3,
+// 8192 x 8192 x 4096 and 6144 x 6144 x 2048: wide 1.00, narrow/1 0.93,
+// narrow/2 0.92.
 int sgemm_pick_tn(int M, int N, int K, int sms, double* score_out = nullptr) {
   if (score_out != nullptr) *score_out = 1.0;
   if (const int forced = forced_sgemm_tn()) return forced;
@@ -383,7 +384,7 @@ int sgemm_pick_tn(int M, int N, int K, int sms, double* score_out = nullptr) {
     int tn, per_sm;
     double speed;
   };
-  const Cfg cfgs[3] = {{16, 1, 1.00}, {9, 1, 0.96}, {8, 2, 0.95}};
+  const Cfg cfgs[3] = {{16, 1, 1.00}, {9, 1, 0.93}, {8, 2, 0.92}};
   int best = 16;
   double best_score = -1.0;
   for (const Cfg& c : cfgs) {

@@ -186,7 +186,7 @@ def test_plan_paths():
     assert (p.tiles, p.splitk_slices, p.ctas) == (4, 32, 128)
     assert p.workspace_bytes == 32 * 256 * 256 * 4
     # 2048^3: 128 wide tiles would leave 24 SMs idle; 256 narrow tiles with
-    # one CTA per SM are balanced by stream-K over all 152 (speed 0.96 x 1
+    # one CTA per SM are balanced by stream-K over all 152 (speed 0.93 x 1
     # beats 1.00 x 128/152)
     ok, p = dg.gemm_plan("f32", 2048, 2048, 2048, FAKE, 2048, FAKE + (1 << 30), 2048,
                          FAKE + (2 << 30), 2048, num_sms=152)
